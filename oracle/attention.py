@@ -1,0 +1,308 @@
+"""Float64 CPU definitions of exact attention and of the (m, d, o) state.
+
+Test infrastructure only (see the package docstring): plain, slow and written
+to be checked against the pages by eye.  No tiling, fusion or reordering
+beyond what each definition states; NumPy's matmul serves as the dot-product
+step.
+
+Page: "Learning FlashAttention the Hard Way - Part 1" (cloudrift.ai).
+"""
+from __future__ import annotations
+
+import math
+from typing import Sequence
+
+import numpy as np
+
+LOG2E = 1.0 / math.log(2.0)
+LN2 = math.log(2.0)
+
+
+def to_f64(x) -> np.ndarray:
+    """Exact conversion of a (torch or NumPy) bf16/fp32 tensor to float64."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            return x.detach().to("cpu").to(torch.float64).numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.asarray(x, dtype=np.float64)
+
+
+# ---------------------------------------------------------------------------
+# Dense attention: the plain definition.
+# Section "FlashAttention: Not So Special": S = Q K^T, P = softmax(S) row-wise,
+# O = P V, with S never needed by the tiled method but materialised here.
+# Section "Softmax Looks Like It Breaks the Rules": the safe softmax subtracts
+# the row maximum m before exponentiating and divides by d = sum_j e^{s_j - m}.
+# ---------------------------------------------------------------------------
+
+def scores(q: np.ndarray, k: np.ndarray, scale: float) -> np.ndarray:
+    """S = (Q K^T) * scale for one head: q [Nq, D], k [Nk, D] -> [Nq, Nk]."""
+    return (q @ k.T) * float(scale)
+
+
+def causal_mask(s: np.ndarray, q_pos: np.ndarray, k_pos: np.ndarray) -> np.ndarray:
+    """Key j is hidden from query i when j > i (positions within a sequence)."""
+    s = s.copy()
+    s[k_pos[None, :] > q_pos[:, None]] = -np.inf
+    return s
+
+
+def safe_softmax_stats(s: np.ndarray):
+    """Row maximum m, shifted weights e^{s - m} and their sum d (three passes:
+    max, sum, divide - the last one left to the caller).  A row whose entries
+    are all -inf has no maximum; it gets m = -inf, weights 0, d = 0."""
+    m = s.max(axis=-1)
+    m_safe = np.where(np.isfinite(m), m, 0.0)
+    w = np.exp(s - m_safe[..., None])
+    d = w.sum(axis=-1)
+    return m, w, d
+
+
+def softmax_ref(s: np.ndarray) -> np.ndarray:
+    """Row-wise safe softmax P = e^{s - m} / d."""
+    _, w, d = safe_softmax_stats(s)
+    return w / d[..., None]
+
+
+def attention_head_ref(q, k, v, scale, causal, rows=None):
+    """One head.  q [Nq, D], k/v [Nk, D] float64; Nq == Nk when causal.
+    Returns O [R, D] and LSE [R] (natural log) for the query rows ``rows``
+    (all rows when None).  A fully masked row gives O = 0 and LSE = -inf."""
+    nq = q.shape[0]
+    rows = np.arange(nq) if rows is None else np.asarray(rows, dtype=np.int64)
+    s = scores(q[rows], k, scale)
+    if causal:
+        s = causal_mask(s, rows, np.arange(k.shape[0]))
+    m, w, d = safe_softmax_stats(s)
+    num = w @ v
+    with np.errstate(invalid="ignore", divide="ignore"):
+        o = np.where(d[:, None] > 0, num / np.where(d > 0, d, 1.0)[:, None], 0.0)
+        lse = np.where(d > 0, m + np.log(np.where(d > 0, d, 1.0)), -np.inf)
+    return o, lse
+
+
+def attention_ref(q, k, v, scale, causal, rows=None):
+    """Dense [B, H, N, D] inputs (any dtype, converted exactly to float64).
+    Returns O [B, H, R, D] and LSE [B, H, R] in float64, looping over heads so
+    that at most one head's score matrix is held at a time."""
+    q, k, v = to_f64(q), to_f64(k), to_f64(v)
+    B, H, N, D = q.shape
+    R = N if rows is None else len(rows)
+    O = np.zeros((B, H, R, D))
+    L = np.zeros((B, H, R))
+    for b in range(B):
+        for h in range(H):
+            O[b, h], L[b, h] = attention_head_ref(q[b, h], k[b, h], v[b, h],
+                                                  scale, causal, rows)
+    return O, L
+
+
+def varlen_ref(q, k, v, cu_seqlens, scale, causal, seqs=None, rows=None):
+    """Packed [T, H, D] inputs with sequence i on tokens
+    [cu_seqlens[i], cu_seqlens[i+1]).  Each sequence is its own dense
+    attention (positions restart at 0).  Returns {seq: (O [L', H, D],
+    LSE [H, L'])} for the chosen sequences (all by default) and query rows
+    (local indices, all by default)."""
+    q, k, v = to_f64(q), to_f64(k), to_f64(v)
+    cu = [int(x) for x in np.asarray(cu_seqlens).tolist()]
+    seqs = range(len(cu) - 1) if seqs is None else seqs
+    H = q.shape[1]
+    out = {}
+    for i in seqs:
+        a, b = cu[i], cu[i + 1]
+        Ls = b - a
+        r = np.arange(Ls) if rows is None else np.asarray(
+            [x for x in rows if x < Ls], dtype=np.int64)
+        O = np.zeros((len(r), H, q.shape[2]))
+        LSE = np.zeros((H, len(r)))
+        for h in range(H):
+            o, l = attention_head_ref(q[a:b, h], k[a:b, h], v[a:b, h], scale,
+                                      causal, r)
+            O[:, h], LSE[h] = o, l
+        out[i] = (O, LSE)
+    return out
+
+
+def decode_ref(q, k_cache, v_cache, cu_seqlens_k, scale, batch=None, heads=None):
+    """One query row per sequence, attending to every key of its sequence
+    (the newest token sees the whole cache, so there is no mask).
+    q [B, H, D]; caches packed [T_k, H, D].  Returns O [B, H, D] and
+    LSE [B, H] for the chosen (batch, head) items (others left as NaN)."""
+    q, kc, vc = to_f64(q), to_f64(k_cache), to_f64(v_cache)
+    cu = [int(x) for x in np.asarray(cu_seqlens_k).tolist()]
+    B, H, D = q.shape
+    O = np.full((B, H, D), np.nan)
+    LSE = np.full((B, H), np.nan)
+    for b in (range(B) if batch is None else batch):
+        a, e = cu[b], cu[b + 1]
+        for h in (range(H) if heads is None else heads):
+            o, l = attention_head_ref(q[b, h][None, :], kc[a:e, h], vc[a:e, h],
+                                      scale, False)
+            O[b, h], LSE[b, h] = o[0], l[0]
+    return O, LSE
+
+
+# ---------------------------------------------------------------------------
+# The state u = (m, d, o) and its merge.
+# Section "The State": over a block of keys, m is the running maximum score,
+# d = sum e^{s_j - m} and o = sum e^{s_j - m} v_j (unnormalised output row).
+# A single pair (s_j, v_j) enters as (s_j, 1, v_j); the row is read off at the
+# end as o / d.
+# Section "The Merge, and the Twist": keep the larger maximum and shrink the
+# other side toward it, so the exponent is never positive.  Identity
+# (-inf, 0, 0) (section "Why Attention's Combine Still Associates").
+# Section "Alternative Twist: Base 2": the same monoid over sigma = s log2(e)
+# with 2^x in place of e^x.
+# ---------------------------------------------------------------------------
+
+def identity(D: int):
+    return (-math.inf, 0.0, np.zeros(D))
+
+
+def inject(s: float, v: np.ndarray):
+    """A single key/value pair as a state: (s, 1, v)."""
+    return (float(s), 1.0, np.asarray(v, dtype=np.float64).copy())
+
+
+def merge(a, b, base: float = math.e):
+    """(m_a, d_a, o_a) (+) (m_b, d_b, o_b), case-split on the larger max.
+    With the identity on either side the other operand is returned (the
+    -inf - (-inf) case has no value; it is defined by the identity law)."""
+    ma, da, oa = a
+    mb, db, ob = b
+    if mb == -math.inf:
+        return (ma, da, np.array(oa, dtype=np.float64))
+    if ma == -math.inf:
+        return (mb, db, np.array(ob, dtype=np.float64))
+    if ma >= mb:
+        f = base ** (mb - ma)
+        return (ma, da + db * f, oa + ob * f)
+    f = base ** (ma - mb)
+    return (mb, da * f + db, oa * f + ob)
+
+
+def fold_left(states, D: int, base: float = math.e):
+    acc = identity(D)
+    for u in states:
+        acc = merge(acc, u, base)
+    return acc
+
+
+def fold_tree(states, tree, base: float = math.e):
+    """Fold following an explicit bracketing: ``tree`` is an int (a leaf
+    index) or a pair (left_tree, right_tree)."""
+    if isinstance(tree, int):
+        return states[tree]
+    l, r = tree
+    return merge(fold_tree(states, l, base), fold_tree(states, r, base), base)
+
+
+def finalize(state, base: float = math.e):
+    """Output row o / d and log-sum-exp in natural log: ln(base) * m + ln d."""
+    m, d, o = state
+    if d == 0.0:
+        return np.zeros_like(o), -math.inf
+    return o / d, math.log(base) * m + math.log(d)
+
+
+def row_state(s: np.ndarray, v: np.ndarray, base: float = math.e):
+    """The state of a whole block by its definition (no merging):
+    m = max s, d = sum base^{s - m}, o = sum base^{s - m} v."""
+    if s.size == 0:
+        return identity(v.shape[-1])
+    m = float(s.max())
+    if m == -math.inf:
+        return identity(v.shape[-1])
+    w = np.power(base, s - m)
+    return (m, float(w.sum()), w @ v)
+
+
+# ---------------------------------------------------------------------------
+# Split-KV decode: chunk states and their combine.
+# Section "Associativity is All You Need": split-K lets separate thread blocks
+# own chunks, write partial results to scratch and fold them in a small second
+# kernel; "The Merge, and the Twist" gives the fold.  Chunking reading: chunk c
+# of a length-L sequence covers keys [c*ceil(L/S), min(L, (c+1)*ceil(L/S))),
+# possibly empty.  States are kept in the base-2 coordinates
+# (sigma = s * log2(e)).
+# ---------------------------------------------------------------------------
+
+def chunk_bounds(L: int, num_splits: int):
+    size = -(-L // num_splits) if L > 0 else 0
+    out = []
+    for c in range(num_splits):
+        a = min(L, c * size)
+        b = min(L, (c + 1) * size)
+        out.append((a, b))
+    return out
+
+
+def chunk_states_ref(q, k_cache, v_cache, cu_seqlens_k, num_splits, scale,
+                     batch=None, heads=None):
+    """Base-2 states (m2, d, o) of every KV chunk of every (b, h).
+    Returns m2 [B, H, S], d [B, H, S], o [B, H, S, D] float64; empty chunks hold
+    the identity (-inf, 0, 0).  Items not selected are NaN."""
+    q, kc, vc = to_f64(q), to_f64(k_cache), to_f64(v_cache)
+    cu = [int(x) for x in np.asarray(cu_seqlens_k).tolist()]
+    B, H, D = q.shape
+    S = int(num_splits)
+    M = np.full((B, H, S), np.nan)
+    Dn = np.full((B, H, S), np.nan)
+    Ot = np.full((B, H, S, D), np.nan)
+    for b in (range(B) if batch is None else batch):
+        a0 = cu[b]
+        L = cu[b + 1] - a0
+        for h in (range(H) if heads is None else heads):
+            for c, (a, e) in enumerate(chunk_bounds(L, S)):
+                sig = (kc[a0 + a:a0 + e, h] @ q[b, h]) * (float(scale) * LOG2E)
+                m, d, o = row_state(sig, vc[a0 + a:a0 + e, h], base=2.0)
+                M[b, h, c], Dn[b, h, c], Ot[b, h, c] = m, d, o
+    return M, Dn, Ot
+
+
+def combine_ref(m2, d, o):
+    """Fold the base-2 chunk states of each row left to right (chunk 0 first)
+    and finalise: O = o / d, LSE = ln2 * (m2 + log2 d).
+    m2, d: [..., S]; o: [..., S, D].  Returns O [..., D], LSE [...]."""
+    m2 = np.asarray(m2, dtype=np.float64)
+    d = np.asarray(d, dtype=np.float64)
+    o = np.asarray(o, dtype=np.float64)
+    lead = m2.shape[:-1]
+    S = m2.shape[-1]
+    D = o.shape[-1]
+    Ofl = np.zeros(lead + (D,))
+    Lfl = np.zeros(lead)
+    for idx in np.ndindex(*lead):
+        acc = identity(D)
+        for c in range(S):
+            acc = merge(acc, (float(m2[idx + (c,)]), float(d[idx + (c,)]),
+                              o[idx + (c,)]), base=2.0)
+        Ofl[idx], Lfl[idx] = finalize(acc, base=2.0)
+    return Ofl, Lfl
+
+
+# ---------------------------------------------------------------------------
+# Enumeration helpers for the associativity pins (brute force, tiny N).
+# ---------------------------------------------------------------------------
+
+def all_bracketings(lo: int, hi: int):
+    """Every full binary bracketing of leaves lo..hi-1 (Catalan many)."""
+    if hi - lo == 1:
+        return [lo]
+    out = []
+    for mid in range(lo + 1, hi):
+        for left in all_bracketings(lo, mid):
+            for right in all_bracketings(mid, hi):
+                out.append((left, right))
+    return out
+
+
+def all_chunkings(n: int) -> list[list[tuple[int, int]]]:
+    """Every split of 0..n-1 into contiguous non-empty chunks (2^(n-1))."""
+    out = []
+    for mask in range(1 << (n - 1)):
+        cuts = [0] + [i + 1 for i in range(n - 1) if mask >> i & 1] + [n]
+        out.append([(cuts[i], cuts[i + 1]) for i in range(len(cuts) - 1)])
+    return out
