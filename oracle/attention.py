@@ -53,7 +53,7 @@ def safe_softmax_stats(s: np.ndarray):
     """Row maximum m, shifted weights e^{s - m} and their sum d (three passes:
     max, sum, divide - the last one left to the caller).  A row whose entries
     are all -inf has no maximum; it gets m = -inf, weights 0, d = 0."""
-    m = s.max(axis=-1)
+    m = s.max(axis=-1, initial=-np.inf)  # an empty block is the identity
     m_safe = np.where(np.isfinite(m), m, 0.0)
     w = np.exp(s - m_safe[..., None])
     d = w.sum(axis=-1)

@@ -407,3 +407,15 @@ def test_varlen_is_dense_per_sequence():
     np.testing.assert_array_equal(out2[1][0], out[1][0])
     # length-1 sequence: O = v
     np.testing.assert_array_equal(out[1][0][0], v[5])
+
+
+def test_empty_blocks_are_the_identity():
+    """A block with no keys is the identity (-inf, 0, 0): a row that sees no
+    key reads off O = 0 and LSE = -inf; a sequence with no tokens has no rows."""
+    q = np.ones((2, 3))
+    o, l = ora.attention_head_ref(q, np.zeros((0, 3)), np.zeros((0, 3)), 0.5, False)
+    assert o.shape == (2, 3) and not o.any() and (l == -np.inf).all()
+    out = ora.varlen_ref(np.ones((3, 1, 4)), np.ones((3, 1, 4)), np.ones((3, 1, 4)),
+                         [0, 2, 2, 3], 0.5, True)
+    assert out[1][0].shape == (0, 1, 4) and out[1][1].shape == (1, 0)
+    np.testing.assert_array_equal(out[2][0][0, 0], np.ones(4))
