@@ -1,0 +1,386 @@
+"""Benchmark of the exact attention forward on GB300.
+
+One step = one pass of the whole hot path on resident synthetic inputs:
+  1. causal bf16 prefill  B=1 H=32 N=16384 D=128, Q,K ~ N(0, 3^2), V ~ N(0, 1)
+     (fa_fwd, the tensor-core kernel) - the headline workload;
+  2. split-KV decode      B=64 H=32 D=128, KV lengths U[1024, 32768], 16 chunks
+     (fa_decode_splitkv + fa_combine_states).
+`value` is the prefill throughput in TFLOP/s (4 B H N^2 D, halved for causal)
+over the prefill launches of the timed steps; the decode bandwidth is reported
+in the `decode` object.  Inputs (537 MB prefill, ~17.7 GB decode) are larger
+than the 129 MB L2, so no flush is needed between iterations.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun (N > 1) each rank runs the same workload on its own GPU (weak
+scaling, no collective on the data path); the time is the max over ranks.
+`--impl reference` times the float64 CPU oracle instead, on a bounded sample
+of the prefill workload per step (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import fa_inputs as inp  # noqa: E402
+
+PREFILL = dict(B=1, H=32, N=16384, D=128)
+DECODE = dict(B=64, H=32, D=128, S=16)
+METRIC = "attention fwd TFLOP/s (bf16, causal) and % of GB300 BF16 peak; decode GB/s"
+WORKLOAD = ("prefill B=1 H=32 N=16384 D=128 causal bf16, Q,K~N(0,9) V~N(0,1); "
+            "decode B=64 H=32 D=128 L~U[1024,32768] 16 KV chunks")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def prefill_flops(B, H, N, D, causal=True) -> float:
+    f = 4.0 * B * H * N * N * D
+    return f / 2 if causal else f
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def load_traffic(kernel: str, source: str):
+    """DRAM bytes per launch from a committed ncu capture, or None when the
+    kernel source changed since the capture."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f).get(kernel)
+    if not d:
+        return None
+    with open(os.path.join(ROOT, source), "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()
+    return d["bytes_per_launch"] if d.get("source_sha256") == h else None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        return rank, world, local, dist
+    return 0, 1, 0, None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(x: float, dist) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ oracle arm
+
+def oracle_sample_step(q, k, v, scale, head: int, rows):
+    """The float64 oracle on query rows `rows` of one head; returns the
+    algorithmic causal FLOPs of that sample."""
+    from oracle import attention as ora
+    ora.attention_head_ref(q[head], k[head], v[head], scale, True, rows)
+    D = q.shape[-1]
+    return float(sum(4.0 * D * (int(r) + 1) for r in rows))
+
+
+def cpu_sample_inputs():
+    """Two heads of the prefill workload, drawn on the CPU generator with the
+    prefill seed, as float64 (rows sampled per step)."""
+    import numpy as np
+    c = inp.dense(1, 2, PREFILL["N"], PREFILL["D"], seed=3, causal=True, qk_std=3.0)
+    f = lambda t: t[0].to(torch.float64).numpy()
+    return f(c.q), f(c.k), f(c.v), c.scale, np
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    q, k, v, scale, np = cpu_sample_inputs()
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    N = PREFILL["N"]
+    rows = np.arange(N - 384, N)  # the last 384 rows: each sees ~16K keys
+    for _ in range(args.warmup):
+        oracle_sample_step(q, k, v, scale, 0, rows[:64])
+    t0 = time.perf_counter()
+    flops = 0.0
+    for s in range(args.steps):
+        flops += oracle_sample_step(q, k, v, scale, s % 2, rows)
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    sample = (f"float64 NumPy oracle, per step the last {len(rows)} query rows of one "
+              f"head (of {PREFILL['H']}) against all visible keys, N={N} D={PREFILL['D']} causal")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def cpu_baseline_leg():
+    """The oracle as it stands on this host's cores, on a bounded sample
+    (about 10 s): the last 2048 query rows of 2 heads of the prefill workload."""
+    q, k, v, scale, np = cpu_sample_inputs()
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    N = PREFILL["N"]
+    rows = np.arange(N - 2048, N)
+    oracle_sample_step(q, k, v, scale, 0, rows[:32])
+    t0 = time.perf_counter()
+    flops = 0.0
+    for h in range(2):
+        flops += oracle_sample_step(q, k, v, scale, h, rows)
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"last {len(rows)} query rows of 2 heads, N={N} D=128 causal, float64 "
+                      f"NumPy ({dt:.1f} s)"}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_gpu(args, rank, world, dist):
+    import exact_io_aware_15_gb300 as fa
+    fa.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+
+    P = PREFILL
+    pc = inp.dense(P["B"], P["H"], P["N"], P["D"], seed=3, causal=True, qk_std=3.0,
+                   device="cuda")
+    o = torch.empty_like(pc.q)
+    lse = torch.empty((P["B"], P["H"], P["N"]), dtype=torch.float32, device=dev)
+    dc = inp.config4(device="cuda")
+    cu = dc.cu_seqlens_k.to(dev)
+    Dd = DECODE
+    pm = torch.empty((Dd["B"], Dd["H"], Dd["S"]), dtype=torch.float32, device=dev)
+    pd = torch.empty_like(pm)
+    po = torch.empty((Dd["B"], Dd["H"], Dd["S"], Dd["D"]), dtype=torch.float32, device=dev)
+    od = torch.empty((Dd["B"], Dd["H"], Dd["D"]), dtype=torch.bfloat16, device=dev)
+    lsed = torch.empty((Dd["B"], Dd["H"]), dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        fa.fa_fwd(pc.q, pc.k, pc.v, pc.scale, True, o=o, lse=lse)
+        if ev is not None:
+            ev[1].record(stream)
+        fa.fa_decode_splitkv(dc.q, dc.k_cache, dc.v_cache, cu, Dd["S"], dc.scale, pm, pd, po)
+        if ev is not None:
+            ev[2].record(stream)
+        fa.fa_combine_states(pm, pd, po, o=od, lse=lsed)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    status = fa.fa_check_device_status()
+    if status != fa.FA_OK:
+        raise RuntimeError(f"device status after warm-up: {fa.fa_status_string(status)}")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        start.record(stream)
+        for s in range(args.steps):
+            step(evs[s])
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(dist)
+    total_ms = start.elapsed_time(end)
+    t_pre = [e[0].elapsed_time(e[1]) for e in evs]
+    t_dec = [e[1].elapsed_time(e[2]) for e in evs]
+    t_cmb = [e[2].elapsed_time(e[3]) for e in evs]
+    status = fa.fa_check_device_status()
+    if status != fa.FA_OK:
+        raise RuntimeError(f"device status after timing: {fa.fa_status_string(status)}")
+
+    flops = prefill_flops(P["B"], P["H"], P["N"], P["D"])
+    pre_ms = max_over_ranks(sum(t_pre), dist)
+    dec_ms = max_over_ranks(sum(t_dec), dist)
+    cmb_ms = max_over_ranks(sum(t_cmb), dist)
+    total_ms = max_over_ranks(total_ms, dist)
+    K = args.steps
+    value = world * flops * K / (pre_ms * 1e-3) / 1e12
+
+    lens = dc.meta["lens"]
+    kv_bytes = float(sum(lens)) * Dd["H"] * Dd["D"] * 2 * 2
+    dec_bytes = kv_bytes + Dd["B"] * Dd["H"] * Dd["D"] * 2 + \
+        Dd["B"] * Dd["H"] * Dd["S"] * (Dd["D"] + 2) * 4        # q + partial states written
+    cmb_bytes = Dd["B"] * Dd["H"] * (Dd["S"] * (Dd["D"] + 2) * 4 + Dd["D"] * 2 + 4)
+    dec_alg = kv_bytes + Dd["B"] * Dd["H"] * (Dd["D"] * 2 * 2 + 4)  # K,V,q,O,LSE
+    peaks, kind = load_peaks()
+    pk_tf = float(peaks["bf16_tflops"])
+    pk_bw = float(peaks["hbm_gbs"])
+    achieved = flops / (pre_ms / K * 1e-3) / 1e12
+    dec_gbs = dec_bytes / (dec_ms / K * 1e-3) / 1e9
+    e2e_dec_gbs = world * dec_alg * K / ((dec_ms + cmb_ms) * 1e-3) / 1e9
+
+    # end to end through the C ABI with host buffers (pinned), copies timed
+    e2e = None
+    hq, hk, hv = (t.cpu().pin_memory() for t in (pc.q, pc.k, pc.v))
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    dq, dk, dv = (torch.empty_like(pc.q) for _ in range(3))
+    torch.cuda.synchronize()
+    n_e2e = max(1, min(K, 20))
+    barrier(dist)
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        fa.fa_fwd(dq, dk, dv, pc.scale, True, o=o, lse=lse)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+        torch.cuda.synchronize()
+    dt = max_over_ranks(time.perf_counter() - t0, dist)
+    e2e = {"value": world * flops * n_e2e / dt / 1e12, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": 3 * pc.q.numel() * 2,
+           "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4,
+           "steps": n_e2e}
+
+    if rank != 0:
+        return 0
+    cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline_leg()
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": total_ms / K,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "l2": "inputs larger than L2 (no flush)",
+                   "prefill_ms": pre_ms / K, "decode_ms": dec_ms / K, "combine_ms": cmb_ms / K,
+                   "parallelism": f"replicas x{world} (independent heads per GPU)"},
+        "roofline": {"kernel": "fa_fwd_tc_kernel<128>", "bound": "tensor",
+                     "achieved": achieved, "peak": pk_tf, "unit": "TFLOP/s",
+                     "frac": achieved / pk_tf, "peak_kind": f"{kind} bf16 burst",
+                     "traffic": load_traffic("fa_fwd_tc_kernel<128>",
+                                             "exact_io_aware_15_gb300/csrc/fwd_tc.cu")},
+        "decode": {"metric": "split-KV decode GB/s", "value": dec_gbs, "unit": "GB/s",
+                   "frac": dec_gbs / pk_bw, "peak": pk_bw, "peak_kind": f"{kind} hbm copy",
+                   "frac_of_nominal_8tbs": dec_gbs / 8000.0,
+                   "bytes_per_launch": dec_bytes, "kv_tokens": int(sum(lens)),
+                   "combine_us": cmb_ms / K * 1e3,
+                   "end_to_end_gbs": e2e_dec_gbs,
+                   "traffic": load_traffic("fa_decode_splitkv_kernel<128>",
+                                           "exact_io_aware_15_gb300/csrc/decode.cu")},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 3 * K,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl != "reference":
+        args.warmup = 3
+    rank, world, local, dist = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, rank, world)
+        return run_gpu(args, rank, world, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,281 @@
+"""Exact tiled attention forward for GB300 (sm_103a): Python binding.
+
+A thin ctypes layer over the C ABI in ``include/fa_gb300.h`` (library
+``_lib/libfa_gb300.so``, built by ``build.build()``).  Each function here has
+the name of the C entry point it calls and only marshals arguments: shape,
+dtype and device checks, output allocation through PyTorch when the caller
+passes none, the current CUDA stream, and the status code.  Every step of the
+computation runs in the library's CUDA kernels; there is no other code path.
+If the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libfa_gb300.so")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = -1
+FA_ERR_UNSUPPORTED_ARCH = -2
+FA_ERR_LAUNCH = -3
+FA_ERR_DEVICE_TIMEOUT = -4
+FA_ERR_DEVICE_BOUNDS = -5
+FA_ERR_DRIVER = -6
+FA_ERR_CUDA = -7
+FA_DTYPE_BF16 = 0
+FA_DTYPE_F32 = 1
+
+# Every symbol the header declares, with its ctypes signature.
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+SIGNATURES = {
+    "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_fwd_f32": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_fwd_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _I, _P]),
+    "fa_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_decode_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
+    "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
+    "fa_combine_states": (_I, [_P, _P, _P, _I, _I, _I, _P, _I, _P, _P]),
+    "fa_check_device_status": (_I, [_P]),
+    "fa_status_string": (ctypes.c_char_p, [_I]),
+    "fa_last_cuda_error": (_I, []),
+}
+
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {fa_status_string(code)} (code {code})")
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads the CUDA library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"CUDA library not built: {path} is missing "
+                "(run exact_io_aware_15_gb300.build.build())")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def fa_status_string(code: int) -> str:
+    try:
+        return load_library().fa_status_string(int(code)).decode()
+    except RuntimeError:
+        return f"status {code}"
+
+
+def _check(code: int, where: str) -> None:
+    if code != FA_OK:
+        raise FAError(code, where)
+
+
+def _stream(t: torch.Tensor) -> int:
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim: int) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _scale(scale, D):
+    return 1.0 / math.sqrt(D) if scale is None else float(scale)
+
+
+_DT = {torch.bfloat16: FA_DTYPE_BF16, torch.float32: FA_DTYPE_F32}
+
+
+def fa_fwd_ex(q, k, v, scale=None, causal=False, o_dtype=None, o=None, lse=None):
+    """Dense forward.  q, k, v: [B, H, N, D] bf16 (tensor cores) or fp32
+    (FFMA kernel).  Returns (o [B, H, N, D] in o_dtype, lse [B, H, N] fp32)."""
+    in_dtype = q.dtype
+    if in_dtype not in _DT:
+        raise TypeError("q, k, v must be bf16 or fp32")
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, in_dtype, 4)
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must have the same shape [B, H, N, D]")
+    B, H, N, D = q.shape
+    o_dtype = in_dtype if o_dtype is None else o_dtype
+    if o_dtype not in _DT:
+        raise TypeError("o_dtype must be bf16 or fp32")
+    if o is None:
+        o = torch.empty_like(q, dtype=o_dtype)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _need(o, "o", o_dtype, 4)
+    _need(lse, "lse", torch.float32, 3)
+    rc = load_library().fa_fwd_ex(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, D,
+        _scale(scale, D), int(bool(causal)), _DT[in_dtype], _DT[o_dtype],
+        _stream(q))
+    _check(rc, "fa_fwd_ex")
+    return o, lse
+
+
+def fa_fwd(q, k, v, scale=None, causal=False, o=None, lse=None):
+    """Dense bf16 forward on the tensor cores (fa_fwd)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, 4)
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must have the same shape [B, H, N, D]")
+    B, H, N, D = q.shape
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    _need(o, "o", torch.bfloat16, 4)
+    _need(lse, "lse", torch.float32, 3)
+    rc = load_library().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                               B, H, N, D, _scale(scale, D), int(bool(causal)),
+                               _stream(q))
+    _check(rc, "fa_fwd")
+    return o, lse
+
+
+def fa_fwd_f32(q, k, v, scale=None, causal=False, o=None, lse=None):
+    """Dense fp32 forward on the CUDA cores (fa_fwd_f32)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.float32, 4)
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must have the same shape [B, H, N, D]")
+    B, H, N, D = q.shape
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    _need(o, "o", torch.float32, 4)
+    _need(lse, "lse", torch.float32, 3)
+    rc = load_library().fa_fwd_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                   B, H, N, D, _scale(scale, D), int(bool(causal)),
+                                   _stream(q))
+    _check(rc, "fa_fwd_f32")
+    return o, lse
+
+
+def fa_fwd_varlen(q, k, v, cu_seqlens, max_seqlen, scale=None, causal=True,
+                  o=None, lse=None):
+    """Packed variable-length forward.  q, k, v: [T, H, D] bf16; cu_seqlens:
+    int32 [num_seqs + 1] on the same device.  Returns (o [T, H, D] bf16,
+    lse [H, T] fp32)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, 3)
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must have the same shape [T, H, D]")
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    T, H, D = q.shape
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((H, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    _need(o, "o", torch.bfloat16, 3)
+    _need(lse, "lse", torch.float32, 2)
+    rc = load_library().fa_fwd_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens),
+        cu_seqlens.numel() - 1, T, int(max_seqlen), H, D, _scale(scale, D),
+        int(bool(causal)), _stream(q))
+    _check(rc, "fa_fwd_varlen")
+    return o, lse
+
+
+def fa_decode_workspace_bytes(B: int, H: int, D: int, num_splits: int) -> int:
+    return int(load_library().fa_decode_workspace_bytes(B, H, D, num_splits))
+
+
+def fa_decode_splitkv(q, k_cache, v_cache, cu_seqlens_k, num_splits, scale=None,
+                      part_m=None, part_d=None, part_o=None):
+    """Split-KV first pass.  q [B, H, D] bf16; caches [T_k, H, D] bf16;
+    cu_seqlens_k int32 [B + 1] on the device.  Returns the base-2 chunk states
+    (part_m [B, H, S], part_d [B, H, S], part_o [B, H, S, D]) in fp32."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 3)
+    _need(v_cache, "v_cache", torch.bfloat16, 3)
+    _need(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+    B, H, D = q.shape
+    if k_cache.shape != v_cache.shape or k_cache.shape[1:] != (H, D):
+        raise ValueError("caches must be [T_k, H, D] like q's heads and head dim")
+    if cu_seqlens_k.numel() != B + 1:
+        raise ValueError("cu_seqlens_k must have B + 1 entries")
+    S = int(num_splits)
+    dev = q.device
+    part_m = torch.empty((B, H, S), dtype=torch.float32, device=dev) if part_m is None else part_m
+    part_d = torch.empty((B, H, S), dtype=torch.float32, device=dev) if part_d is None else part_d
+    part_o = torch.empty((B, H, S, D), dtype=torch.float32, device=dev) if part_o is None else part_o
+    _need(part_m, "part_m", torch.float32, 3)
+    _need(part_d, "part_d", torch.float32, 3)
+    _need(part_o, "part_o", torch.float32, 4)
+    rc = load_library().fa_decode_splitkv(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_k), k_cache.shape[0],
+        B, H, D, S, _scale(scale, D), _ptr(part_m), _ptr(part_d), _ptr(part_o),
+        _stream(q))
+    _check(rc, "fa_decode_splitkv")
+    return part_m, part_d, part_o
+
+
+def fa_combine_states(part_m, part_d, part_o, o_dtype=torch.bfloat16, o=None, lse=None):
+    """Split-KV second pass over states [..., S] / [..., S, D] (fp32).
+    Returns (o [..., D] in o_dtype, lse [...] fp32)."""
+    for t, n in ((part_m, "part_m"), (part_d, "part_d"), (part_o, "part_o")):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous fp32 CUDA tensor")
+    lead = tuple(part_m.shape[:-1])
+    S = part_m.shape[-1]
+    D = part_o.shape[-1]
+    if tuple(part_d.shape) != lead + (S,) or tuple(part_o.shape) != lead + (S, D):
+        raise ValueError("state shapes do not match")
+    rows = 1
+    for x in lead:
+        rows *= x
+    if o_dtype not in _DT:
+        raise TypeError("o_dtype must be bf16 or fp32")
+    o = torch.empty(lead + (D,), dtype=o_dtype, device=part_o.device) if o is None else o
+    lse = torch.empty(lead, dtype=torch.float32, device=part_o.device) if lse is None else lse
+    rc = load_library().fa_combine_states(
+        _ptr(part_m), _ptr(part_d), _ptr(part_o), rows, S, D, _ptr(o), _DT[o_dtype],
+        _ptr(lse), _stream(part_o))
+    _check(rc, "fa_combine_states")
+    return o, lse
+
+
+def fa_check_device_status(stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Synchronises the stream and returns (and clears) the device status:
+    FA_OK, FA_ERR_DEVICE_TIMEOUT or FA_ERR_DEVICE_BOUNDS."""
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(load_library().fa_check_device_status(s.cuda_stream))
+
+
+def decode(q, k_cache, v_cache, cu_seqlens_k, num_splits=16, scale=None,
+           o_dtype=torch.bfloat16):
+    """Split-KV decode end to end: fa_decode_splitkv then fa_combine_states."""
+    pm, pd, po = fa_decode_splitkv(q, k_cache, v_cache, cu_seqlens_k, num_splits, scale)
+    return fa_combine_states(pm, pd, po, o_dtype=o_dtype)
+
+
+__all__ = [
+    "fa_fwd", "fa_fwd_f32", "fa_fwd_ex", "fa_fwd_varlen", "fa_decode_workspace_bytes",
+    "fa_decode_splitkv", "fa_combine_states", "fa_check_device_status",
+    "fa_status_string", "decode", "load_library", "FAError", "LIB_PATH",
+]

@@ -1,0 +1,357 @@
+// C ABI of the library (declared in include/fa_gb300.h): argument checks,
+// TMA tensor-map encoding and dispatch to the kernels.  Nothing here
+// allocates device memory or synchronises, except fa_check_device_status.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "fa_device.cuh"
+#include "fa_gb300.h"
+#include "fa_internal.h"
+
+namespace {
+
+// Device status word: kernels OR fa::kStatus* bits into it.
+__device__ unsigned int g_fa_status;
+
+constexpr int kMaxDevices = 64;
+thread_local int t_last_cuda_error = 0;
+
+struct DeviceInfo {
+  bool probed = false;
+  bool sm103 = false;
+  unsigned int* status = nullptr;
+};
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_mutex;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int record(cudaError_t e) {
+  t_last_cuda_error = static_cast<int>(e);
+  return FA_ERR_CUDA;
+}
+
+// Checks that the current device is sm_103 and returns its status word.
+int current_device(unsigned int** status) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return record(e);
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED_ARCH;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceInfo& info = g_devices[dev];
+  if (!info.probed) {
+    int major = 0, minor = 0;
+    e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e != cudaSuccess) return record(e);
+    e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess) return record(e);
+    info.sm103 = (major == 10 && minor == 3);
+    if (info.sm103) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_fa_status);
+      if (e != cudaSuccess) return record(e);
+      info.status = static_cast<unsigned int*>(p);
+    }
+    info.probed = true;
+  }
+  if (!info.sm103) return FA_ERR_UNSUPPORTED_ARCH;
+  *status = info.status;
+  return FA_OK;
+}
+
+int get_encoder() {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_encode) return FA_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                   cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) {
+    t_last_cuda_error = static_cast<int>(e);
+    return FA_ERR_DRIVER;
+  }
+  g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  return FA_OK;
+}
+
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+bool good_scale(float s) { return isfinite(s) && s >= 0.f; }
+float scale_log2(float s) {
+  return static_cast<float>(static_cast<double>(s) * 1.4426950408889634073599);
+}
+
+// 3-D bf16 map with a (64, box1, box2) box and 128-byte swizzle.
+int encode_map(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+               uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box1, uint32_t box2) {
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  const cuuint32_t box[3] = {64u, box1, box2};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_DRIVER;
+}
+
+int launched(cudaError_t e) {
+  if (e == cudaSuccess) return FA_OK;
+  t_last_cuda_error = static_cast<int>(e);
+  return FA_ERR_LAUNCH;
+}
+
+int fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+             int N, int D, float scale, int causal, int o_f32, void* stream) {
+  if (B >= 0 && H >= 0 && N >= 0 && (B == 0 || H == 0 || N == 0) &&
+      (D == 64 || D == 128) && good_scale(scale))
+    return FA_OK;  // empty problem: nothing to read or write
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse))
+    return FA_ERR_INVALID_ARG;
+  if (B < 0 || H < 0 || N < 0 || (D != 64 && D != 128) || !good_scale(scale))
+    return FA_ERR_INVALID_ARG;
+  const long long BH = static_cast<long long>(B) * H;
+  const long long mblocks = (static_cast<long long>(N) + 127) / 128;
+  if (BH > 0x7fffffffLL || mblocks > 65535) return FA_ERR_INVALID_ARG;
+  unsigned int* status = nullptr;
+  int rc = current_device(&status);
+  if (rc != FA_OK) return rc;
+  if (BH == 0 || N == 0) return FA_OK;
+  rc = get_encoder();
+  if (rc != FA_OK) return rc;
+  fa::TcMaps maps;
+  const uint64_t rs = static_cast<uint64_t>(D) * 2u;
+  const uint64_t hs = rs * static_cast<uint64_t>(N);
+  if (encode_map(&maps.q, q, D, N, BH, rs, hs, 128u, 1u) != FA_OK ||
+      encode_map(&maps.k, k, D, N, BH, rs, hs, 128u, 1u) != FA_OK ||
+      encode_map(&maps.v, v, D, N, BH, rs, hs, 128u, 1u) != FA_OK)
+    return FA_ERR_DRIVER;
+  fa::TcFwdArgs a{};
+  a.H = H;
+  a.N = N;
+  a.num_mblocks = static_cast<int>(mblocks);
+  a.causal = causal ? 1 : 0;
+  a.scale_log2 = scale_log2(scale);
+  a.cu_seqlens = nullptr;
+  a.o = o;
+  a.o_f32 = o_f32;
+  a.lse = lse;
+  a.status = status;
+  return launched(fa::launch_fwd_tc(maps, a, D, static_cast<int>(BH),
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+int fwd_f32(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+            int N, int D, float scale, int causal, int o_f32, void* stream) {
+  if (B >= 0 && H >= 0 && N >= 0 && (B == 0 || H == 0 || N == 0) &&
+      (D == 64 || D == 128) && good_scale(scale))
+    return FA_OK;  // empty problem: nothing to read or write
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse))
+    return FA_ERR_INVALID_ARG;
+  if (B < 0 || H < 0 || N < 0 || (D != 64 && D != 128) || !good_scale(scale))
+    return FA_ERR_INVALID_ARG;
+  const long long BH = static_cast<long long>(B) * H;
+  const long long mblocks = (static_cast<long long>(N) + 63) / 64;
+  if (BH > 0x7fffffffLL || mblocks > 65535) return FA_ERR_INVALID_ARG;
+  unsigned int* status = nullptr;
+  int rc = current_device(&status);
+  if (rc != FA_OK) return rc;
+  if (BH == 0 || N == 0) return FA_OK;
+  fa::F32FwdArgs a{};
+  a.q = static_cast<const float*>(q);
+  a.k = static_cast<const float*>(k);
+  a.v = static_cast<const float*>(v);
+  a.o = o;
+  a.o_f32 = o_f32;
+  a.lse = lse;
+  a.BH = static_cast<int>(BH);
+  a.N = N;
+  a.causal = causal ? 1 : 0;
+  a.scale_log2 = scale_log2(scale);
+  return launched(fa::launch_fwd_f32(a, D, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+           int N, int D, float scale, int causal, void* stream) {
+  return fwd_bf16(q, k, v, o, lse, B, H, N, D, scale, causal, 0, stream);
+}
+
+int fa_fwd_f32(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int N, int D, float scale, int causal, void* stream) {
+  return fwd_f32(q, k, v, o, lse, B, H, N, D, scale, causal, 1, stream);
+}
+
+int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+              int N, int D, float scale, int causal, int in_dtype, int o_dtype, void* stream) {
+  if (o_dtype != FA_DTYPE_BF16 && o_dtype != FA_DTYPE_F32) return FA_ERR_INVALID_ARG;
+  const int o_f32 = o_dtype == FA_DTYPE_F32 ? 1 : 0;
+  if (in_dtype == FA_DTYPE_BF16)
+    return fwd_bf16(q, k, v, o, lse, B, H, N, D, scale, causal, o_f32, stream);
+  if (in_dtype == FA_DTYPE_F32)
+    return fwd_f32(q, k, v, o, lse, B, H, N, D, scale, causal, o_f32, stream);
+  return FA_ERR_INVALID_ARG;
+}
+
+int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                  const int* cu_seqlens, int num_seqs, int total_tokens, int max_seqlen, int H,
+                  int D, float scale, int causal, void* stream) {
+  if (num_seqs >= 0 && H >= 0 && total_tokens >= 0 && max_seqlen >= 0 &&
+      (num_seqs == 0 || H == 0 || total_tokens == 0) && (D == 64 || D == 128) &&
+      good_scale(scale))
+    return FA_OK;  // empty problem: nothing to read or write
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse) ||
+      !aligned4(cu_seqlens))
+    return FA_ERR_INVALID_ARG;
+  if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0 || H < 0 ||
+      (D != 64 && D != 128) || !good_scale(scale))
+    return FA_ERR_INVALID_ARG;
+  const long long SH = static_cast<long long>(num_seqs) * H;
+  const long long mblocks = (static_cast<long long>(max_seqlen) + 127) / 128;
+  if (SH > 0x7fffffffLL || mblocks > 65535) return FA_ERR_INVALID_ARG;
+  unsigned int* status = nullptr;
+  int rc = current_device(&status);
+  if (rc != FA_OK) return rc;
+  if (SH == 0 || total_tokens == 0 || max_seqlen == 0) return FA_OK;
+  rc = get_encoder();
+  if (rc != FA_OK) return rc;
+  fa::TcMaps maps;
+  const uint64_t hs = static_cast<uint64_t>(D) * 2u;
+  const uint64_t ts = hs * static_cast<uint64_t>(H);
+  if (encode_map(&maps.q, q, D, H, total_tokens, hs, ts, 1u, 128u) != FA_OK ||
+      encode_map(&maps.k, k, D, H, total_tokens, hs, ts, 1u, 128u) != FA_OK ||
+      encode_map(&maps.v, v, D, H, total_tokens, hs, ts, 1u, 128u) != FA_OK)
+    return FA_ERR_DRIVER;
+  fa::TcFwdArgs a{};
+  a.H = H;
+  a.N = 0;
+  a.num_mblocks = static_cast<int>(mblocks);
+  a.causal = causal ? 1 : 0;
+  a.scale_log2 = scale_log2(scale);
+  a.cu_seqlens = cu_seqlens;
+  a.total_tokens = total_tokens;
+  a.max_seqlen = max_seqlen;
+  a.o = o;
+  a.o_f32 = 0;
+  a.lse = lse;
+  a.status = status;
+  return launched(fa::launch_fwd_tc(maps, a, D, static_cast<int>(SH),
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+size_t fa_decode_workspace_bytes(int B, int H, int D, int num_splits) {
+  if (B < 0 || H < 0 || (D != 64 && D != 128) || num_splits < 1 || num_splits > 256) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * num_splits;
+  return rows * sizeof(float) * (2 + static_cast<size_t>(D));
+}
+
+int fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
+                      const int* cu_seqlens_k, int total_kv_tokens, int B, int H, int D,
+                      int num_splits, float scale, float* part_m, float* part_d, float* part_o,
+                      void* stream) {
+  if (B >= 0 && H >= 0 && (B == 0 || H == 0) && (D == 64 || D == 128) && num_splits >= 1 &&
+      num_splits <= 256 && good_scale(scale))
+    return FA_OK;  // empty problem: nothing to read or write
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned4(cu_seqlens_k) ||
+      !aligned4(part_m) || !aligned4(part_d) || !aligned16(part_o))
+    return FA_ERR_INVALID_ARG;
+  if (B < 0 || H < 0 || total_kv_tokens < 0 || (D != 64 && D != 128) || num_splits < 1 ||
+      num_splits > 256 || B > 65535 || H > 8 * 65535 || !good_scale(scale))
+    return FA_ERR_INVALID_ARG;
+  unsigned int* status = nullptr;
+  int rc = current_device(&status);
+  if (rc != FA_OK) return rc;
+  if (B == 0 || H == 0) return FA_OK;
+  fa::DecodeArgs a{};
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.cu_seqlens_k = cu_seqlens_k;
+  a.total_kv = total_kv_tokens;
+  a.B = B;
+  a.H = H;
+  a.S = num_splits;
+  a.scale_log2 = scale_log2(scale);
+  a.part_m = part_m;
+  a.part_d = part_d;
+  a.part_o = part_o;
+  a.status = status;
+  return launched(fa::launch_decode_splitkv(a, D, static_cast<cudaStream_t>(stream)));
+}
+
+int fa_combine_states(const float* part_m, const float* part_d, const float* part_o, int rows,
+                      int num_splits, int D, void* o, int o_dtype, float* lse, void* stream) {
+  if (rows == 0 && num_splits >= 1 && num_splits <= 256 && (D == 64 || D == 128) &&
+      (o_dtype == FA_DTYPE_BF16 || o_dtype == FA_DTYPE_F32))
+    return FA_OK;  // empty problem: nothing to read or write
+  if (!aligned4(part_m) || !aligned4(part_d) || !aligned16(part_o) || !aligned16(o) ||
+      !aligned4(lse))
+    return FA_ERR_INVALID_ARG;
+  if (rows < 0 || num_splits < 1 || num_splits > 256 || (D != 64 && D != 128) ||
+      (o_dtype != FA_DTYPE_BF16 && o_dtype != FA_DTYPE_F32))
+    return FA_ERR_INVALID_ARG;
+  unsigned int* status = nullptr;
+  int rc = current_device(&status);
+  if (rc != FA_OK) return rc;
+  if (rows == 0) return FA_OK;
+  fa::CombineArgs a{};
+  a.part_m = part_m;
+  a.part_d = part_d;
+  a.part_o = part_o;
+  a.rows = rows;
+  a.S = num_splits;
+  a.o = o;
+  a.o_f32 = o_dtype == FA_DTYPE_F32 ? 1 : 0;
+  a.lse = lse;
+  return launched(fa::launch_combine(a, D, static_cast<cudaStream_t>(stream)));
+}
+
+int fa_check_device_status(void* stream) {
+  unsigned int* status = nullptr;
+  int rc = current_device(&status);
+  if (rc != FA_OK) return rc;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return record(e);
+  unsigned int word = 0;
+  e = cudaMemcpy(&word, status, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return record(e);
+  if (word != 0) {
+    const unsigned int zero = 0;
+    e = cudaMemcpy(status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return record(e);
+  }
+  if (word & fa::kStatusTimeout) return FA_ERR_DEVICE_TIMEOUT;
+  if (word & fa::kStatusBounds) return FA_ERR_DEVICE_BOUNDS;
+  return FA_OK;
+}
+
+const char* fa_status_string(int code) {
+  switch (code) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument (pointer, alignment, size, dtype or scale)";
+    case FA_ERR_UNSUPPORTED_ARCH: return "current device is not an sm_103 GPU";
+    case FA_ERR_LAUNCH: return "kernel launch failed";
+    case FA_ERR_DEVICE_TIMEOUT: return "a device pipeline wait exceeded its limit";
+    case FA_ERR_DEVICE_BOUNDS: return "a device-side bounds check failed";
+    case FA_ERR_DRIVER: return "CUDA driver entry point or tensor-map encoding failed";
+    case FA_ERR_CUDA: return "CUDA runtime error";
+    default: return "unknown status code";
+  }
+}
+
+int fa_last_cuda_error(void) { return t_last_cuda_error; }
+
+}  // extern "C"

@@ -1,0 +1,466 @@
+// Exact attention forward on the sm_103a tensor cores (bf16 in, fp32 state).
+//
+// One CTA owns one 128-row query tile of one (sequence, head) and folds the
+// key/value tiles of that sequence into the per-row state (m, d, o) of
+// "Learning FlashAttention the Hard Way - Part 1", sections "The State" and
+// "The Merge, and the Twist", in the base-2 coordinates of "Alternative Twist:
+// Base 2" (sigma = s * scale * log2 e, every exponential an ex2).  Each KV tile
+// is one merge: the tile's own (max, sum, P V) is folded into the running
+// state by rescaling the side with the smaller maximum.  Keys outside the
+// sequence or above the causal diagonal get sigma = -inf, the identity's m,
+// so they add nothing ("Associativity is All You Need": a neutral element
+// pads the ragged tail).  The output division o / d and the log-sum-exp are
+// deferred to the epilogue.  S and P live only in tensor memory.
+//
+// Roles (192 threads):
+//   warp 0      TMA producer: Q once, then K_j and V_j into a ring of stages.
+//   warp 1      MMA issuer (one thread): S_b = Q K_j^T into TMEM buffer
+//               b = j % 2 (SS form), then O += P_j V_j with P_j read from
+//               TMEM (TS form).  Issue order QK_0, QK_1, PV_0, QK_2, PV_1, ...
+//               so QK_{j+1} overlaps the softmax of tile j.
+//   warps 2..5  softmax: thread t owns row 32*(warp%4) + lane; per tile it
+//               loads its S row, masks, takes the row max, computes
+//               p = 2^(sigma - m_new), rounds P to bf16 into TMEM (over the
+//               first half of its S buffer), rescales its O row in TMEM by
+//               2^(m_old - m_new) once PV_{j-1} has landed, then signals.
+//               Epilogue: O / d in fp32, LSE = ln2 (m + log2 d), stores.
+//
+// Shared memory (1024-byte aligned): Q tile, STAGES x (K tile, V tile), the
+// mbarriers.  A 128 x D bf16 tile is stored as D/64 column halves of
+// 128 rows x 128 bytes, 128-byte swizzled (the TMA box layout and the
+// canonical K-major / MN-major tcgen05 operand layouts).
+// Tensor memory (512 columns): S0 [0,128), S1 [128,256), O [256, 256 + D).
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "fa_device.cuh"
+#include "fa_internal.h"
+
+namespace fa {
+
+template <int D>
+struct TcCfg {
+  static constexpr int BM = 128;
+  static constexpr int BN = 128;
+  static constexpr int HALVES = D / 64;
+  static constexpr uint32_t HALF_BYTES = 128u * 128u;
+  static constexpr uint32_t TILE_BYTES = HALVES * HALF_BYTES;
+  static constexpr int STAGES = (D == 128) ? 3 : 4;
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;
+  static constexpr uint32_t OFF_V = OFF_K + STAGES * TILE_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_V + STAGES * TILE_BYTES;
+  // barrier indices
+  static constexpr int B_Q_FULL = 0;
+  static constexpr int B_K_FULL = 1;
+  static constexpr int B_V_FULL = B_K_FULL + STAGES;
+  static constexpr int B_KV_EMPTY = B_V_FULL + STAGES;
+  static constexpr int B_S_FULL = B_KV_EMPTY + STAGES;
+  static constexpr int B_P_FULL = B_S_FULL + 2;
+  static constexpr int B_O_DONE = B_P_FULL + 2;
+  static constexpr int B_DRAIN = B_O_DONE + 1;
+  static constexpr int NUM_BARS = B_DRAIN + 1;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t TMEM_S0 = 0;
+  static constexpr uint32_t TMEM_S1 = 128;
+  static constexpr uint32_t TMEM_O = 256;
+  static constexpr int THREADS = 192;
+  static constexpr int SOFTMAX_THREADS = 128;
+};
+
+// Bounded wait used only while unwinding after an abort: ignores the abort
+// flag (the copies or MMAs it waits for are already in flight) but still
+// gives up after a short time.
+__device__ __forceinline__ void mbar_wait_unwind(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > 200000000ull) return;  // 200 ms
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
+    fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const TcFwdArgs args) {
+  using C = TcCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+
+  // ---- which tile: heaviest query tiles first (grid.y reversed) ----
+  const int mb = args.num_mblocks - 1 - static_cast<int>(blockIdx.y);
+  const int bh = static_cast<int>(blockIdx.x);
+  const int h = bh % args.H;
+  const int seq = bh / args.H;
+  const bool varlen = args.cu_seqlens != nullptr;
+  int L, tok0;
+  if (varlen) {
+    const int a = __ldg(args.cu_seqlens + seq);
+    const int e = __ldg(args.cu_seqlens + seq + 1);
+    if (a < 0 || e < a || e > args.total_tokens || e - a > args.max_seqlen) {
+      if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(args.status, kStatusBounds);
+      return;
+    }
+    L = e - a;
+    tok0 = a;
+  } else {
+    L = args.N;
+    tok0 = 0;
+  }
+  if (mb * C::BM >= L) return;  // no query row of this sequence in the tile
+  int n_kv = (L + C::BN - 1) / C::BN;
+  if (args.causal) n_kv = min(n_kv, mb + 1);
+
+  // ---- shared memory carve-up ----
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw_addr);
+  auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * i; };
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::B_Q_FULL), 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(bar(C::B_K_FULL + s), 1);
+      mbar_init(bar(C::B_V_FULL + s), 1);
+      mbar_init(bar(C::B_KV_EMPTY + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(C::B_S_FULL + b), 1);
+      mbar_init(bar(C::B_P_FULL + b), C::SOFTMAX_THREADS);
+    }
+    mbar_init(bar(C::B_O_DONE), 1);
+    mbar_init(bar(C::B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  // TMA box origin of a 128-row tile starting at sequence position `row0`,
+  // column half `c`.  Dense maps are (D, N, B*H); varlen maps are (D, H, T).
+  auto tile_coords = [&](int c, int row0, int& c0, int& c1, int& c2) {
+    c0 = c * 64;
+    if (varlen) {
+      c1 = h;
+      c2 = tok0 + row0;
+    } else {
+      c1 = row0;
+      c2 = bh;
+    }
+  };
+
+  if (warp == 0) {
+    // ======================= TMA producer =======================
+    if (lane == 0) {
+      int issued = 0;
+      {
+        const uint32_t qb = bar(C::B_Q_FULL);
+        mbar_arrive_expect_tx(qb, C::TILE_BYTES);
+#pragma unroll
+        for (int c = 0; c < C::HALVES; ++c) {
+          int c0, c1, c2;
+          tile_coords(c, mb * C::BM, c0, c1, c2);
+          tma_load_3d(sbase + C::OFF_Q + c * C::HALF_BYTES, &tm_q, qb, c0, c1, c2);
+        }
+      }
+      for (int j = 0; j < n_kv; ++j) {
+        const int st = j % C::STAGES;
+        if (j >= C::STAGES) {
+          if (!mbar_wait(bar(C::B_KV_EMPTY + st), ((j / C::STAGES) - 1) & 1, abort_flag,
+                         args.status))
+            break;
+        }
+        const uint32_t kb = bar(C::B_K_FULL + st);
+        const uint32_t vb = bar(C::B_V_FULL + st);
+        mbar_arrive_expect_tx(kb, C::TILE_BYTES);
+#pragma unroll
+        for (int c = 0; c < C::HALVES; ++c) {
+          int c0, c1, c2;
+          tile_coords(c, j * C::BN, c0, c1, c2);
+          tma_load_3d(sbase + C::OFF_K + st * C::TILE_BYTES + c * C::HALF_BYTES, &tm_k, kb,
+                      c0, c1, c2);
+        }
+        mbar_arrive_expect_tx(vb, C::TILE_BYTES);
+#pragma unroll
+        for (int c = 0; c < C::HALVES; ++c) {
+          int c0, c1, c2;
+          tile_coords(c, j * C::BN, c0, c1, c2);
+          tma_load_3d(sbase + C::OFF_V + st * C::TILE_BYTES + c * C::HALF_BYTES, &tm_v, vb,
+                      c0, c1, c2);
+        }
+        issued = j + 1;
+      }
+      if (*abort_flag) {
+        // Let every copy this thread started land before the CTA exits.
+        mbar_wait_unwind(bar(C::B_Q_FULL), 0);
+        for (int j = max(0, issued - C::STAGES); j < issued; ++j) {
+          const int st = j % C::STAGES;
+          mbar_wait_unwind(bar(C::B_K_FULL + st), (j / C::STAGES) & 1);
+          mbar_wait_unwind(bar(C::B_V_FULL + st), (j / C::STAGES) & 1);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ======================= MMA issuer =======================
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
+      const uint32_t q_s = sbase + C::OFF_Q;
+
+      auto issue_pv = [&](int i) -> bool {
+        const int b = i & 1;
+        const int st = i % C::STAGES;
+        if (!mbar_wait(bar(C::B_P_FULL + b), (i >> 1) & 1, abort_flag, args.status))
+          return false;
+        if (!mbar_wait(bar(C::B_V_FULL + st), (i / C::STAGES) & 1, abort_flag, args.status))
+          return false;
+        tc_fence_after();
+        const uint32_t v_s = sbase + C::OFF_V + st * C::TILE_BYTES;
+        const uint32_t p_t = tmem + (b ? C::TMEM_S1 : C::TMEM_S0);
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk) {
+          // B = V_j as an MN-major operand: N = D (64-column halves
+          // HALF_BYTES apart), K = 16 keys starting at key 16*kk.
+          const uint64_t bdesc = sdesc_sw128(v_s + kk * 16u * 128u, C::HALF_BYTES, 1024u);
+          tc_mma_ts(tmem + C::TMEM_O, p_t + kk * 8u, bdesc, idesc_pv,
+                    (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(bar(C::B_O_DONE));
+        tc_commit(bar(C::B_KV_EMPTY + st));
+        return true;
+      };
+
+      bool ok = mbar_wait(bar(C::B_Q_FULL), 0, abort_flag, args.status);
+      tc_fence_after();
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int st = j % C::STAGES;
+        const int b = j & 1;
+        if (!mbar_wait(bar(C::B_K_FULL + st), (j / C::STAGES) & 1, abort_flag, args.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t k_s = sbase + C::OFF_K + st * C::TILE_BYTES;
+        const uint32_t s_t = tmem + (b ? C::TMEM_S1 : C::TMEM_S0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          // 16-column slice kk of the head dimension: half kk/4, 32 bytes
+          // per slice inside the 128-byte swizzled row.
+          const uint32_t off = (kk >> 2) * C::HALF_BYTES + (kk & 3) * 32u;
+          tc_mma_ss(s_t, sdesc_sw128(q_s + off, 16u, 1024u), sdesc_sw128(k_s + off, 16u, 1024u),
+                    idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(bar(C::B_S_FULL + b));
+        if (j >= 1 && !issue_pv(j - 1)) ok = false;
+      }
+      if (ok) issue_pv(n_kv - 1);
+      // Every MMA this thread issued completes before TMEM is released.
+      tc_commit(bar(C::B_DRAIN));
+      mbar_wait_unwind(bar(C::B_DRAIN), 0);
+    }
+  } else {
+    // ======================= softmax / epilogue =======================
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int qpos = mb * C::BM + r;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const float c = args.scale_log2;
+    float m = -INFINITY;
+    float dsum = 0.f;
+    bool ok = true;
+
+    for (int j = 0; j < n_kv; ++j) {
+      const int b = j & 1;
+      const uint32_t s_t = tmem + lane_off + (b ? C::TMEM_S1 : C::TMEM_S0);
+      const bool w = mbar_wait(bar(C::B_S_FULL + b), (j >> 1) & 1, abort_flag, args.status);
+      if (__any_sync(0xffffffffu, !w)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+
+      float t[128];
+      {
+        uint32_t raw[64];
+        tmem_ld64(s_t, raw);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) t[i] = __uint_as_float(raw[i]) * c;
+        tmem_ld64(s_t + 64, raw);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) t[64 + i] = __uint_as_float(raw[i]) * c;
+      }
+      const int kbase = j * C::BN;
+      if ((args.causal && j == mb) || kbase + C::BN > L) {
+        int lim = L - kbase;  // keys [0, lim) of the tile are visible
+        if (args.causal) lim = min(lim, qpos - kbase + 1);
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i >= lim) t[i] = -INFINITY;
+      }
+      float mx = t[0];
+#pragma unroll
+      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, t[i]);
+      const float m_new = fmaxf(m, mx);
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = (m_new == m) ? 1.f : ex2_approx(m - m_use);
+
+      float rs = 0.f;
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ex2_approx(t[2 * i] - m_use);
+          const float p1 = ex2_approx(t[2 * i + 1] - m_use);
+          rs += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(s_t, pk);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ex2_approx(t[64 + 2 * i] - m_use);
+          const float p1 = ex2_approx(t[64 + 2 * i + 1] - m_use);
+          rs += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(s_t + 32, pk);
+      }
+      dsum = dsum * alpha + rs;
+      m = m_new;
+
+      if (j > 0) {
+        // o <- alpha * o needs PV_{j-1} to have landed in TMEM.
+        const bool w2 = mbar_wait(bar(C::B_O_DONE), (j - 1) & 1, abort_flag, args.status);
+        if (__any_sync(0xffffffffu, !w2)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          const uint32_t o_t = tmem + lane_off + C::TMEM_O;
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 64) {
+            uint32_t ov[64];
+            tmem_ld64(o_t + c0, ov);
+            uint32_t lo[32], hi[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              lo[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+              hi[i] = __float_as_uint(__uint_as_float(ov[32 + i]) * alpha);
+            }
+            tmem_st32(o_t + c0, lo);
+            tmem_st32(o_t + c0 + 32, hi);
+          }
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(C::B_P_FULL + b));
+    }
+
+    if (ok) {
+      const bool w = mbar_wait(bar(C::B_O_DONE), (n_kv - 1) & 1, abort_flag, args.status);
+      if (!__any_sync(0xffffffffu, !w)) {
+        tc_fence_after();
+        const float inv = dsum > 0.f ? 1.f / dsum : 0.f;
+        const float lse = dsum > 0.f ? (m + log2f(dsum)) * 0.69314718055994530942f : -INFINITY;
+        const bool store = qpos < L;
+        size_t orow, lidx;
+        if (varlen) {
+          const size_t t = static_cast<size_t>(tok0) + qpos;
+          orow = t * args.H + h;
+          lidx = static_cast<size_t>(h) * args.total_tokens + t;
+        } else {
+          orow = static_cast<size_t>(bh) * args.N + qpos;
+          lidx = orow;
+        }
+        const uint32_t o_t = tmem + lane_off + C::TMEM_O;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t ov[32];
+          tmem_ld32(o_t + c0, ov);
+          if (store) {
+            if (args.o_f32) {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(args.o) + orow * D + c0);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                dst[i] = make_float4(__uint_as_float(ov[4 * i]) * inv,
+                                     __uint_as_float(ov[4 * i + 1]) * inv,
+                                     __uint_as_float(ov[4 * i + 2]) * inv,
+                                     __uint_as_float(ov[4 * i + 3]) * inv);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.o) + orow * D + c0);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                uint4 u;
+                u.x = pack_bf16x2(__uint_as_float(ov[8 * i + 0]) * inv,
+                                  __uint_as_float(ov[8 * i + 1]) * inv);
+                u.y = pack_bf16x2(__uint_as_float(ov[8 * i + 2]) * inv,
+                                  __uint_as_float(ov[8 * i + 3]) * inv);
+                u.z = pack_bf16x2(__uint_as_float(ov[8 * i + 4]) * inv,
+                                  __uint_as_float(ov[8 * i + 5]) * inv);
+                u.w = pack_bf16x2(__uint_as_float(ov[8 * i + 6]) * inv,
+                                  __uint_as_float(ov[8 * i + 7]) * inv);
+                dst[i] = u;
+              }
+            }
+          }
+        }
+        if (store) args.lse[lidx] = lse;
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D>
+static cudaError_t launch_tc_impl(const TcMaps& maps, const TcFwdArgs& a, int grid_x,
+                                  cudaStream_t stream) {
+  using C = TcCfg<D>;
+  // The shared-memory opt-in is a per-device attribute of the function.
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(C::SMEM_BYTES));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  dim3 grid(static_cast<unsigned>(grid_x), static_cast<unsigned>(a.num_mblocks));
+  fa_fwd_tc_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(maps.q, maps.k, maps.v, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_tc(const TcMaps& maps, const TcFwdArgs& a, int D, int grid_x,
+                          cudaStream_t stream) {
+  if (D == 128) return launch_tc_impl<128>(maps, a, grid_x, stream);
+  return launch_tc_impl<64>(maps, a, grid_x, stream);
+}
+
+}  // namespace fa

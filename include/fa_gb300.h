@@ -1,0 +1,168 @@
+/*
+ * fa_gb300.h - C ABI of the exact tiled attention forward for GB300 (sm_103a).
+ *
+ * What is computed.  For every query row i of every (batch, head):
+ *     s_j = scale * <q_i, k_j>,     O_i = sum_j e^{s_j} v_j / sum_j e^{s_j},
+ *     LSE_i = ln sum_j e^{s_j}      (natural log, fp32),
+ * over the keys j visible to i (all keys; with causal, keys j <= i of the
+ * same sequence).  This is the attention of "Learning FlashAttention the
+ * Hard Way - Part 1" (cloudrift.ai), section "FlashAttention: Not So
+ * Special", computed per row as a fold of the state (m, d, o) of sections
+ * "The State" and "The Merge, and the Twist" with identity (-inf, 0, 0), in
+ * the base-2 coordinates of section "Alternative Twist: Base 2"
+ * (sigma = s log2 e, every exponential a 2^x).  The N x N score matrix is
+ * never written to memory.  Split-KV decode and the state combine follow
+ * section "Associativity is All You Need" (split-K: chunks reduced by
+ * separate thread blocks, partials folded by a second kernel).
+ *
+ * Conventions shared by every call.
+ *  - Pointers named q, k, v, o, lse, cu_seqlens*, part_* are DEVICE pointers
+ *    owned by the caller; the library never allocates, frees or keeps them.
+ *    Every data pointer must be 16-byte aligned and non-NULL, except that
+ *    an empty problem (a zero batch, head, token or row count) returns FA_OK
+ *    at once and reads no pointer (empty tensors may have NULL data).
+ *  - Tensors are contiguous, row-major, without padding.  bf16 is IEEE
+ *    bfloat16 (uint16 storage), f32 is IEEE binary32.
+ *  - stream is a cudaStream_t (NULL = legacy default stream).  Every call
+ *    only enqueues work on it and returns: nothing synchronises, so errors
+ *    raised on the device appear through fa_check_device_status.
+ *  - The device current on the calling thread must be an sm_103 GPU.
+ *  - scale must be finite and >= 0 (0 gives uniform weights).
+ *  - Return value: FA_OK (0) or a negative FA_ERR_* code.  On
+ *    FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED_ARCH nothing was launched and no
+ *    output was touched.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FA_OK                    0
+#define FA_ERR_INVALID_ARG      -1  /* NULL / misaligned pointer, bad size, bad dtype */
+#define FA_ERR_UNSUPPORTED_ARCH -2  /* current device is not sm_103 */
+#define FA_ERR_LAUNCH           -3  /* the CUDA launch itself failed */
+#define FA_ERR_DEVICE_TIMEOUT   -4  /* a device-side pipeline wait ran past its limit */
+#define FA_ERR_DEVICE_BOUNDS    -5  /* a device-side index check failed */
+#define FA_ERR_DRIVER           -6  /* CUDA driver entry point or tensor-map encoding failed */
+#define FA_ERR_CUDA             -7  /* another CUDA runtime error (see fa_last_cuda_error) */
+
+#define FA_DTYPE_BF16 0
+#define FA_DTYPE_F32  1
+
+/*
+ * Dense forward, bf16 in and out.
+ *   q, k, v : bf16 [B, H, N, D]
+ *   o       : bf16 [B, H, N, D]           (written)
+ *   lse     : f32  [B, H, N], natural log (written)
+ *   B, H, N >= 1; D in {64, 128}; causal != 0 hides keys j > i.
+ * Runs the tcgen05 / TMEM / TMA kernel; accumulation in fp32, the softmax
+ * weights rounded to bf16 (nearest-even) before the P V product.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int H, int N, int D, float scale, int causal, void* stream);
+
+/*
+ * Dense forward, fp32 in and out (CUDA-core FFMA kernel, no tensor cores).
+ * Same shapes and meaning as fa_fwd with f32 elements.
+ */
+int fa_fwd_f32(const void* q, const void* k, const void* v, void* o, float* lse,
+               int B, int H, int N, int D, float scale, int causal, void* stream);
+
+/*
+ * Dense forward with explicit dtypes: in_dtype is the dtype of q, k and v,
+ * o_dtype that of o (FA_DTYPE_BF16 or FA_DTYPE_F32).  in_dtype BF16 runs the
+ * tensor-core kernel, F32 the FFMA kernel.  o_dtype F32 with bf16 inputs
+ * returns the fp32 result before the final rounding.
+ */
+int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+              int B, int H, int N, int D, float scale, int causal,
+              int in_dtype, int o_dtype, void* stream);
+
+/*
+ * Variable-length forward over packed sequences, bf16 in and out.
+ *   q, k, v    : bf16 [total_tokens, H, D]; sequence s owns tokens
+ *                [cu_seqlens[s], cu_seqlens[s+1])
+ *   cu_seqlens : int32 [num_seqs + 1] DEVICE array, cu_seqlens[0] = 0,
+ *                non-decreasing, cu_seqlens[num_seqs] = total_tokens
+ *   max_seqlen : >= every sequence length (sizes the launch grid)
+ *   o          : bf16 [total_tokens, H, D]  (written)
+ *   lse        : f32  [H, total_tokens]     (written)
+ * Positions restart at 0 in every sequence (causal = keys j <= i of the same
+ * sequence).  Tiles never mix sequences: rows beyond a sequence's end are
+ * masked with the identity and not stored.  The device checks the
+ * cu_seqlens it reads against total_tokens and max_seqlen and reports
+ * FA_ERR_DEVICE_BOUNDS (through fa_check_device_status) instead of reading
+ * out of range.
+ */
+int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                  const int* cu_seqlens, int num_seqs, int total_tokens,
+                  int max_seqlen, int H, int D, float scale, int causal,
+                  void* stream);
+
+/*
+ * Bytes of the partial-state workspace fa_decode_splitkv writes:
+ * part_m and part_d f32 [B, H, num_splits], part_o f32 [B, H, num_splits, D].
+ * Returns 0 for invalid sizes.
+ */
+size_t fa_decode_workspace_bytes(int B, int H, int D, int num_splits);
+
+/*
+ * Split-KV decode, first pass: one query token per sequence against its
+ * whole KV cache, the keys cut into num_splits chunks; chunk c of a length-L
+ * sequence covers keys [c*ceil(L/S), min(L, (c+1)*ceil(L/S))) (may be empty).
+ *   q            : bf16 [B, H, D]
+ *   k_cache      : bf16 [T_k, H, D], v_cache likewise (packed sequences)
+ *   cu_seqlens_k : int32 [B + 1] DEVICE array of cache offsets (as above)
+ *   total_kv_tokens : T_k, the number of rows of each cache; the device
+ *                  checks every offset it reads against it and reports
+ *                  FA_ERR_DEVICE_BOUNDS instead of reading out of range
+ *   part_m       : f32 [B, H, S]    max of sigma = scale*log2(e)*<q,k> over the chunk
+ *   part_d       : f32 [B, H, S]    sum of 2^(sigma - part_m)
+ *   part_o       : f32 [B, H, S, D] sum of 2^(sigma - part_m) * v
+ * An empty chunk writes the identity (-inf, 0, 0).  1 <= num_splits <= 256,
+ * D in {64, 128}.  Finish with fa_combine_states(rows = B*H).
+ */
+int fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
+                      const int* cu_seqlens_k, int total_kv_tokens,
+                      int B, int H, int D, int num_splits, float scale, float* part_m, float* part_d,
+                      float* part_o, void* stream);
+
+/*
+ * Split-KV second pass: per row, fold chunks 0, 1, ..., num_splits-1 (in that
+ * fixed order, no atomics) with the case-split merge, then O = o / d and
+ * LSE = ln2 * (m + log2 d).  Every step is one IEEE binary32 operation
+ * rounded to nearest, and the two exponentials are computed in software
+ * (2^x by range reduction and a degree-7 Taylor polynomial; ln by
+ * 2 atanh((x-1)/(x+1))), so the result is bit-reproducible on any launch and
+ * equal bit for bit to a serial CPU fold that performs the same steps.
+ *   part_*  : as written by fa_decode_splitkv, rows = B*H
+ *   o       : [rows, D] in o_dtype (FA_DTYPE_BF16 or FA_DTYPE_F32)
+ *   lse     : f32 [rows]
+ * A row whose chunks are all empty gets O = 0 and LSE = -inf.
+ */
+int fa_combine_states(const float* part_m, const float* part_d,
+                      const float* part_o, int rows, int num_splits, int D,
+                      void* o, int o_dtype, float* lse, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word of the
+ * current device that the kernels set on a failed device-side check.
+ * Returns FA_OK, FA_ERR_DEVICE_TIMEOUT, FA_ERR_DEVICE_BOUNDS or FA_ERR_CUDA.
+ */
+int fa_check_device_status(void* stream);
+
+/* Static English description of a status code. */
+const char* fa_status_string(int code);
+
+/* The last CUDA runtime error code seen by the library on this thread. */
+int fa_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */
