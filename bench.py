@@ -362,6 +362,36 @@ def run_gpu(args, rank, world, dist):
     return 0
 
 
+def run_profile_case(args):
+    """Only one workload, W + K launches, nothing else: the command the ncu
+    captures run.  prefill = the full causal N=16384 prefill (537 MB of
+    inputs); decode = split-KV decode on the first 8 sequences of the decode
+    workload (about 2.2 GB of KV cache, larger than L2, small enough for a
+    multi-pass capture)."""
+    import exact_io_aware_15_gb300 as fa
+    fa.load_library()
+    if args.profile_case == "prefill":
+        P = PREFILL
+        c = inp.dense(P["B"], P["H"], P["N"], P["D"], seed=3, causal=True, qk_std=3.0,
+                      device="cuda")
+        o = torch.empty_like(c.q)
+        lse = torch.empty((P["B"], P["H"], P["N"]), dtype=torch.float32, device="cuda")
+        run = lambda: fa.fa_fwd(c.q, c.k, c.v, c.scale, True, o=o, lse=lse)
+    else:
+        g = torch.Generator().manual_seed(4)
+        lens = torch.randint(1024, 32769, (64,), generator=g).tolist()[:8]
+        c = inp.decode(8, DECODE["H"], DECODE["D"], seed=4, num_splits=DECODE["S"],
+                       lens=lens, device="cuda")
+        cu = c.cu_seqlens_k.cuda()
+        run = lambda: fa.decode(c.q, c.k_cache, c.v_cache, cu, DECODE["S"], c.scale)
+    for _ in range(args.warmup + args.steps):
+        run()
+    torch.cuda.synchronize()
+    rc = fa.fa_check_device_status()
+    print(json.dumps({"profile_case": args.profile_case, "status": fa.fa_status_string(rc)}))
+    return 0 if rc == fa.FA_OK else 1
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -369,7 +399,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", choices=["prefill", "decode"], default=None)
     args = ap.parse_args(argv)
+    if args.profile_case:
+        return run_profile_case(args)
     if args.warmup < 3 and args.impl != "reference":
         args.warmup = 3
     rank, world, local, dist = dist_setup(args.gpus)
