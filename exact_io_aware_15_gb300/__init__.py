@@ -28,6 +28,7 @@ FA_ERR_DEVICE_TIMEOUT = -4
 FA_ERR_DEVICE_BOUNDS = -5
 FA_ERR_DRIVER = -6
 FA_ERR_CUDA = -7
+FA_ERR_SCRATCH_CAPACITY = -8
 FA_DTYPE_BF16 = 0
 FA_DTYPE_F32 = 1
 
@@ -43,6 +44,8 @@ SIGNATURES = {
     "fa_decode_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
     "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
     "fa_combine_states": (_I, [_P, _P, _P, _I, _I, _I, _P, _I, _P, _P]),
+    "fa_decode_splitkv_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _I, _P,
+                                       _P]),
     "fa_check_device_status": (_I, [_P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_last_cuda_error": (_I, []),
@@ -260,6 +263,35 @@ def fa_combine_states(part_m, part_d, part_o, o_dtype=torch.bfloat16, o=None, ls
     return o, lse
 
 
+def fa_decode_splitkv_noalloc(q, k_cache, v_cache, cu_seqlens_k, num_splits, scale=None,
+                              o_dtype=torch.bfloat16, o=None, lse=None):
+    """Split-KV decode, both passes, for callers that may not allocate device
+    memory: the partial states go to the library's static 32 MiB device array
+    instead of a workspace (the outputs still come from the caller, or from
+    torch here when not given).  Returns (o [B, H, D], lse [B, H])."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 3)
+    _need(v_cache, "v_cache", torch.bfloat16, 3)
+    _need(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+    B, H, D = q.shape
+    if k_cache.shape != v_cache.shape or k_cache.shape[1:] != (H, D):
+        raise ValueError("caches must be [T_k, H, D] like q's heads and head dim")
+    if cu_seqlens_k.numel() != B + 1:
+        raise ValueError("cu_seqlens_k must have B + 1 entries")
+    if o_dtype not in _DT:
+        raise TypeError("o_dtype must be bf16 or fp32")
+    o = torch.empty((B, H, D), dtype=o_dtype, device=q.device) if o is None else o
+    lse = torch.empty((B, H), dtype=torch.float32, device=q.device) if lse is None else lse
+    _need(o, "o", o_dtype, 3)
+    _need(lse, "lse", torch.float32, 2)
+    rc = load_library().fa_decode_splitkv_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_k), k_cache.shape[0],
+        B, H, D, int(num_splits), _scale(scale, D), _ptr(o), _DT[o_dtype], _ptr(lse),
+        _stream(q))
+    _check(rc, "fa_decode_splitkv_noalloc")
+    return o, lse
+
+
 def fa_check_device_status(stream: Optional[torch.cuda.Stream] = None) -> int:
     """Synchronises the stream and returns (and clears) the device status:
     FA_OK, FA_ERR_DEVICE_TIMEOUT or FA_ERR_DEVICE_BOUNDS."""
@@ -276,6 +308,7 @@ def decode(q, k_cache, v_cache, cu_seqlens_k, num_splits=16, scale=None,
 
 __all__ = [
     "fa_fwd", "fa_fwd_f32", "fa_fwd_ex", "fa_fwd_varlen", "fa_decode_workspace_bytes",
-    "fa_decode_splitkv", "fa_combine_states", "fa_check_device_status",
+    "fa_decode_splitkv", "fa_combine_states", "fa_decode_splitkv_noalloc",
+    "fa_check_device_status",
     "fa_status_string", "decode", "load_library", "FAError", "LIB_PATH",
 ]

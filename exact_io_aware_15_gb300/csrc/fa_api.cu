@@ -183,6 +183,8 @@ int fwd_f32(const void* q, const void* k, const void* v, void* o, float* lse, in
 
 }  // namespace
 
+int fa::checked_current_device(unsigned int** status) { return current_device(status); }
+
 extern "C" {
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
@@ -348,6 +350,8 @@ const char* fa_status_string(int code) {
     case FA_ERR_DEVICE_BOUNDS: return "a device-side bounds check failed";
     case FA_ERR_DRIVER: return "CUDA driver entry point or tensor-map encoding failed";
     case FA_ERR_CUDA: return "CUDA runtime error";
+    case FA_ERR_SCRATCH_CAPACITY:
+      return "problem needs more scratch than the no-allocation entry point's static array holds";
     default: return "unknown status code";
   }
 }

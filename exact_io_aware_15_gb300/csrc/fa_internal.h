@@ -69,4 +69,8 @@ struct CombineArgs {
 };
 cudaError_t launch_combine(const CombineArgs& a, int D, cudaStream_t stream);
 
+// The sm_103 check of the current device and its device status word, as used
+// by every entry point of fa_api.cu (returns an FA_* status code).
+int checked_current_device(unsigned int** status);
+
 }  // namespace fa

@@ -49,6 +49,7 @@ extern "C" {
 #define FA_ERR_DEVICE_BOUNDS    -5  /* a device-side index check failed */
 #define FA_ERR_DRIVER           -6  /* CUDA driver entry point or tensor-map encoding failed */
 #define FA_ERR_CUDA             -7  /* another CUDA runtime error (see fa_last_cuda_error) */
+#define FA_ERR_SCRATCH_CAPACITY -8  /* fa_decode_splitkv_noalloc: problem exceeds its static scratch */
 
 #define FA_DTYPE_BF16 0
 #define FA_DTYPE_F32  1
@@ -147,6 +148,34 @@ int fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
 int fa_combine_states(const float* part_m, const float* part_d,
                       const float* part_o, int rows, int num_splits, int D,
                       void* o, int o_dtype, float* lse, void* stream);
+
+/*
+ * Split-KV decode (both passes) without any device allocation, for callers
+ * that are handed only their input and output buffers and may not allocate:
+ * for example a host framework's plugin or custom-op interface that offers
+ * no workspace, or a serving loop that fixes all device memory at start-up
+ * because cudaMalloc can synchronise the device and fail under
+ * fragmentation.  The pages have no counterpart: this is a deployment form
+ * of fa_decode_splitkv + fa_combine_states, with the same arguments and
+ * results (o_dtype FA_DTYPE_BF16 or FA_DTYPE_F32, lse f32 [B, H]).
+ *
+ * The partial states live in one static device array of the library,
+ * 32 MiB per GPU that loads it (held until the process exits).  A problem
+ * needing more than that, i.e. B*H*num_splits*(D+2)*4 bytes > 32 MiB, is
+ * refused with FA_ERR_SCRATCH_CAPACITY before anything is launched.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, no allocation); make that first call before
+ *    capturing the stream.
+ *  - Nothing has to be cleared between calls: the first pass writes every
+ *    state the second pass reads.
+ *  - All calls on a device share the one array, so calls whose work
+ *    overlaps on the GPU (different streams, no ordering) race on it.
+ * The function calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+int fa_decode_splitkv_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                              const int* cu_seqlens_k, int total_kv_tokens, int B,
+                              int H, int D, int num_splits, float scale, void* o,
+                              int o_dtype, float* lse, void* stream);
 
 /*
  * Synchronises `stream`, then reads and clears the device status word of the

@@ -47,7 +47,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_strings(lib):
     import exact_io_aware_15_gb300 as fa
     assert fa.fa_status_string(0) == "ok"
-    for code in range(-7, 0):
+    for code in range(-8, 0):
         assert fa.fa_status_string(code) != "unknown status code"
 
 
