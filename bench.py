@@ -223,6 +223,48 @@ def cpu_baseline_leg():
 
 # ------------------------------------------------------------------ GPU arm
 
+def _time_launches(fn, iters: int, warmup: int = 2) -> float:
+    """Mean device milliseconds of fn() over `iters` back-to-back calls
+    (CUDA events on the current stream, after warm-up)."""
+    for _ in range(warmup):
+        fn()
+    st = torch.cuda.current_stream()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(st)
+    for _ in range(iters):
+        fn()
+    b.record(st)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / iters
+
+
+def other_configs(fa):
+    """The remaining workloads, each timed on its own after the main timed
+    region (not part of `value`): dense causal B=4 H=16 N=2048 D=128, the
+    ragged varlen prefill (65536 tokens, H=16, D=64 and 128) and the fp32
+    path (B=H=1, N=256, D=64)."""
+    out = {}
+    c2 = inp.config2(device="cuda")
+    ms = _time_launches(lambda: fa.fa_fwd(c2.q, c2.k, c2.v, c2.scale, True), 20)
+    out["dense_B4_H16_N2048_D128_causal"] = {
+        "tflops": prefill_flops(4, 16, 2048, 128) / (ms * 1e-3) / 1e12, "ms": ms}
+    for D in (64, 128):
+        c5 = inp.config5(D, device="cuda")
+        cu = c5.cu_seqlens.cuda()
+        flops = sum(2.0 * 16 * L * L * D for L in c5.meta["lens"])  # causal: 4 H L^2 D / 2
+        ms = _time_launches(lambda: fa.fa_fwd_varlen(c5.q, c5.k, c5.v, cu, c5.max_seqlen,
+                                                     c5.scale, True), 20)
+        out[f"varlen_T65536_H16_D{D}_causal"] = {
+            "tflops": flops / (ms * 1e-3) / 1e12, "ms": ms, "seqs": len(c5.meta["lens"])}
+    c1 = inp.config1(device="cuda")
+    ms = _time_launches(lambda: fa.fa_fwd_f32(c1.q, c1.k, c1.v, c1.scale, False), 200)
+    out["fp32_B1_H1_N256_D64"] = {"us": ms * 1e3,
+                                  "gflops": 4.0 * 256 * 256 * 64 / (ms * 1e-3) / 1e9}
+    return out
+
+
 def run_gpu(args, rank, world, dist):
     import exact_io_aware_15_gb300 as fa
     fa.load_library()
@@ -331,6 +373,7 @@ def run_gpu(args, rank, world, dist):
 
     if rank != 0:
         return 0
+    others = None if args.no_other_configs else other_configs(fa)
     cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline_leg()
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -354,6 +397,7 @@ def run_gpu(args, rank, world, dist):
                    "traffic": load_traffic("fa_decode_splitkv_kernel<128>",
                                            "exact_io_aware_15_gb300/csrc/decode.cu")},
         "cpu_baseline": cpu,
+        "other_configs": others,
         "e2e": e2e,
         "gpu_launches": 3 * K,
         "clocks": clk.summary(),
@@ -399,6 +443,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-configs", action="store_true")
     ap.add_argument("--profile-case", choices=["prefill", "decode"], default=None)
     args = ap.parse_args(argv)
     if args.profile_case:

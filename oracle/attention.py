@@ -66,15 +66,27 @@ def softmax_ref(s: np.ndarray) -> np.ndarray:
     return w / d[..., None]
 
 
-def attention_head_ref(q, k, v, scale, causal, rows=None):
+def window_mask(s: np.ndarray, q_pos: np.ndarray, k_pos: np.ndarray, window: int) -> np.ndarray:
+    """Sliding window: key j is hidden from query i when j <= i - window, so
+    with the causal mask query i sees keys i - window + 1 .. i."""
+    s = s.copy()
+    s[k_pos[None, :] <= q_pos[:, None] - int(window)] = -np.inf
+    return s
+
+
+def attention_head_ref(q, k, v, scale, causal, rows=None, window=None):
     """One head.  q [Nq, D], k/v [Nk, D] float64; Nq == Nk when causal.
     Returns O [R, D] and LSE [R] (natural log) for the query rows ``rows``
-    (all rows when None).  A fully masked row gives O = 0 and LSE = -inf."""
+    (all rows when None).  ``window`` (with causal) keeps only the last
+    ``window`` keys of each row.  A fully masked row gives O = 0 and
+    LSE = -inf."""
     nq = q.shape[0]
     rows = np.arange(nq) if rows is None else np.asarray(rows, dtype=np.int64)
     s = scores(q[rows], k, scale)
     if causal:
         s = causal_mask(s, rows, np.arange(k.shape[0]))
+    if window is not None:
+        s = window_mask(s, rows, np.arange(k.shape[0]), window)
     m, w, d = safe_softmax_stats(s)
     num = w @ v
     with np.errstate(invalid="ignore", divide="ignore"):
@@ -83,7 +95,7 @@ def attention_head_ref(q, k, v, scale, causal, rows=None):
     return o, lse
 
 
-def attention_ref(q, k, v, scale, causal, rows=None):
+def attention_ref(q, k, v, scale, causal, rows=None, window=None):
     """Dense [B, H, N, D] inputs (any dtype, converted exactly to float64).
     Returns O [B, H, R, D] and LSE [B, H, R] in float64, looping over heads so
     that at most one head's score matrix is held at a time."""
@@ -95,7 +107,7 @@ def attention_ref(q, k, v, scale, causal, rows=None):
     for b in range(B):
         for h in range(H):
             O[b, h], L[b, h] = attention_head_ref(q[b, h], k[b, h], v[b, h],
-                                                  scale, causal, rows)
+                                                  scale, causal, rows, window)
     return O, L
 
 
@@ -142,6 +154,59 @@ def decode_ref(q, k_cache, v_cache, cu_seqlens_k, scale, batch=None, heads=None)
                                       scale, False)
             O[b, h], LSE[b, h] = o[0], l[0]
     return O, LSE
+
+
+def paged_kv_gather(k_pages, v_pages, block_table, seqlen: int, b: int):
+    """The KV cache of sequence b as contiguous [L, H_kv, D] arrays: key t
+    lives in page block_table[b][t // page_size], row t % page_size.
+    Pages are [num_pages, page_size, H_kv, D]."""
+    page = k_pages.shape[1]
+    idx = np.arange(seqlen)
+    pages = np.asarray(block_table)[b][idx // page]
+    return k_pages[pages, idx % page], v_pages[pages, idx % page]
+
+
+def decode_paged_ref(q, k_pages, v_pages, block_table, seqlens, scale,
+                     batch=None, heads=None):
+    """One query row per sequence against its paged KV cache, with grouped
+    query heads: query head h reads KV head h // (H / H_kv).
+    q [B, H, D]; pages [P, page_size, H_kv, D]; block_table [B, max_blocks];
+    seqlens [B].  Returns O [B, H, D], LSE [B, H] (unselected items NaN)."""
+    q, kp, vp = to_f64(q), to_f64(k_pages), to_f64(v_pages)
+    B, H, D = q.shape
+    Hkv = kp.shape[2]
+    group = H // Hkv
+    O = np.full((B, H, D), np.nan)
+    LSE = np.full((B, H), np.nan)
+    for b in (range(B) if batch is None else batch):
+        kc, vc = paged_kv_gather(kp, vp, block_table, int(seqlens[b]), b)
+        for h in (range(H) if heads is None else heads):
+            o, l = attention_head_ref(q[b, h][None, :], kc[:, h // group],
+                                      vc[:, h // group], scale, False)
+            O[b, h], LSE[b, h] = o[0], l[0]
+    return O, LSE
+
+
+def chunk_states_paged_ref(q, k_pages, v_pages, block_table, seqlens, num_splits,
+                           scale, batch=None, heads=None):
+    """Base-2 chunk states of split-KV decode over a paged cache with grouped
+    query heads (chunking as chunk_bounds).  Shapes as chunk_states_ref."""
+    q, kp, vp = to_f64(q), to_f64(k_pages), to_f64(v_pages)
+    B, H, D = q.shape
+    group = H // kp.shape[2]
+    S = int(num_splits)
+    M = np.full((B, H, S), np.nan)
+    Dn = np.full((B, H, S), np.nan)
+    Ot = np.full((B, H, S, D), np.nan)
+    for b in (range(B) if batch is None else batch):
+        L = int(seqlens[b])
+        kc, vc = paged_kv_gather(kp, vp, block_table, L, b)
+        for h in (range(H) if heads is None else heads):
+            for c, (a, e) in enumerate(chunk_bounds(L, S)):
+                sig = (kc[a:e, h // group] @ q[b, h]) * (float(scale) * LOG2E)
+                M[b, h, c], Dn[b, h, c], Ot[b, h, c] = row_state(
+                    sig, vc[a:e, h // group], base=2.0)
+    return M, Dn, Ot
 
 
 # ---------------------------------------------------------------------------
