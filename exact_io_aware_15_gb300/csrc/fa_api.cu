@@ -122,7 +122,7 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, i
     return FA_ERR_INVALID_ARG;
   const long long BH = static_cast<long long>(B) * H;
   const long long mblocks = (static_cast<long long>(N) + 127) / 128;
-  if (BH > 0x7fffffffLL || mblocks > 65535) return FA_ERR_INVALID_ARG;
+  if (BH > 0x7fffffffLL || BH * mblocks > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   unsigned int* status = nullptr;
   int rc = current_device(&status);
   if (rc != FA_OK) return rc;
@@ -223,7 +223,7 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
     return FA_ERR_INVALID_ARG;
   const long long SH = static_cast<long long>(num_seqs) * H;
   const long long mblocks = (static_cast<long long>(max_seqlen) + 127) / 128;
-  if (SH > 0x7fffffffLL || mblocks > 65535) return FA_ERR_INVALID_ARG;
+  if (SH > 0x7fffffffLL || SH * mblocks > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   unsigned int* status = nullptr;
   int rc = current_device(&status);
   if (rc != FA_OK) return rc;

@@ -19,10 +19,13 @@
 //               TMEM (TS form).  Issue order QK_0, QK_1, PV_0, QK_2, PV_1, ...
 //               so QK_{j+1} overlaps the softmax of tile j.
 //   warps 2..5  softmax: thread t owns row 32*(warp%4) + lane; per tile it
-//               loads its S row, masks, takes the row max, computes
-//               p = 2^(sigma - m_new), rounds P to bf16 into TMEM (over the
-//               first half of its S buffer), rescales its O row in TMEM by
-//               2^(m_old - m_new) once PV_{j-1} has landed, then signals.
+//               loads its raw S row, masks, takes the row max (3-input max
+//               instructions, four independent chains), computes
+//               p = 2^(s c - m_new) with one packed fused multiply-add per
+//               pair of columns, rounds P to bf16 into TMEM (over the first
+//               half of its S buffer), sums p with packed adds, and, when a
+//               row of its warp raised its maximum, waits for PV_{j-1} and
+//               rescales its O row in TMEM by 2^(m_old - m_new); then signals.
 //               Epilogue: O / d in fp32, LSE = ln2 (m + log2 d), stores.
 //
 // Shared memory (1024-byte aligned): Q tile, STAGES x (K tile, V tile), the
@@ -72,6 +75,13 @@ struct TcCfg {
   static constexpr int SOFTMAX_THREADS = 128;
 };
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // Bounded wait used only while unwinding after an abort: ignores the abort
 // flag (the copies or MMAs it waits for are already in flight) but still
 // gives up after a short time.
@@ -90,9 +100,20 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
   using C = TcCfg<D>;
   extern __shared__ uint8_t smem_raw[];
 
-  // ---- which tile: heaviest query tiles first (grid.y reversed) ----
-  const int mb = args.num_mblocks - 1 - static_cast<int>(blockIdx.y);
-  const int bh = static_cast<int>(blockIdx.x);
+  // ---- which tile ----
+  // A 1-D grid of (heads x query tiles).  Heads are taken in groups of four;
+  // inside a group the heaviest query tiles (the longest causal KV ranges)
+  // come first.  A group's K/V (4 heads x 8 MB at N = 16384, D = 128) stays
+  // in L2 while its tiles run, and the light tiles fill the tail.
+  const int nmb = args.num_mblocks;
+  const int BHt = static_cast<int>(gridDim.x) / nmb;
+  const long long lin = blockIdx.x;
+  const long long per_group = 4LL * nmb;
+  const int g = static_cast<int>(lin / per_group);
+  const int gsize = min(4, BHt - g * 4);
+  const int rr = static_cast<int>(lin - g * per_group);
+  const int mb = nmb - 1 - rr / gsize;
+  const int bh = g * 4 + rr % gsize;
   const int h = bh % args.H;
   const int seq = bh / args.H;
   const bool varlen = args.cu_seqlens != nullptr;
@@ -283,7 +304,10 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
     const int r = quarter * 32 + lane;
     const int qpos = mb * C::BM + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const float c = args.scale_log2;
+    // sigma = s * c; with c = 0 every visible score is 0 and the masked ones
+    // -inf, which c = 1 applied to (0 | -inf) reproduces without 0 * inf.
+    const bool zero_scale = args.scale_log2 == 0.f;
+    const float c = zero_scale ? 1.f : args.scale_log2;
     float m = -INFINITY;
     float dsum = 0.f;
     bool ok = true;
@@ -303,10 +327,10 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
         uint32_t raw[64];
         tmem_ld64(s_t, raw);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) t[i] = __uint_as_float(raw[i]) * c;
+        for (int i = 0; i < 64; ++i) t[i] = __uint_as_float(raw[i]);
         tmem_ld64(s_t + 64, raw);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) t[64 + i] = __uint_as_float(raw[i]) * c;
+        for (int i = 0; i < 64; ++i) t[64 + i] = __uint_as_float(raw[i]);
       }
       const int kbase = j * C::BN;
       if ((args.causal && j == mb) || kbase + C::BN > L) {
@@ -316,37 +340,44 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
         for (int i = 0; i < 128; ++i)
           if (i >= lim) t[i] = -INFINITY;
       }
-      float mx = t[0];
+      if (zero_scale) {
 #pragma unroll
-      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, t[i]);
+        for (int i = 0; i < 128; ++i) t[i] = (t[i] == -INFINITY) ? -INFINITY : 0.f;
+      }
+      float mx0 = fmax3(t[0], t[1], t[2]), mx1 = fmax3(t[3], t[4], t[5]);
+      float mx2 = fmax3(t[6], t[7], t[8]), mx3 = fmax3(t[9], t[10], t[11]);
+#pragma unroll
+      for (int i = 12; i < 124; i += 8) {
+        mx0 = fmax3(mx0, t[i], t[i + 1]);
+        mx1 = fmax3(mx1, t[i + 2], t[i + 3]);
+        mx2 = fmax3(mx2, t[i + 4], t[i + 5]);
+        mx3 = fmax3(mx3, t[i + 6], t[i + 7]);
+      }
+      mx0 = fmax3(mx0, t[124], t[125]);
+      mx1 = fmax3(mx1, t[126], t[127]);
+      const float mx = fmaxf(fmax3(mx0, mx1, mx2), mx3) * c;
       const float m_new = fmaxf(m, mx);
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = (m_new == m) ? 1.f : ex2_approx(m - m_use);
-
-      float rs = 0.f;
-      {
+      const float2 cc = make_float2(c, c), nm = make_float2(-m_use, -m_use);
+      float2 a0 = make_float2(0.f, 0.f), a1 = a0;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2_approx(t[2 * i] - m_use);
-          const float p1 = ex2_approx(t[2 * i + 1] - m_use);
-          rs += p0 + p1;
-          pk[i] = pack_bf16x2(p0, p1);
+          const float2 x = __ffma2_rn(make_float2(t[64 * h + 2 * i], t[64 * h + 2 * i + 1]), cc, nm);
+          const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          if (i & 1) a1 = __fadd2_rn(a1, p); else a0 = __fadd2_rn(a0, p);
+          pk[i] = pack_bf16x2(p.x, p.y);
         }
-        tmem_st32(s_t, pk);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2_approx(t[64 + 2 * i] - m_use);
-          const float p1 = ex2_approx(t[64 + 2 * i + 1] - m_use);
-          rs += p0 + p1;
-          pk[i] = pack_bf16x2(p0, p1);
-        }
-        tmem_st32(s_t + 32, pk);
+        tmem_st32(s_t + 32u * h, pk);
       }
-      dsum = dsum * alpha + rs;
+      const float2 aa = __fadd2_rn(a0, a1);
+      dsum = dsum * alpha + (aa.x + aa.y);
       m = m_new;
 
-      if (j > 0) {
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         // o <- alpha * o needs PV_{j-1} to have landed in TMEM.
         const bool w2 = mbar_wait(bar(C::B_O_DONE), (j - 1) & 1, abort_flag, args.status);
         if (__any_sync(0xffffffffu, !w2)) {
@@ -452,7 +483,7 @@ static cudaError_t launch_tc_impl(const TcMaps& maps, const TcFwdArgs& a, int gr
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  dim3 grid(static_cast<unsigned>(grid_x), static_cast<unsigned>(a.num_mblocks));
+  dim3 grid(static_cast<unsigned>(grid_x * a.num_mblocks));
   fa_fwd_tc_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(maps.q, maps.k, maps.v, a);
   return cudaGetLastError();
 }
