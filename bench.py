@@ -258,6 +258,26 @@ def other_configs(fa):
                                                      c5.scale, True), 20)
         out[f"varlen_T65536_H16_D{D}_causal"] = {
             "tflops": flops / (ms * 1e-3) / 1e12, "ms": ms, "seqs": len(c5.meta["lens"])}
+    # causal sliding window, B=1 H=32 N=16384 D=128, window 4096
+    cw = inp.dense(1, 32, 16384, 128, seed=3, causal=True, qk_std=3.0, device="cuda")
+    ms = _time_launches(lambda: fa.fa_fwd_window(cw.q, cw.k, cw.v, 4096, cw.scale), 10)
+    wf = 32 * 4.0 * 128 * sum(min(i + 1, 4096) for i in range(16384))
+    out["window4096_B1_H32_N16384_D128"] = {"tflops": wf / (ms * 1e-3) / 1e12, "ms": ms}
+    del cw
+    # paged KV decode with grouped query heads: the decode lengths, H=32 over
+    # H_kv=8, pages of 64 keys
+    pc = inp.paged_decode(64, 32, 8, 128, 64, seed=4, num_splits=16, device="cuda")
+    tab, sl = pc.block_table.cuda(), pc.seqlens.cuda()
+
+    def paged():
+        pm, pd, po = fa.fa_decode_paged_splitkv(pc.q, pc.k_pages, pc.v_pages, tab, sl, 16,
+                                                pc.scale)
+        fa.fa_combine_states(pm, pd, po)
+    ms = _time_launches(paged, 10)
+    kvb = float(sum(pc.meta["lens"])) * 8 * 128 * 2 * 2
+    out["paged_gqa_decode_B64_H32_Hkv8_page64"] = {"gbs": kvb / (ms * 1e-3) / 1e9, "ms": ms,
+                                                  "kv_bytes": kvb}
+    del pc
     c1 = inp.config1(device="cuda")
     ms = _time_launches(lambda: fa.fa_fwd_f32(c1.q, c1.k, c1.v, c1.scale, False), 200)
     out["fp32_B1_H1_N256_D64"] = {"us": ms * 1e3,

@@ -40,10 +40,13 @@ SIGNATURES = {
     "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "fa_fwd_f32": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "fa_fwd_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _I, _P]),
+    "fa_fwd_window": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "fa_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
     "fa_decode_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
     "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
     "fa_combine_states": (_I, [_P, _P, _P, _I, _I, _I, _P, _I, _P, _P]),
+    "fa_decode_paged_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F,
+                                     _P, _P, _P, _P]),
     "fa_decode_splitkv_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _I, _P,
                                        _P]),
     "fa_check_device_status": (_I, [_P]),
@@ -163,6 +166,23 @@ def fa_fwd(q, k, v, scale=None, causal=False, o=None, lse=None):
     return o, lse
 
 
+def fa_fwd_window(q, k, v, window, scale=None, o=None, lse=None):
+    """Causal sliding-window forward (bf16): query i sees keys i-window+1 .. i."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, 4)
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must have the same shape [B, H, N, D]")
+    B, H, N, D = q.shape
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    _need(o, "o", torch.bfloat16, 4)
+    _need(lse, "lse", torch.float32, 3)
+    rc = load_library().fa_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                      B, H, N, D, _scale(scale, D), int(window), _stream(q))
+    _check(rc, "fa_fwd_window")
+    return o, lse
+
+
 def fa_fwd_f32(q, k, v, scale=None, causal=False, o=None, lse=None):
     """Dense fp32 forward on the CUDA cores (fa_fwd_f32)."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
@@ -238,6 +258,36 @@ def fa_decode_splitkv(q, k_cache, v_cache, cu_seqlens_k, num_splits, scale=None,
     return part_m, part_d, part_o
 
 
+def fa_decode_paged_splitkv(q, k_pages, v_pages, block_table, seqlens, num_splits,
+                            scale=None, part_m=None, part_d=None, part_o=None):
+    """Split-KV first pass over a paged cache with grouped query heads.
+    q [B, H, D] bf16; pages [P, page_size, H_kv, D] bf16; block_table int32
+    [B, max_blocks] and seqlens int32 [B] on the device.  Returns the base-2
+    chunk states (part_m, part_d [B, H, S], part_o [B, H, S, D])."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_pages, "k_pages", torch.bfloat16, 4)
+    _need(v_pages, "v_pages", torch.bfloat16, 4)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seqlens, "seqlens", torch.int32, 1)
+    B, H, D = q.shape
+    P, page, Hkv, Dk = k_pages.shape
+    if v_pages.shape != k_pages.shape or Dk != D:
+        raise ValueError("pages must be [P, page_size, H_kv, D] like q's head dim")
+    if block_table.shape[0] != B or seqlens.numel() != B:
+        raise ValueError("block_table and seqlens need one row per sequence")
+    S = int(num_splits)
+    dev = q.device
+    part_m = torch.empty((B, H, S), dtype=torch.float32, device=dev) if part_m is None else part_m
+    part_d = torch.empty((B, H, S), dtype=torch.float32, device=dev) if part_d is None else part_d
+    part_o = torch.empty((B, H, S, D), dtype=torch.float32, device=dev) if part_o is None else part_o
+    rc = load_library().fa_decode_paged_splitkv(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seqlens), P, page,
+        block_table.shape[1], B, H, Hkv, D, S, _scale(scale, D), _ptr(part_m), _ptr(part_d),
+        _ptr(part_o), _stream(q))
+    _check(rc, "fa_decode_paged_splitkv")
+    return part_m, part_d, part_o
+
+
 def fa_combine_states(part_m, part_d, part_o, o_dtype=torch.bfloat16, o=None, lse=None):
     """Split-KV second pass over states [..., S] / [..., S, D] (fp32).
     Returns (o [..., D] in o_dtype, lse [...] fp32)."""
@@ -307,8 +357,9 @@ def decode(q, k_cache, v_cache, cu_seqlens_k, num_splits=16, scale=None,
 
 
 __all__ = [
-    "fa_fwd", "fa_fwd_f32", "fa_fwd_ex", "fa_fwd_varlen", "fa_decode_workspace_bytes",
+    "fa_fwd", "fa_fwd_f32", "fa_fwd_ex", "fa_fwd_window", "fa_fwd_varlen", "fa_decode_workspace_bytes",
     "fa_decode_splitkv", "fa_combine_states", "fa_decode_splitkv_noalloc",
+    "fa_decode_paged_splitkv",
     "fa_check_device_status",
     "fa_status_string", "decode", "load_library", "FAError", "LIB_PATH",
 ]

@@ -8,13 +8,13 @@
 // of sigma = s * log2 e, d = sum 2^(sigma - m), o = sum 2^(sigma - m) v.
 //
 // The pass streams the whole KV cache once, so it is bound by HBM bandwidth.
-// Grid (num_splits, ceil(H / 8), B); a CTA of 8 warps covers 8 consecutive
-// heads of one (sequence, chunk), so for each key the CTA reads 8 adjacent
-// 256-byte rows (2 KB contiguous at D = 128).  Within a warp, D/8 lanes cover
-// one key row with 16-byte loads and the warp covers 32/(D/8) keys per load;
-// every lane keeps 8 loads of K and 8 of V in flight.  Each lane group folds
-// its keys into its own state; the groups are merged by warp shuffles at the
-// end (the same merge, once more).
+// Within a warp, D/8 lanes cover one key row with 16-byte loads and the warp
+// covers 32/(D/8) keys per load; every lane keeps 8 loads of K and 8 of V in
+// flight.  Each lane group folds its keys into its own state; the groups are
+// merged by warp shuffles at the end (the same merge, once more).  Two cache
+// layouts share that fold: a packed [T_k, H, D] cache with cu_seqlens, and a
+// paged cache (pages [P, page_size, H_kv, D] reached through a block table)
+// whose KV heads may each serve a group of query heads.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -38,46 +38,68 @@ __device__ __forceinline__ float2 bf16x2_to_f2(uint32_t u) {
   return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
 }
 
-template <int D>
-__global__ void __launch_bounds__(256) fa_decode_splitkv_kernel(const DecodeArgs a) {
+// Where the key rows of one (sequence, KV head) live.  `row` gives the element
+// offset of key `key` from the warp's base pointers, or false for a key whose
+// page index is out of range.
+struct ContigRows {  // packed [T_k, H, D] caches
+  const uint16_t* k;
+  const uint16_t* v;
+  size_t stride;  // elements between consecutive keys (H * D)
+  __device__ __forceinline__ bool row(int key, size_t& off) const {
+    off = static_cast<size_t>(key) * stride;
+    return true;
+  }
+  // streamed once: no L1 allocation
+  __device__ __forceinline__ uint4 load(const uint16_t* p) const { return ld_stream_u4(p); }
+};
+
+struct PagedRows {  // pages [num_pages, page_size, H_kv, D] and a block table
+  const uint16_t* k;
+  const uint16_t* v;
+  const int* table;  // this sequence's row of the block table
+  int page_shift;    // log2(page_size)
+  int num_pages;
+  size_t page_stride;  // elements per page (page_size * H_kv * D)
+  size_t row_stride;   // elements between keys of one page (H_kv * D)
+  __device__ __forceinline__ bool row(int key, size_t& off) const {
+    const int pg = __ldg(table + (key >> page_shift));
+    if (pg < 0 || pg >= num_pages) return false;
+    off = static_cast<size_t>(pg) * page_stride +
+          static_cast<size_t>(key & ((1 << page_shift) - 1)) * row_stride;
+    return true;
+  }
+  // the query heads of one KV head read the same rows: keep them in L1
+  __device__ __forceinline__ uint4 load(const uint16_t* p) const {
+    return __ldg(reinterpret_cast<const uint4*>(p));
+  }
+};
+
+// Folds keys [k0, k1) of one (sequence, query head) into the base-2 state
+// (m, d, o) and writes it to slot `out` of the partial-state arrays; an
+// empty range writes the identity (-inf, 0, 0).  One warp: D/8 lanes per
+// key row, 16-byte loads, 8 loads of K and 8 of V in flight per lane.
+template <int D, class Rows>
+__device__ __forceinline__ void fold_chunk(const Rows& rows, const uint16_t* qrow,
+                                           float scale_log2, int k0, int k1, size_t out,
+                                           float* part_m, float* part_d, float* part_o,
+                                           unsigned int* status) {
   constexpr int LPR = D / 8;         // lanes per key row (8 bf16 = 16 B per lane)
   constexpr int GROUPS = 32 / LPR;   // keys per warp-wide load
   constexpr int U = 8;               // loads in flight per lane per operand
   constexpr int KPI = GROUPS * U;    // keys per iteration
-
-  const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int c = blockIdx.x;
-  const int h = blockIdx.y * 8 + warp;
-  const int b = blockIdx.z;
-  const int S = a.S;
-  const int H = a.H;
-
-  const int k_begin = __ldg(a.cu_seqlens_k + b);
-  const int k_end = __ldg(a.cu_seqlens_k + b + 1);
-  if (k_begin < 0 || k_end < k_begin || k_end > a.total_kv) {
-    if (threadIdx.x == 0) atomicOr(a.status, kStatusBounds);
-    return;
-  }
-  if (h >= H) return;
-  const int L = k_end - k_begin;
-  const int size = (L + S - 1) / S;
-  const int k0 = min(L, c * size);
-  const int k1 = min(L, (c + 1) * size);
-  const size_t out = (static_cast<size_t>(b) * H + h) * S + c;
-
   const int g = lane / LPR;
   const int dl = lane % LPR;
 
   if (k0 >= k1) {  // empty chunk: the identity (-inf, 0, 0)
     if (g == 0) {
-      float4* po = reinterpret_cast<float4*>(a.part_o + out * D + dl * 8);
+      float4* po = reinterpret_cast<float4*>(part_o + out * D + dl * 8);
       po[0] = make_float4(0.f, 0.f, 0.f, 0.f);
       po[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     if (lane == 0) {
-      a.part_m[out] = -INFINITY;
-      a.part_d[out] = 0.f;
+      part_m[out] = -INFINITY;
+      part_d[out] = 0.f;
     }
     return;
   }
@@ -85,38 +107,36 @@ __global__ void __launch_bounds__(256) fa_decode_splitkv_kernel(const DecodeArgs
   // q pre-multiplied by scale*log2(e): the dot product is sigma directly.
   float qv[8];
   {
-    const uint4 qr = *reinterpret_cast<const uint4*>(
-        static_cast<const uint16_t*>(a.q) + (static_cast<size_t>(b) * H + h) * D + dl * 8);
+    const uint4 qr = *reinterpret_cast<const uint4*>(qrow + dl * 8);
     const uint32_t w[4] = {qr.x, qr.y, qr.z, qr.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float2 f = bf16x2_to_f2(w[i]);
-      qv[2 * i] = f.x * a.scale_log2;
-      qv[2 * i + 1] = f.y * a.scale_log2;
+      qv[2 * i] = f.x * scale_log2;
+      qv[2 * i + 1] = f.y * scale_log2;
     }
   }
-
-  const size_t row_stride = static_cast<size_t>(H) * D;  // elements between keys
-  const uint16_t* kbase =
-      static_cast<const uint16_t*>(a.k_cache) + static_cast<size_t>(k_begin) * row_stride +
-      static_cast<size_t>(h) * D + dl * 8;
-  const uint16_t* vbase =
-      static_cast<const uint16_t*>(a.v_cache) + static_cast<size_t>(k_begin) * row_stride +
-      static_cast<size_t>(h) * D + dl * 8;
+  const uint16_t* kbase = rows.k + dl * 8;
+  const uint16_t* vbase = rows.v + dl * 8;
 
   float m = -INFINITY, dsum = 0.f;
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  bool bad = false;
 
   for (int kb = k0; kb < k1; kb += KPI) {
     uint4 kr[U], vr[U];
+    bool vis[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int key = kb + u * GROUPS + g;
-      if (key < k1) {
-        kr[u] = ld_stream_u4(kbase + static_cast<size_t>(key) * row_stride);
-        vr[u] = ld_stream_u4(vbase + static_cast<size_t>(key) * row_stride);
+      size_t off = 0;
+      vis[u] = key < k1 && rows.row(key, off);
+      bad |= key < k1 && !vis[u];
+      if (vis[u]) {
+        kr[u] = rows.load(kbase + off);
+        vr[u] = rows.load(vbase + off);
       } else {
         kr[u] = make_uint4(0u, 0u, 0u, 0u);
         vr[u] = kr[u];
@@ -143,8 +163,7 @@ __global__ void __launch_bounds__(256) fa_decode_splitkv_kernel(const DecodeArgs
     float mx = -INFINITY;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int key = kb + u * GROUPS + g;
-      if (key >= k1) t[u] = -INFINITY;
+      if (!vis[u]) t[u] = -INFINITY;  // the identity's m
       mx = fmaxf(mx, t[u]);
     }
     const float m_new = fmaxf(m, mx);
@@ -168,6 +187,7 @@ __global__ void __launch_bounds__(256) fa_decode_splitkv_kernel(const DecodeArgs
     dsum = dsum * alpha + rs;
     m = m_new;
   }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(status, kStatusBounds);
 
   // Merge the lane groups' states (each group saw a disjoint subset of keys).
 #pragma unroll
@@ -199,14 +219,95 @@ __global__ void __launch_bounds__(256) fa_decode_splitkv_kernel(const DecodeArgs
   }
 
   if (g == 0) {
-    float4* po = reinterpret_cast<float4*>(a.part_o + out * D + dl * 8);
+    float4* po = reinterpret_cast<float4*>(part_o + out * D + dl * 8);
     po[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
     po[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
   }
   if (lane == 0) {
-    a.part_m[out] = m;
-    a.part_d[out] = dsum;
+    part_m[out] = m;
+    part_d[out] = dsum;
   }
+}
+
+// Chunk c of a length-L sequence: keys [c*ceil(L/S), min(L, (c+1)*ceil(L/S))).
+__device__ __forceinline__ void chunk_range(int L, int S, int c, int& k0, int& k1) {
+  const int size = (L + S - 1) / S;
+  k0 = min(L, c * size);
+  k1 = min(L, (c + 1) * size);
+}
+
+// Grid (num_splits, ceil(H / 8), B); a CTA of 8 warps covers 8 consecutive
+// heads of one (sequence, chunk), so for each key the CTA reads 8 adjacent
+// 256-byte rows (2 KB contiguous at D = 128).
+template <int D>
+__global__ void __launch_bounds__(256) fa_decode_splitkv_kernel(const DecodeArgs a) {
+  const int warp = threadIdx.x >> 5;
+  const int c = blockIdx.x;
+  const int h = blockIdx.y * 8 + warp;
+  const int b = blockIdx.z;
+  const int S = a.S;
+  const int H = a.H;
+
+  const int k_begin = __ldg(a.cu_seqlens_k + b);
+  const int k_end = __ldg(a.cu_seqlens_k + b + 1);
+  if (k_begin < 0 || k_end < k_begin || k_end > a.total_kv) {
+    if (threadIdx.x == 0) atomicOr(a.status, kStatusBounds);
+    return;
+  }
+  if (h >= H) return;
+  int k0, k1;
+  chunk_range(k_end - k_begin, S, c, k0, k1);
+  const size_t stride = static_cast<size_t>(H) * D;
+  const size_t base = static_cast<size_t>(k_begin) * stride + static_cast<size_t>(h) * D;
+  ContigRows rows{static_cast<const uint16_t*>(a.k_cache) + base,
+                  static_cast<const uint16_t*>(a.v_cache) + base, stride};
+  const uint16_t* qrow =
+      static_cast<const uint16_t*>(a.q) + (static_cast<size_t>(b) * H + h) * D;
+  fold_chunk<D>(rows, qrow, a.scale_log2, k0, k1, (static_cast<size_t>(b) * H + h) * S + c,
+                a.part_m, a.part_d, a.part_o, a.status);
+}
+
+// Paged cache with grouped query heads: query head h reads KV head
+// h / (H / H_kv); the CTA's 8 warps are 8 consecutive query heads, so warps
+// of one group read the same rows (served by L1 after the first).
+template <int D>
+__global__ void __launch_bounds__(256) fa_decode_paged_kernel(const PagedDecodeArgs a) {
+  const int warp = threadIdx.x >> 5;
+  const int c = blockIdx.x;
+  const int h = blockIdx.y * 8 + warp;
+  const int b = blockIdx.z;
+  const int L = __ldg(a.seqlens + b);
+  if (L < 0 || L > a.max_blocks * a.page_size) {
+    if (threadIdx.x == 0) atomicOr(a.status, kStatusBounds);
+    return;
+  }
+  if (h >= a.H) return;
+  const int hk = h / (a.H / a.Hkv);
+  int k0, k1;
+  chunk_range(L, a.S, c, k0, k1);
+  const size_t row_stride = static_cast<size_t>(a.Hkv) * D;
+  PagedRows rows{static_cast<const uint16_t*>(a.k_pages) + static_cast<size_t>(hk) * D,
+                 static_cast<const uint16_t*>(a.v_pages) + static_cast<size_t>(hk) * D,
+                 a.block_table + static_cast<size_t>(b) * a.max_blocks,
+                 __ffs(a.page_size) - 1,
+                 a.num_pages,
+                 static_cast<size_t>(a.page_size) * row_stride,
+                 row_stride};
+  const uint16_t* qrow =
+      static_cast<const uint16_t*>(a.q) + (static_cast<size_t>(b) * a.H + h) * D;
+  fold_chunk<D>(rows, qrow, a.scale_log2, k0, k1,
+                (static_cast<size_t>(b) * a.H + h) * a.S + c, a.part_m, a.part_d, a.part_o,
+                a.status);
+}
+
+cudaError_t launch_decode_paged(const PagedDecodeArgs& a, int D, cudaStream_t stream) {
+  dim3 grid(static_cast<unsigned>(a.S), static_cast<unsigned>((a.H + 7) / 8),
+            static_cast<unsigned>(a.B));
+  if (D == 128)
+    fa_decode_paged_kernel<128><<<grid, 256, 0, stream>>>(a);
+  else
+    fa_decode_paged_kernel<64><<<grid, 256, 0, stream>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_decode_splitkv(const DecodeArgs& a, int D, cudaStream_t stream) {

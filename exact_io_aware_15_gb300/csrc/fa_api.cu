@@ -112,7 +112,7 @@ int launched(cudaError_t e) {
 }
 
 int fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-             int N, int D, float scale, int causal, int o_f32, void* stream) {
+             int N, int D, float scale, int causal, int o_f32, void* stream, int window = 0) {
   if (B >= 0 && H >= 0 && N >= 0 && (B == 0 || H == 0 || N == 0) &&
       (D == 64 || D == 128) && good_scale(scale))
     return FA_OK;  // empty problem: nothing to read or write
@@ -141,6 +141,7 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, i
   a.N = N;
   a.num_mblocks = static_cast<int>(mblocks);
   a.causal = causal ? 1 : 0;
+  a.window = window;
   a.scale_log2 = scale_log2(scale);
   a.cu_seqlens = nullptr;
   a.o = o;
@@ -190,6 +191,12 @@ extern "C" {
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
            int N, int D, float scale, int causal, void* stream) {
   return fwd_bf16(q, k, v, o, lse, B, H, N, D, scale, causal, 0, stream);
+}
+
+int fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                  int H, int N, int D, float scale, int window, void* stream) {
+  if (window < 1) return FA_ERR_INVALID_ARG;
+  return fwd_bf16(q, k, v, o, lse, B, H, N, D, scale, 1, 0, stream, window);
 }
 
 int fa_fwd_f32(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
@@ -242,6 +249,7 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
   a.N = 0;
   a.num_mblocks = static_cast<int>(mblocks);
   a.causal = causal ? 1 : 0;
+  a.window = 0;
   a.scale_log2 = scale_log2(scale);
   a.cu_seqlens = cu_seqlens;
   a.total_tokens = total_tokens;
@@ -292,6 +300,44 @@ int fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
   a.part_o = part_o;
   a.status = status;
   return launched(fa::launch_decode_splitkv(a, D, static_cast<cudaStream_t>(stream)));
+}
+
+int fa_decode_paged_splitkv(const void* q, const void* k_pages, const void* v_pages,
+                            const int* block_table, const int* seqlens, int num_pages,
+                            int page_size, int max_blocks, int B, int H, int H_kv, int D,
+                            int num_splits, float scale, float* part_m, float* part_d,
+                            float* part_o, void* stream) {
+  if (B < 0 || H < 0 || H_kv < 1 || num_pages < 0 || page_size < 1 ||
+      (page_size & (page_size - 1)) != 0 || max_blocks < 0 ||
+      (D != 64 && D != 128) || num_splits < 1 || num_splits > 256 || B > 65535 ||
+      H > 8 * 65535 || !good_scale(scale) || (H > 0 && H % H_kv != 0))
+    return FA_ERR_INVALID_ARG;
+  if (B == 0 || H == 0) return FA_OK;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned4(block_table) ||
+      !aligned4(seqlens) || !aligned4(part_m) || !aligned4(part_d) || !aligned16(part_o))
+    return FA_ERR_INVALID_ARG;
+  unsigned int* status = nullptr;
+  int rc = current_device(&status);
+  if (rc != FA_OK) return rc;
+  fa::PagedDecodeArgs a{};
+  a.q = q;
+  a.k_pages = k_pages;
+  a.v_pages = v_pages;
+  a.block_table = block_table;
+  a.seqlens = seqlens;
+  a.num_pages = num_pages;
+  a.page_size = page_size;
+  a.max_blocks = max_blocks;
+  a.B = B;
+  a.H = H;
+  a.Hkv = H_kv;
+  a.S = num_splits;
+  a.scale_log2 = scale_log2(scale);
+  a.part_m = part_m;
+  a.part_d = part_d;
+  a.part_o = part_o;
+  a.status = status;
+  return launched(fa::launch_decode_paged(a, D, static_cast<cudaStream_t>(stream)));
 }
 
 int fa_combine_states(const float* part_m, const float* part_d, const float* part_o, int rows,

@@ -13,6 +13,7 @@ struct TcFwdArgs {
   int N;             // dense: sequence length (queries = keys); unused for varlen
   int num_mblocks;   // 128-row query tiles per sequence (grid.y)
   int causal;
+  int window;        // > 0: causal sliding window, query i sees keys i-window+1 .. i
   float scale_log2;  // softmax scale * log2(e)
   const int* cu_seqlens;  // varlen token offsets [num_seqs + 1]; NULL when dense
   int total_tokens;       // varlen: T
@@ -57,6 +58,22 @@ struct DecodeArgs {
   unsigned int* status;
 };
 cudaError_t launch_decode_splitkv(const DecodeArgs& a, int D, cudaStream_t stream);
+
+struct PagedDecodeArgs {
+  const void* q;         // [B, H, D]
+  const void* k_pages;   // [num_pages, page_size, Hkv, D]
+  const void* v_pages;
+  const int* block_table;  // [B, max_blocks]
+  const int* seqlens;      // [B]
+  int num_pages, page_size, max_blocks;
+  int B, H, Hkv, S;
+  float scale_log2;
+  float* part_m;
+  float* part_d;
+  float* part_o;
+  unsigned int* status;
+};
+cudaError_t launch_decode_paged(const PagedDecodeArgs& a, int D, cudaStream_t stream);
 
 struct CombineArgs {
   const float* part_m;

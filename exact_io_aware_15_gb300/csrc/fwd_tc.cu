@@ -134,6 +134,15 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
   if (mb * C::BM >= L) return;  // no query row of this sequence in the tile
   int n_kv = (L + C::BN - 1) / C::BN;
   if (args.causal) n_kv = min(n_kv, mb + 1);
+  // With a sliding window the tile's rows see no key below
+  // mb*BM - window + 1, so the KV tiles start at j0 (all later tile indices
+  // j run from 0 and stand for KV tile j0 + j).
+  int j0 = 0;
+  if (args.window > 0) {
+    const int lo = mb * C::BM - args.window + 1;
+    j0 = lo > 0 ? lo / C::BN : 0;
+  }
+  n_kv -= j0;
 
   // ---- shared memory carve-up ----
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -216,7 +225,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
 #pragma unroll
         for (int c = 0; c < C::HALVES; ++c) {
           int c0, c1, c2;
-          tile_coords(c, j * C::BN, c0, c1, c2);
+          tile_coords(c, (j0 + j) * C::BN, c0, c1, c2);
           tma_load_3d(sbase + C::OFF_K + st * C::TILE_BYTES + c * C::HALF_BYTES, &tm_k, kb,
                       c0, c1, c2);
         }
@@ -224,7 +233,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
 #pragma unroll
         for (int c = 0; c < C::HALVES; ++c) {
           int c0, c1, c2;
-          tile_coords(c, j * C::BN, c0, c1, c2);
+          tile_coords(c, (j0 + j) * C::BN, c0, c1, c2);
           tma_load_3d(sbase + C::OFF_V + st * C::TILE_BYTES + c * C::HALF_BYTES, &tm_v, vb,
                       c0, c1, c2);
         }
@@ -332,13 +341,15 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 64; ++i) t[64 + i] = __uint_as_float(raw[i]);
       }
-      const int kbase = j * C::BN;
-      if ((args.causal && j == mb) || kbase + C::BN > L) {
-        int lim = L - kbase;  // keys [0, lim) of the tile are visible
+      const int kbase = (j0 + j) * C::BN;
+      const bool win_edge = args.window > 0 && kbase < mb * C::BM + C::BM - args.window;
+      if ((args.causal && j0 + j == mb) || kbase + C::BN > L || win_edge) {
+        int lim = L - kbase;  // keys [lo, lim) of the tile are visible
         if (args.causal) lim = min(lim, qpos - kbase + 1);
+        const int lo = args.window > 0 ? qpos - args.window + 1 - kbase : 0;
 #pragma unroll
         for (int i = 0; i < 128; ++i)
-          if (i >= lim) t[i] = -INFINITY;
+          if (i >= lim || i < lo) t[i] = -INFINITY;
       }
       if (zero_scale) {
 #pragma unroll

@@ -150,6 +150,51 @@ def decode(B, H, D, *, seed, num_splits, lens=None, min_len=1024,
                                          T=T))
 
 
+@dataclass
+class PagedDecodeCase:
+    q: torch.Tensor            # [B, H, D]
+    k_pages: torch.Tensor      # [num_pages, page_size, H_kv, D]
+    v_pages: torch.Tensor
+    block_table: torch.Tensor  # int32 [B, max_blocks], on the CPU
+    seqlens: torch.Tensor      # int32 [B], on the CPU
+    num_splits: int
+    scale: float
+    meta: dict = field(default_factory=dict)
+
+
+def paged_decode(B, H, H_kv, D, page_size, *, seed, num_splits, lens=None,
+                 min_len=1024, max_len=32768, spare_pages=3, dtype=torch.bfloat16,
+                 scale=None, device="cpu") -> PagedDecodeCase:
+    """A paged KV cache: every sequence gets ceil(L / page_size) pages drawn
+    without replacement (a seeded permutation) from a pool with a few spare
+    pages; unused block-table entries are -1.  Lengths are drawn first, on the
+    CPU generator, exactly as in ``decode``."""
+    g = _gen("cpu", seed)
+    if lens is None:
+        lens = [int(x) for x in
+                torch.randint(min_len, max_len + 1, (B,), generator=g).tolist()]
+    lens = [int(n) for n in lens]
+    nblk = [-(-L // page_size) for L in lens]
+    P = sum(nblk) + spare_pages
+    perm = torch.randperm(P, generator=g).tolist()
+    table = torch.full((B, max(1, max(nblk) if nblk else 1)), -1, dtype=torch.int32)
+    i = 0
+    for b in range(B):
+        for c in range(nblk[b]):
+            table[b, c] = perm[i]
+            i += 1
+    gd = g if device == "cpu" else _gen(device, seed)
+    q = randn((B, H, D), dtype=dtype, device=device, gen=gd)
+    kp = randn((P, page_size, H_kv, D), dtype=dtype, device=device, gen=gd)
+    vp = randn((P, page_size, H_kv, D), dtype=dtype, device=device, gen=gd)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    return PagedDecodeCase(q, kp, vp, table, torch.tensor(lens, dtype=torch.int32),
+                           int(num_splits), float(scale),
+                           dict(B=B, H=H, H_kv=H_kv, D=D, page_size=page_size,
+                                seed=seed, lens=lens, pages=P))
+
+
 # The five measured configurations, by number.
 def config1(device="cpu") -> DenseCase:
     """B=1 H=1 N=256 D=64, fp32 N(0,1), scale 1/8, non-causal."""

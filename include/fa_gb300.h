@@ -67,6 +67,16 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int N, int D, float scale, int causal, void* stream);
 
 /*
+ * Dense causal forward with a sliding window, bf16 in and out: query i sees
+ * keys max(0, i - window + 1) .. i.  Same layouts as fa_fwd; window >= 1
+ * (window >= N is plain causal attention).  Key tiles outside every row's
+ * window are not read.  Hidden keys enter the fold as the identity
+ * (-inf, 0, 0), the masking of "Associativity is All You Need".
+ */
+int fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse,
+                  int B, int H, int N, int D, float scale, int window, void* stream);
+
+/*
  * Dense forward, fp32 in and out (CUDA-core FFMA kernel, no tensor cores).
  * Same shapes and meaning as fa_fwd with f32 elements.
  */
@@ -131,6 +141,29 @@ int fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
                       const int* cu_seqlens_k, int total_kv_tokens,
                       int B, int H, int D, int num_splits, float scale, float* part_m, float* part_d,
                       float* part_o, void* stream);
+
+/*
+ * Split-KV decode, first pass, over a paged KV cache with grouped query
+ * heads.  Same chunking and outputs as fa_decode_splitkv (part_m, part_d,
+ * part_o for B*H rows; finish with fa_combine_states).
+ *   q           : bf16 [B, H, D]
+ *   k_pages     : bf16 [num_pages, page_size, H_kv, D], v_pages likewise
+ *   block_table : int32 [B, max_blocks] DEVICE array: key t of sequence b is
+ *                 row t % page_size of page block_table[b][t / page_size];
+ *                 page_size is a power of two
+ *   seqlens     : int32 [B] DEVICE array, 0 <= seqlens[b] <= max_blocks*page_size
+ *   H_kv        : KV heads, H % H_kv == 0; query head h reads KV head
+ *                 h / (H / H_kv)
+ * The device checks every length and page index it reads (page indices in
+ * [0, num_pages)) and reports FA_ERR_DEVICE_BOUNDS through
+ * fa_check_device_status instead of reading out of range; such keys are left
+ * out of the fold.
+ */
+int fa_decode_paged_splitkv(const void* q, const void* k_pages, const void* v_pages,
+                            const int* block_table, const int* seqlens, int num_pages,
+                            int page_size, int max_blocks, int B, int H, int H_kv, int D,
+                            int num_splits, float scale, float* part_m, float* part_d,
+                            float* part_o, void* stream);
 
 /*
  * Split-KV second pass: per row, fold chunks 0, 1, ..., num_splits-1 (in that

@@ -111,6 +111,44 @@ def attention_ref(q, k, v, scale, causal, rows=None, window=None):
     return O, L
 
 
+def attention_bwd_head_ref(q, k, v, do, scale, causal):
+    """Gradients of one head's attention with respect to q, k, v, given the
+    output gradient do (all [N, D] float64).  Recomputation, as the tiled
+    backward does it: P is rebuilt from the scores and the row log-sum-exp
+    (P = e^{S - LSE}), never stored.  With O = P V and S = scale Q K^T:
+        dV = P^T dO,  dP = dO V^T,  Delta_i = sum_j P_ij dP_ij = dO_i . O_i,
+        dS = P * (dP - Delta),  dQ = scale dS K,  dK = scale dS^T Q.
+    Returns dq, dk, dv and Delta."""
+    q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
+    n = q.shape[0]
+    o, lse = attention_head_ref(q, k, v, scale, causal)
+    s = scores(q, k, scale)
+    if causal:
+        s = causal_mask(s, np.arange(n), np.arange(k.shape[0]))
+    p = np.exp(s - lse[:, None])  # rows with no visible key do not occur
+    dv = p.T @ do
+    dp = do @ v.T
+    delta = (do * o).sum(axis=1)
+    ds = p * (dp - delta[:, None])
+    dq = scale * (ds @ k)
+    dk = scale * (ds.T @ q)
+    return dq, dk, dv, delta
+
+
+def attention_bwd_ref(q, k, v, do, scale, causal):
+    """[B, H, N, D] inputs (any dtype, converted exactly to float64); returns
+    dq, dk, dv [B, H, N, D] and Delta [B, H, N] in float64."""
+    q, k, v, do = to_f64(q), to_f64(k), to_f64(v), to_f64(do)
+    B, H, N, D = q.shape
+    dq, dk, dv = (np.zeros((B, H, N, D)) for _ in range(3))
+    delta = np.zeros((B, H, N))
+    for b in range(B):
+        for h in range(H):
+            dq[b, h], dk[b, h], dv[b, h], delta[b, h] = attention_bwd_head_ref(
+                q[b, h], k[b, h], v[b, h], do[b, h], scale, causal)
+    return dq, dk, dv, delta
+
+
 def varlen_ref(q, k, v, cu_seqlens, scale, causal, seqs=None, rows=None):
     """Packed [T, H, D] inputs with sequence i on tokens
     [cu_seqlens[i], cu_seqlens[i+1]).  Each sequence is its own dense

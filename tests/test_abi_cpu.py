@@ -73,3 +73,9 @@ def test_host_validation_without_gpu(lib):
     assert lib.fa_decode_splitkv(p, p, p, p, 16, 1, 1, 128, 0, 0.1, p, p, p, null) == -1
     assert lib.fa_decode_splitkv(p, p, p, p, 16, 1, 1, 128, 300, 0.1, p, p, p, null) == -1
     assert lib.fa_combine_states(p, p, p, 1, 16, 128, p, 7, p, null) == -1
+    # paged decode: page size not a power of two, H not a multiple of H_kv
+    assert lib.fa_decode_paged_splitkv(p, p, p, p, p, 4, 24, 4, 1, 8, 2, 128, 4, 0.1,
+                                       p, p, p, null) == -1
+    assert lib.fa_decode_paged_splitkv(p, p, p, p, p, 4, 16, 4, 1, 8, 3, 128, 4, 0.1,
+                                       p, p, p, null) == -1
+    assert lib.fa_fwd_window(p, p, p, p, p, 1, 1, 16, 64, 0.1, 0, null) == -1

@@ -1,0 +1,72 @@
+"""Pins of the float64 backward oracle.  The pages name the backward pass
+(recomputation instead of storing P) but give no formulas, so the oracle's
+explicit formulas are pinned against things that do not share them: central
+finite differences of the forward oracle, torch autograd in float64, and
+identities the gradient must satisfy."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as ora
+
+
+def _case(N, D, seed, std=1.0):
+    rng = np.random.default_rng(seed)
+    return tuple(rng.standard_normal((N, D)) * (std if i < 2 else 1.0) for i in range(4))
+
+
+def _loss(q, k, v, do, scale, causal):
+    o, _ = ora.attention_head_ref(q, k, v, scale, causal)
+    return float((o * do).sum())
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_finite_differences(causal):
+    """d/dx of <O(q, k, v), dO> by central differences matches every entry."""
+    q, k, v, do = _case(5, 3, 1 + causal, std=1.5)
+    scale = 0.6
+    dq, dk, dv, _ = ora.attention_bwd_head_ref(q, k, v, do, scale, causal)
+    h = 1e-6
+    for x, g in ((q, dq), (k, dk), (v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            old = x[idx]
+            x[idx] = old + h
+            lp = _loss(q, k, v, do, scale, causal)
+            x[idx] = old - h
+            lm = _loss(q, k, v, do, scale, causal)
+            x[idx] = old
+            num[idx] = (lp - lm) / (2 * h)
+        np.testing.assert_allclose(g, num, rtol=1e-6, atol=1e-8)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_against_torch_autograd_float64(causal):
+    B, H, N, D = 1, 2, 37, 8
+    g = torch.Generator().manual_seed(3)
+    q, k, v, do = (torch.randn(B, H, N, D, generator=g, dtype=torch.float64) for _ in range(4))
+    scale = 0.35
+    dq, dk, dv, delta = ora.attention_bwd_ref(q, k, v, do, scale, causal)
+    qq, kk, vv = (t.clone().requires_grad_(True) for t in (q, k, v))
+    o = torch.nn.functional.scaled_dot_product_attention(qq, kk, vv, is_causal=causal,
+                                                         scale=scale)
+    o.backward(do)
+    np.testing.assert_allclose(dq, qq.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dk, kk.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dv, vv.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(delta, (do * o.detach()).sum(-1).numpy(), rtol=1e-12)
+
+
+def test_gradient_identities():
+    """Softmax rows are shift invariant, so dS rows sum to zero: the dQ of a
+    constant key shift and sum_j dK_j both vanish; dV sums to sum_i dO_i
+    (every row of P sums to 1)."""
+    q, k, v, do = _case(11, 4, 7)
+    dq, dk, dv, _ = ora.attention_bwd_head_ref(q, k, v, do, 0.8, True)
+    np.testing.assert_allclose(dk.sum(0), 0.0, atol=1e-12)
+    np.testing.assert_allclose(dv.sum(0), do.sum(0), rtol=1e-12, atol=1e-12)
+    # a single key: the output is v whatever q is, so dq = 0 and dk = 0
+    dq1, dk1, dv1, _ = ora.attention_bwd_head_ref(q[:1], k[:1], v[:1], do[:1], 0.8, False)
+    np.testing.assert_allclose(dq1, 0.0, atol=1e-14)
+    np.testing.assert_allclose(dk1, 0.0, atol=1e-14)
+    np.testing.assert_array_equal(dv1, do[:1])
