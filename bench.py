@@ -39,6 +39,7 @@ import fa_inputs as inp  # noqa: E402
 
 PREFILL = dict(B=1, H=32, N=16384, D=128)
 DECODE = dict(B=64, H=32, D=128, S=16)
+ROWSTATS = dict(R=65536, C=4096)  # LayerNorm statistics of 4 x 16384 tokens, hidden 4096
 METRIC = "attention fwd TFLOP/s (bf16, causal) and % of GB300 BF16 peak; decode GB/s"
 WORKLOAD = ("prefill B=1 H=32 N=16384 D=128 causal bf16, Q,K~N(0,9) V~N(0,1); "
             "decode B=64 H=32 D=128 L~U[1024,32768] 16 KV chunks")
@@ -264,6 +265,38 @@ def other_configs(fa):
     wf = 32 * 4.0 * 128 * sum(min(i + 1, 4096) for i in range(16384))
     out["window4096_B1_H32_N16384_D128"] = {"tflops": wf / (ms * 1e-3) / 1e12, "ms": ms}
     del cw
+    # backward by recomputation of the causal prefill workload (B=1 H=32
+    # N=16384 D=128): five N x N x D products per head, half of them under
+    # the causal mask = 2.5x the forward's FLOPs
+    cb = inp.dense(1, 32, 16384, 128, seed=5, causal=True, device="cuda")
+    dout = inp.output_grad((1, 32, 16384, 128), seed=6, device="cuda")
+    ob, lb = fa.fa_fwd(cb.q, cb.k, cb.v, cb.scale, True)
+    gq, gk, gv = (torch.empty_like(cb.q) for _ in range(3))
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(1, 32, 16384) // 4, dtype=torch.float32,
+                     device="cuda")
+    ms = _time_launches(lambda: fa.fa_bwd(cb.q, cb.k, cb.v, ob, dout, lb, cb.scale, True,
+                                          gq, gk, gv, ws), 10)
+    out["bwd_B1_H32_N16384_D128_causal"] = {
+        "tflops": 2.5 * prefill_flops(1, 32, 16384, 128) / (ms * 1e-3) / 1e12, "ms": ms}
+    del cb, dout, ob, lb, gq, gk, gv, ws
+    # Welford row statistics: LayerNorm statistics of 4 x 16384 tokens at
+    # hidden size 4096 (bf16, 512 MiB, larger than L2), and the split-K pair
+    # on 64 rows of 2^22 fp32 values in 128 chunks
+    R, C = ROWSTATS["R"], ROWSTATS["C"]
+    xs = inp.stats_rows(R, C, seed=11, loc=0.5, std=1.0, row_spread=1.0, device="cuda")
+    outs = [torch.empty(R, dtype=torch.float32, device="cuda") for _ in range(3)]
+    ms = _time_launches(lambda: fa.fa_row_stats(xs, 1e-5, *outs), 20)
+    out[f"rowstats_R{R}_C{C}_bf16"] = {"gbs": R * C * 2 / (ms * 1e-3) / 1e9, "ms": ms}
+    del xs, outs
+    ys = inp.stats_rows(64, 1 << 22, seed=12, loc=2.0, std=1.0, dtype=torch.float32,
+                        device="cuda")
+
+    def split():
+        fa.fa_row_stats_combine(*fa.fa_row_stats_partials(ys, 128))
+    ms = _time_launches(split, 20)
+    out["rowstats_split_R64_C4194304_f32_S128"] = {
+        "gbs": 64 * (1 << 22) * 4 / (ms * 1e-3) / 1e9, "ms": ms}
+    del ys
     # paged KV decode with grouped query heads: the decode lengths, H=32 over
     # H_kv=8, pages of 64 keys
     pc = inp.paged_decode(64, 32, 8, 128, 64, seed=4, num_splits=16, device="cuda")
@@ -429,7 +462,8 @@ def run_gpu(args, rank, world, dist):
 def run_profile_case(args):
     """Only one workload, W + K launches, nothing else: the command the ncu
     captures run.  prefill = the full causal N=16384 prefill (537 MB of
-    inputs); decode = split-KV decode on the first 8 sequences of the decode
+    inputs); bwd = its backward (Delta, dK/dV, dQ kernels); rowstats = the
+    LayerNorm statistics of 65536 x 4096 bf16; decode = split-KV decode on the first 8 sequences of the decode
     workload (about 2.2 GB of KV cache, larger than L2, small enough for a
     multi-pass capture)."""
     import exact_io_aware_15_gb300 as fa
@@ -441,6 +475,19 @@ def run_profile_case(args):
         o = torch.empty_like(c.q)
         lse = torch.empty((P["B"], P["H"], P["N"]), dtype=torch.float32, device="cuda")
         run = lambda: fa.fa_fwd(c.q, c.k, c.v, c.scale, True, o=o, lse=lse)
+    elif args.profile_case == "bwd":
+        P = PREFILL
+        c = inp.dense(P["B"], P["H"], P["N"], P["D"], seed=5, causal=True, device="cuda")
+        dout = inp.output_grad((P["B"], P["H"], P["N"], P["D"]), seed=6, device="cuda")
+        o, lse = fa.fa_fwd(c.q, c.k, c.v, c.scale, True)
+        grads = [torch.empty_like(c.q) for _ in range(3)]
+        ws = torch.empty(P["B"] * P["H"] * P["N"], dtype=torch.float32, device="cuda")
+        run = lambda: fa.fa_bwd(c.q, c.k, c.v, o, dout, lse, c.scale, True, *grads, ws)
+    elif args.profile_case == "rowstats":
+        x = inp.stats_rows(ROWSTATS["R"], ROWSTATS["C"], seed=11, loc=0.5, std=1.0,
+                           row_spread=1.0, device="cuda")
+        outs = [torch.empty(ROWSTATS["R"], dtype=torch.float32, device="cuda") for _ in range(3)]
+        run = lambda: fa.fa_row_stats(x, 1e-5, *outs)
     else:
         g = torch.Generator().manual_seed(4)
         lens = torch.randint(1024, 32769, (64,), generator=g).tolist()[:8]
@@ -464,7 +511,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-other-configs", action="store_true")
-    ap.add_argument("--profile-case", choices=["prefill", "decode"], default=None)
+    ap.add_argument("--profile-case", choices=["prefill", "decode", "bwd", "rowstats"],
+                    default=None)
     args = ap.parse_args(argv)
     if args.profile_case:
         return run_profile_case(args)

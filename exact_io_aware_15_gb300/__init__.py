@@ -42,6 +42,12 @@ SIGNATURES = {
     "fa_fwd_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _I, _P]),
     "fa_fwd_window": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "fa_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I]),
+    "fa_row_stats": (_I, [_P, _I, _I, _I, _F, _P, _P, _P, _P]),
+    "fa_row_stats_workspace_bytes": (ctypes.c_size_t, [_I, _I]),
+    "fa_row_stats_partials": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P]),
+    "fa_row_stats_combine": (_I, [_P, _P, _P, _I, _I, _F, _P, _P, _P, _P]),
+    "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "fa_decode_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
     "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
     "fa_combine_states": (_I, [_P, _P, _P, _I, _I, _I, _P, _I, _P, _P]),
@@ -181,6 +187,87 @@ def fa_fwd_window(q, k, v, window, scale=None, o=None, lse=None):
                                       B, H, N, D, _scale(scale, D), int(window), _stream(q))
     _check(rc, "fa_fwd_window")
     return o, lse
+
+
+def fa_bwd(q, k, v, o, do, lse, scale=None, causal=False, dq=None, dk=None, dv=None,
+           workspace=None):
+    """Backward of the dense bf16 forward by recomputation (fa_bwd): returns
+    dq, dk, dv (bf16) given the forward's o and lse and the output gradient do."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
+        _need(t, n, torch.bfloat16, 4)
+        if t.shape != q.shape:
+            raise ValueError(f"{n} must have the shape of q [B, H, N, D]")
+    B, H, N, D = q.shape
+    _need(lse, "lse", torch.float32, 3)
+    if tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse must be [B, H, N]")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _need(t, n, torch.bfloat16, 4)
+    lib = load_library()
+    if workspace is None:
+        workspace = torch.empty(max(1, lib.fa_bwd_workspace_bytes(B, H, N) // 4),
+                                dtype=torch.float32, device=q.device)
+    _need(workspace, "workspace", torch.float32, 1)
+    if workspace.numel() * 4 < lib.fa_bwd_workspace_bytes(B, H, N):
+        raise ValueError("workspace too small")
+    rc = lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                    _ptr(dk), _ptr(dv), _ptr(workspace), B, H, N, D, _scale(scale, D),
+                    int(bool(causal)), _stream(q))
+    _check(rc, "fa_bwd")
+    return dq, dk, dv
+
+
+def _rows_dtype(x):
+    if not isinstance(x, torch.Tensor) or not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor")
+    if x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous [R, C] matrix")
+    if x.dtype not in _DT:
+        raise TypeError(f"x must be bf16 or fp32, got {x.dtype}")
+    return _DT[x.dtype]
+
+
+def fa_row_stats(x, eps=0.0, mean=None, var=None, rstd=None):
+    """Per-row mean, population variance and 1/sqrt(var + eps) of a [R, C]
+    bf16 or fp32 matrix (fa_row_stats): Welford states, one pass."""
+    dt = _rows_dtype(x)
+    R, C = x.shape
+    mk = lambda t: torch.empty(R, dtype=torch.float32, device=x.device) if t is None else t
+    mean, var, rstd = mk(mean), mk(var), mk(rstd)
+    rc = load_library().fa_row_stats(_ptr(x), R, C, dt, float(eps), _ptr(mean), _ptr(var),
+                                     _ptr(rstd), _stream(x))
+    _check(rc, "fa_row_stats")
+    return mean, var, rstd
+
+
+def fa_row_stats_partials(x, num_splits):
+    """Split-K first pass: chunk states (n, mu, M2), each [R, num_splits]."""
+    dt = _rows_dtype(x)
+    R, C = x.shape
+    parts = [torch.empty((R, num_splits), dtype=torch.float32, device=x.device)
+             for _ in range(3)]
+    rc = load_library().fa_row_stats_partials(_ptr(x), R, C, dt, int(num_splits),
+                                              *(_ptr(p) for p in parts), _stream(x))
+    _check(rc, "fa_row_stats_partials")
+    return tuple(parts)
+
+
+def fa_row_stats_combine(part_n, part_mu, part_m2, eps=0.0):
+    """Split-K second pass: fixed-order fold of each row's chunk states."""
+    for t, n in ((part_n, "part_n"), (part_mu, "part_mu"), (part_m2, "part_m2")):
+        _need(t, n, torch.float32, 2)
+        if t.shape != part_n.shape:
+            raise ValueError("chunk state arrays must have the same shape")
+    R, S = part_n.shape
+    out = [torch.empty(R, dtype=torch.float32, device=part_n.device) for _ in range(3)]
+    rc = load_library().fa_row_stats_combine(_ptr(part_n), _ptr(part_mu), _ptr(part_m2), R, S,
+                                             float(eps), *(_ptr(o) for o in out),
+                                             _stream(part_n))
+    _check(rc, "fa_row_stats_combine")
+    return tuple(out)
 
 
 def fa_fwd_f32(q, k, v, scale=None, causal=False, o=None, lse=None):
@@ -357,7 +444,9 @@ def decode(q, k_cache, v_cache, cu_seqlens_k, num_splits=16, scale=None,
 
 
 __all__ = [
-    "fa_fwd", "fa_fwd_f32", "fa_fwd_ex", "fa_fwd_window", "fa_fwd_varlen", "fa_decode_workspace_bytes",
+    "fa_fwd", "fa_fwd_f32", "fa_fwd_ex", "fa_fwd_window", "fa_fwd_varlen", "fa_bwd",
+    "fa_bwd_workspace_bytes", "fa_decode_workspace_bytes", "fa_row_stats",
+    "fa_row_stats_workspace_bytes", "fa_row_stats_partials", "fa_row_stats_combine",
     "fa_decode_splitkv", "fa_combine_states", "fa_decode_splitkv_noalloc",
     "fa_decode_paged_splitkv",
     "fa_check_device_status",

@@ -182,6 +182,88 @@ int fwd_f32(const void* q, const void* k, const void* v, void* o, float* lse, in
   return launched(fa::launch_fwd_f32(a, D, static_cast<cudaStream_t>(stream)));
 }
 
+int bwd_bf16(const void* q, const void* k, const void* v, const void* o, const void* dout,
+             const float* lse, void* dq, void* dk, void* dv, float* workspace, int B, int H,
+             int N, int D, float scale, int causal, void* stream) {
+  if (B >= 0 && H >= 0 && N >= 0 && (B == 0 || H == 0 || N == 0) &&
+      (D == 64 || D == 128) && good_scale(scale))
+    return FA_OK;  // empty problem: nothing to read or write
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned4(lse) ||
+      !aligned4(workspace))
+    return FA_ERR_INVALID_ARG;
+  if (B < 0 || H < 0 || N < 0 || (D != 64 && D != 128) || !good_scale(scale))
+    return FA_ERR_INVALID_ARG;
+  const long long BH = static_cast<long long>(B) * H;
+  const long long tiles = (static_cast<long long>(N) + 127) / 128;
+  if (BH > 0x7fffffffLL || BH * tiles > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  unsigned int* status = nullptr;
+  int rc = current_device(&status);
+  if (rc != FA_OK) return rc;
+  rc = get_encoder();
+  if (rc != FA_OK) return rc;
+  fa::BwdMaps maps;
+  const uint64_t rs = static_cast<uint64_t>(D) * 2u;
+  const uint64_t hs = rs * static_cast<uint64_t>(N);
+  if (encode_map(&maps.q, q, D, N, BH, rs, hs, 128u, 1u) != FA_OK ||
+      encode_map(&maps.k, k, D, N, BH, rs, hs, 128u, 1u) != FA_OK ||
+      encode_map(&maps.v, v, D, N, BH, rs, hs, 128u, 1u) != FA_OK ||
+      encode_map(&maps.dout, dout, D, N, BH, rs, hs, 128u, 1u) != FA_OK)
+    return FA_ERR_DRIVER;
+  fa::BwdArgs a{};
+  a.BH = static_cast<int>(BH);
+  a.N = N;
+  a.num_tiles = static_cast<int>(tiles);
+  a.causal = causal ? 1 : 0;
+  a.rows = BH * N;
+  a.scale = scale;
+  a.scale_log2 = scale_log2(scale);
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  a.delta = workspace;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.status = status;
+  return launched(fa::launch_bwd(maps, a, D, static_cast<cudaStream_t>(stream)));
+}
+
+bool aligned_to(const void* p, unsigned int a) {
+  return p && (reinterpret_cast<uintptr_t>(p) & (a - 1u)) == 0;
+}
+
+int row_stats(const void* x, int R, int C, int dtype, int S, float eps, float* part_n,
+              float* part_mu, float* part_m2, float* mean, float* var, float* rstd,
+              void* stream) {
+  if (R < 0 || C < 1 || S < 1 || S > 65535 || (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F32))
+    return FA_ERR_INVALID_ARG;
+  if (!isfinite(eps) || eps < 0.f) return FA_ERR_INVALID_ARG;
+  if (R == 0) return FA_OK;
+  if (!aligned_to(x, dtype == FA_DTYPE_BF16 ? 2u : 4u)) return FA_ERR_INVALID_ARG;
+  if (part_n ? (!aligned4(part_n) || !aligned4(part_mu) || !aligned4(part_m2))
+             : (!aligned4(mean) || !aligned4(var) || (rstd && !aligned4(rstd))))
+    return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(R) * S > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  unsigned int* status = nullptr;
+  int rc = current_device(&status);
+  if (rc != FA_OK) return rc;
+  fa::RowStatsArgs a{};
+  a.x = x;
+  a.R = R;
+  a.C = C;
+  a.S = S;
+  a.bf16 = dtype == FA_DTYPE_BF16 ? 1 : 0;
+  a.part_n = part_n;
+  a.part_mu = part_mu;
+  a.part_m2 = part_m2;
+  a.mean = mean;
+  a.var = var;
+  a.rstd = rstd;
+  a.eps = eps;
+  return launched(fa::launch_row_stats(a, static_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 
 int fa::checked_current_device(unsigned int** status) { return current_device(status); }
@@ -260,6 +342,19 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
   a.status = status;
   return launched(fa::launch_fwd_tc(maps, a, D, static_cast<int>(SH),
                                     static_cast<cudaStream_t>(stream)));
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int N) {
+  if (B < 0 || H < 0 || N < 0) return 0;
+  return static_cast<size_t>(B) * static_cast<size_t>(H) * static_cast<size_t>(N) *
+         sizeof(float);
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+           const float* lse, void* dq, void* dk, void* dv, float* workspace, int B, int H,
+           int N, int D, float scale, int causal, void* stream) {
+  return bwd_bf16(q, k, v, o, dout, lse, dq, dk, dv, workspace, B, H, N, D, scale, causal,
+                  stream);
 }
 
 size_t fa_decode_workspace_bytes(int B, int H, int D, int num_splits) {
@@ -365,6 +460,48 @@ int fa_combine_states(const float* part_m, const float* part_d, const float* par
   a.o_f32 = o_dtype == FA_DTYPE_F32 ? 1 : 0;
   a.lse = lse;
   return launched(fa::launch_combine(a, D, static_cast<cudaStream_t>(stream)));
+}
+
+int fa_row_stats(const void* x, int R, int C, int dtype, float eps, float* mean, float* var,
+                 float* rstd, void* stream) {
+  return row_stats(x, R, C, dtype, 1, eps, nullptr, nullptr, nullptr, mean, var, rstd, stream);
+}
+
+size_t fa_row_stats_workspace_bytes(int R, int num_splits) {
+  if (R < 0 || num_splits < 1) return 0;
+  return 3u * static_cast<size_t>(R) * static_cast<size_t>(num_splits) * sizeof(float);
+}
+
+int fa_row_stats_partials(const void* x, int R, int C, int dtype, int num_splits,
+                          float* part_n, float* part_mu, float* part_m2, void* stream) {
+  if (R > 0 && (!part_n || !part_mu || !part_m2)) return FA_ERR_INVALID_ARG;
+  return row_stats(x, R, C, dtype, num_splits, 0.f, part_n, part_mu, part_m2, nullptr, nullptr,
+                   nullptr, stream);
+}
+
+int fa_row_stats_combine(const float* part_n, const float* part_mu, const float* part_m2, int R,
+                         int num_splits, float eps, float* mean, float* var, float* rstd,
+                         void* stream) {
+  if (R < 0 || num_splits < 1 || num_splits > 65535 || !isfinite(eps) || eps < 0.f)
+    return FA_ERR_INVALID_ARG;
+  if (R == 0) return FA_OK;
+  if (!aligned4(part_n) || !aligned4(part_mu) || !aligned4(part_m2) || !aligned4(mean) ||
+      !aligned4(var) || (rstd && !aligned4(rstd)))
+    return FA_ERR_INVALID_ARG;
+  unsigned int* status = nullptr;
+  int rc = current_device(&status);
+  if (rc != FA_OK) return rc;
+  fa::RowStatsCombineArgs a{};
+  a.part_n = part_n;
+  a.part_mu = part_mu;
+  a.part_m2 = part_m2;
+  a.R = R;
+  a.S = num_splits;
+  a.eps = eps;
+  a.mean = mean;
+  a.var = var;
+  a.rstd = rstd;
+  return launched(fa::launch_row_stats_combine(a, static_cast<cudaStream_t>(stream)));
 }
 
 int fa_check_device_status(void* stream) {

@@ -75,6 +75,32 @@ struct PagedDecodeArgs {
 };
 cudaError_t launch_decode_paged(const PagedDecodeArgs& a, int D, cudaStream_t stream);
 
+// Arguments of the backward kernels (dense bf16 [B, H, N, D], D = 64 or 128).
+struct BwdArgs {
+  int BH;            // B * H
+  int N;             // sequence length (queries = keys)
+  int num_tiles;     // 128-row tiles per sequence
+  int causal;
+  long long rows;    // BH * N
+  float scale;       // softmax scale (dQ, dK epilogue)
+  float scale_log2;  // scale * log2(e)
+  const void* o;     // forward output, bf16
+  const void* dout;  // dO, bf16
+  const float* lse;  // forward log-sum-exp (natural log) [BH * N]
+  float* delta;      // workspace: rowsum(dO * O) [BH * N]
+  void* dq;          // bf16 outputs
+  void* dk;
+  void* dv;
+  unsigned int* status;
+};
+
+struct BwdMaps {
+  CUtensorMap q, k, v, dout;
+};
+
+// Delta, then dK/dV, then dQ, in stream order.
+cudaError_t launch_bwd(const BwdMaps& maps, const BwdArgs& a, int D, cudaStream_t stream);
+
 struct CombineArgs {
   const float* part_m;
   const float* part_d;
@@ -85,6 +111,33 @@ struct CombineArgs {
   float* lse;
 };
 cudaError_t launch_combine(const CombineArgs& a, int D, cudaStream_t stream);
+
+// Per-row Welford statistics of a [R, C] matrix (rowstats.cu).
+struct RowStatsArgs {
+  const void* x;
+  int R, C, S;       // rows, columns, column chunks per row
+  int bf16;          // 1: bf16 elements, 0: fp32
+  float* part_n;     // chunk states [R, S] (NULL: S == 1, write the statistics)
+  float* part_mu;
+  float* part_m2;
+  float* mean;       // [R]
+  float* var;        // [R], population variance
+  float* rstd;       // [R], 1 / sqrt(var + eps); may be NULL
+  float eps;
+};
+cudaError_t launch_row_stats(const RowStatsArgs& a, cudaStream_t stream);
+
+struct RowStatsCombineArgs {
+  const float* part_n;
+  const float* part_mu;
+  const float* part_m2;
+  int R, S;
+  float eps;
+  float* mean;
+  float* var;
+  float* rstd;
+};
+cudaError_t launch_row_stats_combine(const RowStatsCombineArgs& a, cudaStream_t stream);
 
 // The sm_103 check of the current device and its device status word, as used
 // by every entry point of fa_api.cu (returns an FA_* status code).

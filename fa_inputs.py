@@ -85,6 +85,23 @@ def dense(B, H, N, D, *, seed, causal, dtype=torch.bfloat16, qk_std=1.0,
                      dict(B=B, H=H, N=N, D=D, seed=seed, qk_std=qk_std))
 
 
+def output_grad(shape, *, seed, std=1.0, dtype=torch.bfloat16, device="cpu") -> torch.Tensor:
+    """The loss gradient dO fed to the backward: N(0, std^2), rounded once."""
+    return randn(shape, std=std, dtype=dtype, device=device, gen=_gen(device, seed))
+
+
+def stats_rows(R, C, *, seed, loc=0.0, std=1.0, row_spread=0.0, dtype=torch.bfloat16,
+               device="cpu") -> torch.Tensor:
+    """A [R, C] matrix for the row statistics: row r is loc_r + std * z with
+    z ~ N(0, 1) and loc_r = loc + row_spread * g_r, g_r ~ N(0, 1) (drawn
+    first), computed in fp32 and rounded once to ``dtype``."""
+    g = _gen(device, seed)
+    offs = torch.randn((R, 1), generator=g, device=device, dtype=torch.float32)
+    x = torch.randn((R, C), generator=g, device=device, dtype=torch.float32)
+    x.mul_(std).add_(offs * row_spread + loc)
+    return x.to(dtype)
+
+
 def varlen_lengths(total_tokens: int, max_len: int, *, gen: torch.Generator,
                    min_len: int = 1) -> list[int]:
     """Draw lengths U[min_len, max_len] until they cover ``total_tokens``;

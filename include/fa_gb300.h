@@ -115,6 +115,82 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
                   void* stream);
 
 /*
+ * Backward of the dense bf16 forward, by recomputation: the attention weights
+ * P_ij = e^{s_ij - LSE_i} are rebuilt tile by tile from Q, K and the
+ * forward's LSE, never read from or written to memory ("Understanding
+ * FlashAttention Pt 1: Personal Notes", Introduction: tiling + online
+ * softmax + recomputation).  With dO the gradient of the loss with respect
+ * to O:
+ *     Delta_i = <dO_i, O_i>,   dS_ij = P_ij (<dO_i, v_j> - Delta_i),
+ *     dQ = scale dS K,   dK = scale dS^T Q,   dV = P^T dO.
+ *   q, k, v, o, dout : bf16 [B, H, N, D]  (o and lse as fa_fwd wrote them,
+ *                      same scale and causal flag)
+ *   lse              : f32 [B, H, N]
+ *   dq, dk, dv       : bf16 [B, H, N, D]  (written, not accumulated into)
+ *   workspace        : f32, fa_bwd_workspace_bytes(B, H, N) bytes, caller-
+ *                      owned DEVICE scratch (Delta is written there)
+ *   B, H, N >= 1; D in {64, 128}.
+ * Products on the tensor cores in bf16 with fp32 accumulation; P and dS are
+ * rounded to bf16 before their products.  Three kernels in stream order
+ * (Delta, dK/dV, dQ); no atomics, so the result is deterministic.
+ */
+size_t fa_bwd_workspace_bytes(int B, int H, int N);
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+           const float* lse, void* dq, void* dk, void* dv, float* workspace,
+           int B, int H, int N, int D, float scale, int causal, void* stream);
+
+/*
+ * Row statistics as a monoid reduction: per row of a [R, C] matrix, the
+ * Welford state (n, mu, M2) of "Learning FlashAttention the Hard Way -
+ * Part 1", section "The Same Move: Welford's Variance" (a sample injects as
+ * (1, x, 0); partials over disjoint chunks merge symmetrically with identity
+ * (0, 0, 0); variance = M2 / n), reduced with the split-K + combine
+ * structure of the decode above ("only the combine changes").
+ *   x      : DEVICE [R, C] row-major, dtype FA_DTYPE_BF16 or FA_DTYPE_F32,
+ *            aligned to its element size (16-byte aligned rows are read with
+ *            16-byte loads; other rows one element at a time)
+ *   mean   : f32 [R]  (written)
+ *   var    : f32 [R]  population variance M2 / n (written)
+ *   rstd   : f32 [R]  1 / sqrt(var + eps), the LayerNorm scale (written;
+ *            may be NULL)
+ *   R >= 0, C >= 1, eps finite and >= 0.
+ * Accumulation in fp32; the fold order depends only on R, C and the
+ * alignment of x, so results are deterministic.
+ */
+int fa_row_stats(const void* x, int R, int C, int dtype, float eps,
+                 float* mean, float* var, float* rstd, void* stream);
+
+/*
+ * Bytes of the chunk states fa_row_stats_partials writes:
+ * part_n, part_mu, part_m2, each f32 [R, num_splits].  0 for invalid sizes.
+ */
+size_t fa_row_stats_workspace_bytes(int R, int num_splits);
+
+/*
+ * Split-K first pass: chunk c of a row covers columns
+ * [c*ceil(C/S), min(C, (c+1)*ceil(C/S))) (may be empty: state (0, 0, 0)),
+ * S = num_splits in [1, 65535], R * S <= 2^31 - 1.  Writes each chunk's
+ * state (n, mu, M2) to part_n / part_mu / part_m2 [R, S] (caller-owned).
+ */
+int fa_row_stats_partials(const void* x, int R, int C, int dtype, int num_splits,
+                          float* part_n, float* part_mu, float* part_m2, void* stream);
+
+/*
+ * Split-K second pass: per row, folds its chunk states left to right, chunk
+ * 0 first, with the merge
+ *     n = n_a + n_b, delta = mu_b - mu_a, r = n_b / n,
+ *     mu = mu_a + delta * r, M2 = (M2_a + M2_b) + ((delta * delta) * n_a) * r
+ * (states with n = 0 are skipped), every operation rounded once in binary32
+ * in this order, then var = M2 / n and rstd = 1 / sqrt(var + eps) with a
+ * correctly rounded sqrt: bit-reproducible by any IEEE fp32 implementation
+ * of the same sequence.  Outputs as fa_row_stats.
+ */
+int fa_row_stats_combine(const float* part_n, const float* part_mu, const float* part_m2,
+                         int R, int num_splits, float eps, float* mean, float* var,
+                         float* rstd, void* stream);
+
+/*
  * Bytes of the partial-state workspace fa_decode_splitkv writes:
  * part_m and part_d f32 [B, H, num_splits], part_o f32 [B, H, num_splits, D].
  * Returns 0 for invalid sizes.

@@ -135,6 +135,42 @@ def attention_bwd_head_ref(q, k, v, do, scale, causal):
     return dq, dk, dv, delta
 
 
+def attention_bwd_sampled_ref(q, k, v, do, scale, causal, rows, cols, chunk=1024):
+    """Selected gradient rows of one head, for heads too long for the full
+    matrices: dq at the query rows `rows`, dk and dv at the key rows `cols`.
+    O and LSE of every query row come from attention_head_ref over row
+    chunks; then, per query row i, the row of P and dP; per key row j, the
+    column of P and dP (P_ij = e^{s_ij - LSE_i}, hidden keys 0).  The same
+    formulas as attention_bwd_head_ref, evaluated one row or column at a time.
+    Returns dq[len(rows), D], dk[len(cols), D], dv[len(cols), D]."""
+    q, k, v, do = to_f64(q), to_f64(k), to_f64(v), to_f64(do)
+    n = q.shape[0]
+    o = np.zeros_like(q)
+    lse = np.zeros(n)
+    for r0 in range(0, n, chunk):
+        r = np.arange(r0, min(n, r0 + chunk))
+        o[r], lse[r] = attention_head_ref(q, k, v, scale, causal, rows=r)
+    delta = (do * o).sum(axis=1)
+    pos = np.arange(n)
+    dq = np.zeros((len(rows), q.shape[1]))
+    for t, i in enumerate(rows):
+        s = scale * (k @ q[i])
+        vis = pos <= i if causal else np.ones(n, dtype=bool)
+        p = np.where(vis, np.exp(s - lse[i]), 0.0)
+        ds = p * (v @ do[i] - delta[i])
+        dq[t] = scale * (ds @ k)
+    dk = np.zeros((len(cols), q.shape[1]))
+    dv = np.zeros((len(cols), q.shape[1]))
+    for t, j in enumerate(cols):
+        s = scale * (q @ k[j])
+        vis = pos >= j if causal else np.ones(n, dtype=bool)
+        p = np.where(vis, np.exp(s - lse), 0.0)
+        ds = p * (do @ v[j] - delta)
+        dv[t] = p @ do
+        dk[t] = scale * (ds @ q)
+    return dq, dk, dv
+
+
 def attention_bwd_ref(q, k, v, do, scale, causal):
     """[B, H, N, D] inputs (any dtype, converted exactly to float64); returns
     dq, dk, dv [B, H, N, D] and Delta [B, H, N] in float64."""

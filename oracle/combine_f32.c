@@ -153,3 +153,61 @@ int fa_oracle_combine_f32(const float* part_m, const float* part_d,
     }
     return 0;
 }
+
+/*
+ * Plain C, fp32, fixed-order fold of Welford states (n, mu, M2), one row at a
+ * time (page: "Learning FlashAttention the Hard Way - Part 1", section "The
+ * Same Move: Welford's Variance": identity (0, 0, 0), the symmetric merge of
+ * two partials over disjoint chunks, and the division of M2 by n at the end).
+ * Every row folds chunk 0, 1, ..., S-1 into the identity, left to right:
+ *   a (+) b = b if n_a = 0;  a if n_b = 0;  otherwise
+ *     n = n_a + n_b,  delta = mu_b - mu_a,  r = n_b / n,
+ *     mu = mu_a + delta * r,
+ *     M2 = (M2_a + M2_b) + ((delta * delta) * n_a) * r,
+ * each operation rounded once in binary32 in this order; then
+ * var = M2 / n and rstd = 1 / sqrt(var + eps) (sqrt correctly rounded).
+ * rstd may be NULL.  Returns -1 on bad sizes, else 0.
+ */
+static void welford_merge_f32(float* n, float* mu, float* m2, float nb, float mub, float m2b) {
+  if (nb == 0.0f) return;
+  if (*n == 0.0f) {
+    *n = nb;
+    *mu = mub;
+    *m2 = m2b;
+    return;
+  }
+  const float na = *n;
+  const float nn = na + nb;
+  const float delta = mub - *mu;
+  const float r = nb / nn;
+  const float t = delta * r;
+  *mu = *mu + t;
+  const float s = *m2 + m2b;
+  const float dd = delta * delta;
+  const float ddn = dd * na;
+  const float cross = ddn * r;
+  *m2 = s + cross;
+  *n = nn;
+}
+
+int fa_oracle_welford_combine_f32(const float* part_n, const float* part_mu,
+                                  const float* part_m2, int rows, int S, float eps,
+                                  float* mean, float* var, float* rstd) {
+  if (rows < 0 || S < 1) return -1;
+  for (int r = 0; r < rows; ++r) {
+    float n = 0.0f, mu = 0.0f, m2 = 0.0f;
+    for (int c = 0; c < S; ++c) {
+      const size_t i = (size_t)r * (size_t)S + (size_t)c;
+      welford_merge_f32(&n, &mu, &m2, part_n[i], part_mu[i], part_m2[i]);
+    }
+    const float v = m2 / n;
+    mean[r] = mu;
+    var[r] = v;
+    if (rstd) {
+      const float ve = v + eps;
+      const float sq = sqrtf(ve);
+      rstd[r] = 1.0f / sq;
+    }
+  }
+  return 0;
+}

@@ -42,6 +42,9 @@ def load():
             fp, fp, fp, ctypes.c_int, ctypes.c_int, ctypes.c_int, fp,
             ctypes.POINTER(ctypes.c_uint16), fp]
         lib.fa_oracle_combine_f32.restype = ctypes.c_int
+        lib.fa_oracle_welford_combine_f32.argtypes = [
+            fp, fp, fp, ctypes.c_int, ctypes.c_int, ctypes.c_float, fp, fp, fp]
+        lib.fa_oracle_welford_combine_f32.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -77,3 +80,22 @@ def combine_f32(part_m, part_d, part_o):
     if rc != 0:
         raise ValueError("fa_oracle_combine_f32: bad sizes")
     return out_o, out_b, out_l
+
+
+def welford_combine_f32(part_n, part_mu, part_m2, eps=0.0):
+    """part_* [rows, S] (castable exactly to float32).  Returns mean, var and
+    rstd = 1/sqrt(var + eps), fp32 [rows], from the fixed-order C fold."""
+    n = np.ascontiguousarray(part_n, dtype=np.float32)
+    mu = np.ascontiguousarray(part_mu, dtype=np.float32)
+    m2 = np.ascontiguousarray(part_m2, dtype=np.float32)
+    rows, S = n.shape
+    assert mu.shape == (rows, S) and m2.shape == (rows, S)
+    mean = np.empty((rows,), np.float32)
+    var = np.empty((rows,), np.float32)
+    rstd = np.empty((rows,), np.float32)
+    rc = load().fa_oracle_welford_combine_f32(_fptr(n), _fptr(mu), _fptr(m2), rows, S,
+                                              ctypes.c_float(eps), _fptr(mean), _fptr(var),
+                                              _fptr(rstd))
+    if rc != 0:
+        raise ValueError("fa_oracle_welford_combine_f32: bad sizes")
+    return mean, var, rstd

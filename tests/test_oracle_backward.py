@@ -70,3 +70,19 @@ def test_gradient_identities():
     np.testing.assert_allclose(dq1, 0.0, atol=1e-14)
     np.testing.assert_allclose(dk1, 0.0, atol=1e-14)
     np.testing.assert_array_equal(dv1, do[:1])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_sampled_equals_full(causal):
+    """The row/column-at-a-time backward used at full sizes agrees with the
+    whole-matrix one (itself pinned above by finite differences), incl. rows
+    and columns at both ends and chunk sizes that do not divide N."""
+    N, D = 70, 6
+    q, k, v, do = _case(N, D, 11 + causal, std=1.3)
+    dq, dk, dv, _ = ora.attention_bwd_head_ref(q, k, v, do, 0.45, causal)
+    rows = [0, 1, 33, 68, 69]
+    cols = [0, 2, 35, 69]
+    sq, sk, sv = ora.attention_bwd_sampled_ref(q, k, v, do, 0.45, causal, rows, cols, chunk=16)
+    np.testing.assert_allclose(sq, dq[rows], rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(sk, dk[cols], rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(sv, dv[cols], rtol=1e-11, atol=1e-13)
