@@ -44,6 +44,7 @@ SIGNATURES = {
     "fa_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
     "fa_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I]),
     "fa_row_stats": (_I, [_P, _I, _I, _I, _F, _P, _P, _P, _P]),
+    "fa_prefix_attention": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P]),
     "fa_row_stats_workspace_bytes": (ctypes.c_size_t, [_I, _I]),
     "fa_row_stats_partials": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P]),
     "fa_row_stats_combine": (_I, [_P, _P, _P, _I, _I, _F, _P, _P, _P, _P]),
@@ -218,6 +219,30 @@ def fa_bwd(q, k, v, o, do, lse, scale=None, causal=False, dq=None, dk=None, dv=N
                     int(bool(causal)), _stream(q))
     _check(rc, "fa_bwd")
     return dq, dk, dv
+
+
+def fa_prefix_attention(q, k_cache, v_cache, cu_seqlens_k, scale=None, o=None, lse=None):
+    """Attention of q[b, h] over every prefix of sequence b's keys
+    (fa_prefix_attention).  q [B, H, D]; caches packed [T, H, D] bf16;
+    cu_seqlens_k int32 [B + 1] on the device.  Returns o [T, H, D] bf16 and
+    lse [H, T] fp32."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 3)
+    _need(v_cache, "v_cache", torch.bfloat16, 3)
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache must have the same shape")
+    _need(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+    B, H, D = q.shape
+    T = k_cache.shape[0]
+    if k_cache.shape[1:] != (H, D) or cu_seqlens_k.numel() != B + 1:
+        raise ValueError("shapes: q [B, H, D], caches [T, H, D], cu_seqlens_k [B + 1]")
+    o = torch.empty_like(k_cache) if o is None else o
+    lse = torch.empty((H, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    rc = load_library().fa_prefix_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                            _ptr(cu_seqlens_k), T, B, H, D, _scale(scale, D),
+                                            _ptr(o), _ptr(lse), _stream(q))
+    _check(rc, "fa_prefix_attention")
+    return o, lse
 
 
 def _rows_dtype(x):
@@ -447,6 +472,7 @@ __all__ = [
     "fa_fwd", "fa_fwd_f32", "fa_fwd_ex", "fa_fwd_window", "fa_fwd_varlen", "fa_bwd",
     "fa_bwd_workspace_bytes", "fa_decode_workspace_bytes", "fa_row_stats",
     "fa_row_stats_workspace_bytes", "fa_row_stats_partials", "fa_row_stats_combine",
+    "fa_prefix_attention",
     "fa_decode_splitkv", "fa_combine_states", "fa_decode_splitkv_noalloc",
     "fa_decode_paged_splitkv",
     "fa_check_device_status",

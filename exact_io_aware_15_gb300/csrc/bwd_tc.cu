@@ -127,6 +127,21 @@ __device__ __forceinline__ void store_row(uint32_t tmem_row, void* dst, size_t r
   }
 }
 
+// Which tile a CTA of the 1-D grid (heads x 128-row tiles) takes.  Heads go
+// in groups of four and, inside a group, the heaviest tiles (under causal
+// masking) first: the tensors the tiles stream (Q and dO, or K and V: 4
+// heads x 8 MB at N = 16384, D = 128) stay in L2 while the group runs.
+// Returns the head and the tile's rank by weight (0 = heaviest).
+__device__ __forceinline__ void tile_of(int nt, int BH, int& bh, int& rank) {
+  const long long lin = blockIdx.x;
+  const long long per_group = 4LL * nt;
+  const int g = static_cast<int>(lin / per_group);
+  const int gsize = min(4, BH - g * 4);
+  const int rr = static_cast<int>(lin - g * per_group);
+  rank = rr / gsize;
+  bh = g * 4 + rr % gsize;
+}
+
 // ============================================================ dK / dV
 
 template <int D>
@@ -154,8 +169,7 @@ struct DkdvCfg {
   static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 384;
 };
 
-// One CTA per (head, 128-key tile n); key tiles with the most query tiles
-// (the first ones under causal masking) launch first.
+// One CTA per (head, 128-key tile n), in tile_of's order.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -174,8 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int N = args.N;
   const int nt = args.num_tiles;
-  const int n = static_cast<int>(blockIdx.x) / args.BH;
-  const int bh = static_cast<int>(blockIdx.x) % args.BH;
+  int bh, n;  // key tile n sees query tiles n..nt-1 under causal masking
+  tile_of(nt, args.BH, bh, n);
   const int t_begin = args.causal ? n : 0;  // first query tile that sees key tile n
   const int count = nt - t_begin;
 
@@ -410,8 +424,7 @@ struct DqCfg {
   static constexpr uint32_t TM_S0 = 0, TM_DP = 256, TM_DQ = 384;
 };
 
-// One CTA per (head, 128-query tile m); query tiles with the most key tiles
-// (the last ones under causal masking) launch first.
+// One CTA per (head, 128-query tile m), in tile_of's order.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -430,8 +443,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int N = args.N;
   const int nt = args.num_tiles;
-  const int m = nt - 1 - static_cast<int>(blockIdx.x) / args.BH;
-  const int bh = static_cast<int>(blockIdx.x) % args.BH;
+  int bh, rank;  // query tile m sees key tiles 0..m under causal masking
+  tile_of(nt, args.BH, bh, rank);
+  const int m = nt - 1 - rank;
   const int count = args.causal ? m + 1 : nt;  // key tiles 0 .. count-1
 
   if (threadIdx.x == 0) {

@@ -504,6 +504,35 @@ int fa_row_stats_combine(const float* part_n, const float* part_mu, const float*
   return launched(fa::launch_row_stats_combine(a, static_cast<cudaStream_t>(stream)));
 }
 
+int fa_prefix_attention(const void* q, const void* k_cache, const void* v_cache,
+                        const int* cu_seqlens_k, int total_kv_tokens, int B, int H, int D,
+                        float scale, void* o, float* lse, void* stream) {
+  if (B < 0 || H < 0 || total_kv_tokens < 0 || (D != 64 && D != 128) || !good_scale(scale))
+    return FA_ERR_INVALID_ARG;
+  if (B == 0 || H == 0) return FA_OK;
+  if (!aligned16(q) || !aligned4(cu_seqlens_k)) return FA_ERR_INVALID_ARG;
+  if (total_kv_tokens > 0 && (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
+                              !aligned4(lse)))
+    return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  unsigned int* status = nullptr;
+  int rc = current_device(&status);
+  if (rc != FA_OK) return rc;
+  fa::ScanArgs a{};
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.cu_seqlens_k = cu_seqlens_k;
+  a.total_kv = total_kv_tokens;
+  a.B = B;
+  a.H = H;
+  a.scale_log2 = scale_log2(scale);
+  a.o = o;
+  a.lse = lse;
+  a.status = status;
+  return launched(fa::launch_prefix_scan(a, D, static_cast<cudaStream_t>(stream)));
+}
+
 int fa_check_device_status(void* stream) {
   unsigned int* status = nullptr;
   int rc = current_device(&status);

@@ -139,6 +139,21 @@ struct RowStatsCombineArgs {
 };
 cudaError_t launch_row_stats_combine(const RowStatsCombineArgs& a, cudaStream_t stream);
 
+// Prefix attention (scan.cu): every prefix of every sequence's keys.
+struct ScanArgs {
+  const void* q;        // [B, H, D] bf16
+  const void* k_cache;  // [T, H, D] bf16, packed sequences
+  const void* v_cache;
+  const int* cu_seqlens_k;  // [B + 1]
+  int total_kv;             // T
+  int B, H;
+  float scale_log2;
+  void* o;                  // [T, H, D] bf16
+  float* lse;               // [H, T]
+  unsigned int* status;
+};
+cudaError_t launch_prefix_scan(const ScanArgs& a, int D, cudaStream_t stream);
+
 // The sm_103 check of the current device and its device status word, as used
 // by every entry point of fa_api.cu (returns an FA_* status code).
 int checked_current_device(unsigned int** status);

@@ -11,11 +11,12 @@
 //     n = n_a + n_b,  delta = mu_b - mu_a,  r = n_b / n,
 //     mu = mu_a + delta r,  M2 = M2_a + M2_b + delta^2 n_a r.
 //
-// fa_row_stats_kernel: a group of WARPS warps reduces one segment (a row, or
-// one column chunk of a row).  Each thread folds 16-byte packs (8 bf16 or 4
-// fp32 values): the pack's own state by its definition (mean of the pack,
-// then the sum of squared deviations), merged into the thread's running
-// state; then the lanes merge by shuffles (lane i with lane i + off) and the
+// fa_row_stats_kernel: a group of WARPS warps (1, or 8 for segments of at
+// least 16384 elements) reduces one segment (a row, or one column chunk of a
+// row).  Each thread folds 16-byte packs (4 fp32 values, or bf16 in pairs of
+// packs, 16 values, in the unrolled loop and 8 in the remainder): the
+// pack's own state by its definition (mean of the pack, then the sum of
+// squared deviations), merged into the thread's running state; then the lanes merge by shuffles (lane i with lane i + off) and the
 // warps of a group in index order through shared memory.  The fold order
 // depends only on the sizes, so results are deterministic.  Loads are 16-byte
 // and streaming (no L1 allocation); ragged heads and tails of a segment that
@@ -73,6 +74,34 @@ __device__ __forceinline__ Welford pack_state(const float (&v)[VEC]) {
   return Welford{static_cast<float>(VEC), mu, m2};
 }
 
+// The state of the 16 bf16 values of two 16-byte packs by its definition,
+// in packed pairs: mean = (sum of the pairs) / 16, then the sum of squared
+// deviations.
+__device__ __forceinline__ Welford pack_state_bf16x16(const uint4& a, const uint4& b) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  float2 v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    v[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+  float2 s[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) s[i] = __fadd2_rn(v[i], v[i + 4]);
+  s[0] = __fadd2_rn(s[0], s[2]);
+  s[1] = __fadd2_rn(s[1], s[3]);
+  s[0] = __fadd2_rn(s[0], s[1]);
+  const float mu = (s[0].x + s[0].y) * (1.f / 16.f);  // exact scaling by a power of two
+  const float2 nm = make_float2(-mu, -mu);
+  float2 q0 = make_float2(0.f, 0.f), q1 = q0;
+#pragma unroll
+  for (int i = 0; i < 8; i += 2) {
+    const float2 d0 = __fadd2_rn(v[i], nm), d1 = __fadd2_rn(v[i + 1], nm);
+    q0 = __ffma2_rn(d0, d0, q0);
+    q1 = __ffma2_rn(d1, d1, q1);
+  }
+  q0 = __fadd2_rn(q0, q1);
+  return Welford{16.f, mu, q0.x + q0.y};
+}
+
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
   uint4 r;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -111,7 +140,7 @@ __global__ void __launch_bounds__(256) fa_row_stats_kernel(const RowStatsArgs a)
   constexpr int ESZ = BF16 ? 2 : 4;        // element bytes
   constexpr int G = WARPS * 32;            // threads per segment
   constexpr int GROUPS = 8 / WARPS;        // segments per CTA
-  constexpr int UNROLL = 4;                // packs in flight per thread
+  constexpr int UNROLL = WARPS == 1 ? 8 : 4;  // packs in flight per thread
   __shared__ Welford part[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = warp / WARPS;
@@ -142,11 +171,16 @@ __global__ void __launch_bounds__(256) fa_row_stats_kernel(const RowStatsArgs a)
       uint4 u[UNROLL];
 #pragma unroll
       for (int k = 0; k < UNROLL; ++k) u[k] = ld_stream(body + p + k * G);
+      if constexpr (BF16) {
 #pragma unroll
-      for (int k = 0; k < UNROLL; ++k) {
-        float v[VEC];
-        unpack<BF16, VEC>(u[k], v);
-        st = merge(st, pack_state<VEC>(v));
+        for (int k = 0; k < UNROLL; k += 2) st = merge(st, pack_state_bf16x16(u[k], u[k + 1]));
+      } else {
+#pragma unroll
+        for (int k = 0; k < UNROLL; ++k) {
+          float v[VEC];
+          unpack<BF16, VEC>(u[k], v);
+          st = merge(st, pack_state<VEC>(v));
+        }
       }
     }
     for (; p < npk; p += G) {
@@ -226,10 +260,10 @@ cudaError_t launch_stats(const RowStatsArgs& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_row_stats(const RowStatsArgs& a, cudaStream_t stream) {
-  // Segments of at least 2048 elements get a whole CTA (8 warps), shorter
-  // ones a warp each.
+  // A warp per segment keeps 8 packs (128 bytes) per lane in flight; only
+  // segments of at least 16384 elements get a whole CTA (8 warps).
   const long long seg_len = (static_cast<long long>(a.C) + a.S - 1) / a.S;
-  const bool wide = seg_len >= 2048;
+  const bool wide = seg_len >= 16384;
   if (a.bf16) return wide ? launch_stats<8, true>(a, stream) : launch_stats<1, true>(a, stream);
   return wide ? launch_stats<8, false>(a, stream) : launch_stats<1, false>(a, stream);
 }

@@ -191,6 +191,28 @@ int fa_row_stats_combine(const float* part_n, const float* part_mu, const float*
                          float* rstd, void* stream);
 
 /*
+ * Prefix attention: for every sequence b, head h and key position i of the
+ * sequence, the attention of q[b, h] over keys 0..i -- the inclusive scan of
+ * the keys' (m, d, o) states under the merge of "Learning FlashAttention the
+ * Hard Way - Part 1" ("Why Attention's Combine Still Associates": the merge
+ * is associative with identity (-inf, 0, 0), so exact attention runs as a
+ * parallel prefix scan).  The last position of a sequence is its decode
+ * output; with the query repeated on every row it is causal attention.
+ *   q            : bf16 [B, H, D]
+ *   k_cache, v_cache : bf16 [T_k, H, D], packed sequences
+ *   cu_seqlens_k : int32 [B + 1] DEVICE array (checked against
+ *                  total_kv_tokens on the device: FA_ERR_DEVICE_BOUNDS)
+ *   o            : bf16 [T_k, H, D]  O_i of the prefix ending at token i (written)
+ *   lse          : f32  [H, T_k]     natural-log LSE of that prefix (written)
+ *   D in {64, 128}.  K and V are read once (one CTA per (b, h) walks its
+ *   sequence in windows of 128 keys; within a window the scan has two
+ *   levels: 16 keys per warp, 8 warp totals).
+ */
+int fa_prefix_attention(const void* q, const void* k_cache, const void* v_cache,
+                        const int* cu_seqlens_k, int total_kv_tokens, int B, int H, int D,
+                        float scale, void* o, float* lse, void* stream);
+
+/*
  * Bytes of the partial-state workspace fa_decode_splitkv writes:
  * part_m and part_d f32 [B, H, num_splits], part_o f32 [B, H, num_splits, D].
  * Returns 0 for invalid sizes.

@@ -445,3 +445,74 @@ def all_chunkings(n: int) -> list[list[tuple[int, int]]]:
         cuts = [0] + [i + 1 for i in range(n - 1) if mask >> i & 1] + [n]
         out.append([(cuts[i], cuts[i + 1]) for i in range(len(cuts) - 1)])
     return out
+
+
+# ---------------------------------------------------------------------------
+# Prefix scan of the (m, d, o) monoid.  "Learning FlashAttention the Hard Way
+# - Part 1", section "Why Attention's Combine Still Associates", ties the
+# monoid to running exact attention as a parallel prefix scan (the ELSA
+# reference, O(log n) depth).  Read here as: for one query vector against a
+# sequence of keys, the inclusive scan of the keys' states gives, at every
+# position i, the attention over keys 0..i.
+
+
+def scan_left(states, D: int, base: float = math.e):
+    """Inclusive scan by a left fold: prefix i = s_0 (+) ... (+) s_i."""
+    out = []
+    acc = identity(D)
+    for u in states:
+        acc = merge(acc, u, base)
+        out.append(acc)
+    return out
+
+
+def scan_tree(states, D: int, base: float = math.e):
+    """The same prefixes by the two-sweep tree scan (O(log n) depth): the
+    up-sweep stores subtree totals at the right child of every pair, the
+    down-sweep hands each node the total of everything to its left, and the
+    inclusive prefix is that exclusive prefix (+) the element."""
+    n = len(states)
+    size = 1
+    while size < n:
+        size *= 2
+    t = list(states) + [identity(D) for _ in range(size - n)]
+    step = 1
+    while step < size:
+        for i in range(2 * step - 1, size, 2 * step):
+            t[i] = merge(t[i - step], t[i], base)
+        step *= 2
+    t[size - 1] = identity(D)
+    step = size // 2
+    while step >= 1:
+        for i in range(2 * step - 1, size, 2 * step):
+            left = t[i - step]
+            t[i - step] = t[i]
+            t[i] = merge(t[i], left, base)
+        step //= 2
+    return [merge(t[i], states[i], base) for i in range(n)]
+
+
+def prefix_attention_ref(q, k_cache, v_cache, cu_seqlens_k, scale, batch=None, heads=None,
+                         positions=None):
+    """For every sequence b and head h, the attention of q[b, h] over keys
+    0..i of the sequence, at every position i (or at the in-sequence
+    positions listed in ``positions[b]``), by the plain definition on each
+    prefix.  q [B, H, D]; caches packed [T_k, H, D].  Returns O [T_k, H, D]
+    and LSE [H, T_k] (natural log); entries not computed are NaN."""
+    q, kc, vc = to_f64(q), to_f64(k_cache), to_f64(v_cache)
+    cu = [int(x) for x in np.asarray(cu_seqlens_k).tolist()]
+    B, H, D = q.shape
+    T = kc.shape[0]
+    O = np.full((T, H, D), np.nan)
+    LSE = np.full((H, T), np.nan)
+    for b in (range(B) if batch is None else batch):
+        a, e = cu[b], cu[b + 1]
+        pos = range(e - a) if positions is None else positions[b]
+        for h in (range(H) if heads is None else heads):
+            for i in pos:
+                s = scores(q[b, h][None, :], kc[a:a + i + 1, h], scale)[0]
+                m = s.max()
+                w = np.exp(s - m)
+                O[a + i, h] = (w @ vc[a:a + i + 1, h]) / w.sum()
+                LSE[h, a + i] = m + math.log(w.sum())
+    return O, LSE
