@@ -244,8 +244,9 @@ def _time_launches(fn, iters: int, warmup: int = 2) -> float:
 def other_configs(fa):
     """The remaining workloads, each timed on its own after the main timed
     region (not part of `value`): dense causal B=4 H=16 N=2048 D=128, the
-    ragged varlen prefill (65536 tokens, H=16, D=64 and 128) and the fp32
-    path (B=H=1, N=256, D=64)."""
+    ragged varlen prefill (65536 tokens, H=16, D=64 and 128), the causal
+    sliding window, the backward, the Welford row statistics, prefix
+    attention, paged GQA decode and the fp32 path (B=H=1, N=256, D=64)."""
     out = {}
     c2 = inp.config2(device="cuda")
     ms = _time_launches(lambda: fa.fa_fwd(c2.q, c2.k, c2.v, c2.scale, True), 20)
@@ -297,6 +298,20 @@ def other_configs(fa):
     out["rowstats_split_R64_C4194304_f32_S128"] = {
         "gbs": 64 * (1 << 22) * 4 / (ms * 1e-3) / 1e9, "ms": ms}
     del ys
+    # prefix attention over the decode workload's caches: every prefix of
+    # every sequence (K, V read once, O and LSE written for every key)
+    pc = inp.decode(DECODE["B"], DECODE["H"], DECODE["D"], seed=4, num_splits=DECODE["S"],
+                    device="cuda")
+    cu = pc.cu_seqlens_k.cuda()
+    T = pc.meta["T"]
+    po = torch.empty_like(pc.k_cache)
+    pl = torch.empty((DECODE["H"], T), dtype=torch.float32, device="cuda")
+    ms = _time_launches(lambda: fa.fa_prefix_attention(pc.q, pc.k_cache, pc.v_cache, cu,
+                                                       pc.scale, po, pl), 10)
+    sb = float(T) * DECODE["H"] * DECODE["D"] * 2 * 3 + float(T) * DECODE["H"] * 4
+    out["prefix_scan_B64_H32_D128_L1024-32768"] = {"gbs": sb / (ms * 1e-3) / 1e9, "ms": ms,
+                                                   "bytes": sb}
+    del pc, po, pl
     # paged KV decode with grouped query heads: the decode lengths, H=32 over
     # H_kv=8, pages of 64 keys
     pc = inp.paged_decode(64, 32, 8, 128, 64, seed=4, num_splits=16, device="cuda")

@@ -95,7 +95,7 @@ __device__ __forceinline__ void merge_into(float& m, float& d, float (&o)[VPL], 
 }
 
 template <int D>
-__global__ void __launch_bounds__(256) fa_prefix_scan_kernel(const ScanArgs a) {
+__global__ void __launch_bounds__(256, 2) fa_prefix_scan_kernel(const ScanArgs a) {
   constexpr int VPL = D / 32;
   __shared__ float tot_m[8], tot_d[8];
   __shared__ __align__(16) float tot_o[8][D];
@@ -129,17 +129,21 @@ __global__ void __launch_bounds__(256) fa_prefix_scan_kernel(const ScanArgs a) {
 #pragma unroll
   for (int j = 0; j < VPL; ++j) co[j] = 0.f;
 
+  // This warp's rows of window w0: K is consumed by the scores and V by the
+  // rescan, so the next window's K is loaded right after the scores and its
+  // V right after the rescan (the loads overlap the rest of the window).
+  Cols<VPL> kr[kKeysPerWarp], vr[kKeysPerWarp];
+  auto load_rows = [&](Cols<VPL>(&r)[kKeysPerWarp], const uint16_t* base, int w0) {
+    const int k0 = w0 + warp * kKeysPerWarp;
+#pragma unroll
+    for (int i = 0; i < kKeysPerWarp; ++i)
+      if (k0 + i < L) r[i] = ld_cols<VPL>(base + static_cast<size_t>(k0 + i) * stride);
+  };
+  load_rows(kr, kp, 0);
+  load_rows(vr, vp, 0);
   for (int w0 = 0; w0 < L; w0 += kWindow) {
     const int k0 = w0 + warp * kKeysPerWarp;  // this warp's first key
     const int nk = max(0, min(kKeysPerWarp, L - k0));
-    Cols<VPL> kr[kKeysPerWarp], vr[kKeysPerWarp];
-#pragma unroll
-    for (int i = 0; i < kKeysPerWarp; ++i) {
-      if (i < nk) {
-        kr[i] = ld_cols<VPL>(kp + static_cast<size_t>(k0 + i) * stride);
-        vr[i] = ld_cols<VPL>(vp + static_cast<size_t>(k0 + i) * stride);
-      }
-    }
     // phase A: scores and the segment total
     float sg[kKeysPerWarp];
 #pragma unroll
@@ -153,6 +157,7 @@ __global__ void __launch_bounds__(256) fa_prefix_scan_kernel(const ScanArgs a) {
       for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
       sg[i] = i < nk ? s * c : -INFINITY;
     }
+    load_rows(kr, kp, w0 + kWindow);
     float lm = -INFINITY;
 #pragma unroll
     for (int i = 0; i < kKeysPerWarp; ++i) lm = fmaxf(lm, sg[i]);
@@ -209,6 +214,7 @@ __global__ void __launch_bounds__(256) fa_prefix_scan_kernel(const ScanArgs a) {
         if (lane == 0) lp[k0 + i] = kLn2 * (m + __log2f(d));
       }
     }
+    load_rows(vr, vp, w0 + kWindow);
     // carry of this window: every warp folds all 8 totals in the same order
 #pragma unroll 1
     for (int w = 0; w < 8; ++w) merge_into<VPL>(cm, cd, co, tot_m[w], tot_d[w], &tot_o[w][lane * VPL]);
