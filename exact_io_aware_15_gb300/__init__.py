@@ -209,7 +209,7 @@ def fa_bwd(q, k, v, o, do, lse, scale=None, causal=False, dq=None, dk=None, dv=N
         _need(t, n, torch.bfloat16, 4)
     lib = load_library()
     if workspace is None:
-        workspace = torch.empty(max(1, lib.fa_bwd_workspace_bytes(B, H, N) // 4),
+        workspace = torch.empty(max(1, fa_bwd_workspace_bytes(B, H, N) // 4),
                                 dtype=torch.float32, device=q.device)
     _need(workspace, "workspace", torch.float32, 1)
     if workspace.numel() * 4 < lib.fa_bwd_workspace_bytes(B, H, N):
@@ -338,6 +338,14 @@ def fa_fwd_varlen(q, k, v, cu_seqlens, max_seqlen, scale=None, causal=True,
 
 def fa_decode_workspace_bytes(B: int, H: int, D: int, num_splits: int) -> int:
     return int(load_library().fa_decode_workspace_bytes(B, H, D, num_splits))
+
+
+def fa_bwd_workspace_bytes(B: int, H: int, N: int) -> int:
+    return int(load_library().fa_bwd_workspace_bytes(B, H, N))
+
+
+def fa_row_stats_workspace_bytes(R: int, num_splits: int) -> int:
+    return int(load_library().fa_row_stats_workspace_bytes(R, num_splits))
 
 
 def fa_decode_splitkv(q, k_cache, v_cache, cu_seqlens_k, num_splits, scale=None,

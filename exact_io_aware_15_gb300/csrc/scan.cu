@@ -8,7 +8,8 @@
 // parallel prefix scan (the ELSA reference).  States are kept in the base-2
 // coordinates of section "Alternative Twist: Base 2" (sigma = s log2 e).
 //
-// fa_prefix_scan_kernel<D>: one CTA (8 warps) per (sequence, head).  The
+// fa_prefix_scan_kernel<D>: one CTA (8 warps) per (sequence, head), longest
+// sequences first.  The
 // sequence is walked in windows of 128 keys, 16 per warp, in two phases:
 //   A. each warp loads its 16 key and value rows into registers (lane l owns
 //      columns [l*D/32, (l+1)*D/32)), computes the 16 scores (warp-reduced
@@ -35,6 +36,7 @@ namespace {
 constexpr int kKeysPerWarp = 16;
 constexpr int kWindow = 8 * kKeysPerWarp;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kRankedSeqs = 256;
 
 template <int VPL>
 struct Cols;  // a lane's VPL bf16 columns of one row
@@ -101,8 +103,26 @@ __global__ void __launch_bounds__(256, 2) fa_prefix_scan_kernel(const ScanArgs a
   __shared__ __align__(16) float tot_o[8][D];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = a.H;
-  const int b = static_cast<int>(blockIdx.x) / H;
   const int h = static_cast<int>(blockIdx.x) % H;
+  // Longest sequences first (ties by index), so the longest rows do not
+  // start last: with up to kRankedSeqs sequences every CTA ranks the lengths
+  // itself (a permutation for any values read); beyond that, index order.
+  int b = static_cast<int>(blockIdx.x) / H;
+  if (a.B <= kRankedSeqs) {
+    __shared__ int s_len[kRankedSeqs];
+    __shared__ int s_seq;
+    for (int i = threadIdx.x; i < a.B; i += blockDim.x)
+      s_len[i] = __ldg(a.cu_seqlens_k + i + 1) - __ldg(a.cu_seqlens_k + i);
+    __syncthreads();
+    for (int i = threadIdx.x; i < a.B; i += blockDim.x) {
+      const int li = s_len[i];
+      int rank = 0;
+      for (int j = 0; j < a.B; ++j) rank += (s_len[j] > li) || (s_len[j] == li && j < i);
+      if (rank == b) s_seq = i;
+    }
+    __syncthreads();
+    b = s_seq;
+  }
   const int k_begin = __ldg(a.cu_seqlens_k + b);
   const int k_end = __ldg(a.cu_seqlens_k + b + 1);
   if (k_begin < 0 || k_end < k_begin || k_end > a.total_kv) {

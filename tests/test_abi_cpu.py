@@ -79,3 +79,10 @@ def test_host_validation_without_gpu(lib):
     assert lib.fa_decode_paged_splitkv(p, p, p, p, p, 4, 16, 4, 1, 8, 3, 128, 4, 0.1,
                                        p, p, p, null) == -1
     assert lib.fa_fwd_window(p, p, p, p, p, 1, 1, 16, 64, 0.1, 0, null) == -1
+
+
+def test_binding_exports_exist():
+    """Every name the binding exports is defined (no GPU needed)."""
+    import exact_io_aware_15_gb300 as fa
+    for name in fa.__all__:
+        assert hasattr(fa, name), name
