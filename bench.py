@@ -20,6 +20,7 @@ of the prefill workload per step (rank 0 only).
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -27,7 +28,9 @@ import os
 import statistics
 import subprocess
 import sys
+import threading
 import time
+from typing import Optional
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
@@ -76,52 +79,122 @@ def load_traffic(kernel: str, source: str):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
-    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock and clock-event (throttle) reasons sampled while the timed
+    region runs.  Reads NVML through ctypes every 20 ms in a background thread
+    (read-only queries), keeping the samples taken between mark_start() and
+    mark_end(); without NVML it falls back to `nvidia-smi -lms 50`."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown"}
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, uuid: Optional[str] = None):
         self.index = index
+        self.uuid = uuid
+        self.samples = []  # (time, sm_mhz, reasons bitmask)
+        self.max_mhz = None
+        self.t0 = self.t1 = None
         self.proc = None
+        self.thread = None
+        self.stop = threading.Event()
+
+    def _nvml(self):
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            return None
+        h = ctypes.c_void_p()
+        ok = False
+        if self.uuid:
+            ok = lib.nvmlDeviceGetHandleByUUID(self.uuid.encode(), ctypes.byref(h)) == 0
+        if not ok:
+            ok = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index),
+                                                   ctypes.byref(h)) == 0
+        if not ok:
+            return None
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # 1 = SM clock
+            self.max_mhz = float(mx.value)
+        reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        return lib, h, reasons
+
+    def _poll(self, lib, h, reasons):
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self.stop.is_set():
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                r = rs.value if reasons(h, ctypes.byref(rs)) == 0 else 0
+                self.samples.append((time.perf_counter(), float(clk.value), int(r)))
+            self.stop.wait(0.02)
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            nv = self._nvml()
         except OSError:
-            self.proc = None
+            nv = None
+        if nv is not None:
+            self.thread = threading.Thread(target=self._poll, args=nv, daemon=True)
+            self.thread.start()
+        else:
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.index),
+                     "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                     "clocks_event_reasons.hw_thermal_slowdown,"
+                     "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                     "--format=csv,noheader,nounits", "-lms", "50"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except OSError:
+                self.proc = None
+        time.sleep(0.1)  # let the first samples arrive before the timed region
         return self
 
+    def mark_start(self):
+        self.t0 = time.perf_counter()
+
+    def mark_end(self):
+        self.t1 = time.perf_counter()
+
     def __exit__(self, *exc):
-        self.out = ""
+        self.stop.set()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
         if self.proc is not None:
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                out, _ = self.proc.communicate(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                self.out, _ = self.proc.communicate()
+                out, _ = self.proc.communicate()
+            bits = [0x8, 0x40, 0x20, 0x4]
+            for line in (out or "").strip().splitlines():
+                parts = [x.strip() for x in line.split(",")]
+                try:
+                    sm = float(parts[0])
+                    self.max_mhz = float(parts[1])
+                except (ValueError, IndexError):
+                    continue
+                r = sum(b for b, v in zip(bits, parts[2:6]) if v.lower() == "active")
+                self.samples.append((None, sm, r))
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in (self.out or "").strip().splitlines():
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 7:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                mx = float(parts[1])
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[3:7]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+        inside = [x for x in self.samples
+                  if x[0] is None or self.t0 is None or self.t0 <= x[0] <= (self.t1 or x[0])]
+        sm = [x[1] for x in inside]
+        reasons = set()
+        for x in inside:
+            for bit, name in self.REASONS.items():
+                if x[2] & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_uuid(dev) -> Optional[str]:
+    """NVML's name of the CUDA device ("GPU-<uuid>"), when torch knows it."""
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+    except (AttributeError, RuntimeError):
+        return None
+    return u if u.startswith("GPU-") else "GPU-" + u
 
 
 def dist_setup(n_gpus: int):
@@ -314,11 +387,12 @@ def other_configs(fa):
     del pc, po, pl
     # paged KV decode with grouped query heads: the decode lengths, H=32 over
     # H_kv=8, pages of 64 keys
-    pc = inp.paged_decode(64, 32, 8, 128, 64, seed=4, num_splits=16, device="cuda")
+    # (4 KV chunks per sequence: B * H_kv * 4 = 2048 CTAs of 128-key tiles)
+    pc = inp.paged_decode(64, 32, 8, 128, 64, seed=4, num_splits=4, device="cuda")
     tab, sl = pc.block_table.cuda(), pc.seqlens.cuda()
 
     def paged():
-        pm, pd, po = fa.fa_decode_paged_splitkv(pc.q, pc.k_pages, pc.v_pages, tab, sl, 16,
+        pm, pd, po = fa.fa_decode_paged_splitkv(pc.q, pc.k_pages, pc.v_pages, tab, sl, 4,
                                                 pc.scale)
         fa.fa_combine_states(pm, pd, po)
     ms = _time_launches(paged, 10)
@@ -379,12 +453,14 @@ def run_gpu(args, rank, world, dist):
     end = torch.cuda.Event(enable_timing=True)
     barrier(dist)
     torch.cuda.synchronize()
-    with ClockSampler(dev.index) as clk:
+    with ClockSampler(dev.index, gpu_uuid(dev)) as clk:
+        clk.mark_start()
         start.record(stream)
         for s in range(args.steps):
             step(evs[s])
         end.record(stream)
         torch.cuda.synchronize()
+        clk.mark_end()
     barrier(dist)
     total_ms = start.elapsed_time(end)
     t_pre = [e[0].elapsed_time(e[1]) for e in evs]

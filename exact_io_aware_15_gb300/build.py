@@ -20,7 +20,8 @@ CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT, "libfa_gb300.so")
 SOURCES = ["fa_api.cu", "fwd_tc.cu", "fwd_f32.cu", "decode.cu", "combine.cu",
-           "decode_noalloc.cu", "bwd_tc.cu", "rowstats.cu", "scan.cu"]
+           "decode_noalloc.cu", "bwd_tc.cu", "rowstats.cu", "scan.cu",
+           "decode_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

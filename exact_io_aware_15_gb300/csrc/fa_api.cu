@@ -432,6 +432,22 @@ int fa_decode_paged_splitkv(const void* q, const void* k_pages, const void* v_pa
   a.part_d = part_d;
   a.part_o = part_o;
   a.status = status;
+  const int G = H / H_kv;
+  const long long pool_rows = static_cast<long long>(num_pages) * page_size;
+  if (fa::decode_paged_tc_supported(D, G, page_size) && num_pages > 0 &&
+      pool_rows <= 0x7fffffffLL - 256) {
+    // query heads of a group packed into one tensor-core product
+    rc = get_encoder();
+    if (rc != FA_OK) return rc;
+    fa::PagedTcMaps maps;
+    const uint64_t rs = static_cast<uint64_t>(D) * 2u;
+    const uint32_t R = static_cast<uint32_t>(page_size < 128 ? page_size : 128);
+    if (encode_map(&maps.q, q, D, H, B, rs, rs * H, 16u, 1u) != FA_OK ||
+        encode_map(&maps.k, k_pages, D, H_kv, pool_rows, rs, rs * H_kv, 1u, R) != FA_OK ||
+        encode_map(&maps.v, v_pages, D, H_kv, pool_rows, rs, rs * H_kv, 1u, R) != FA_OK)
+      return FA_ERR_DRIVER;
+    return launched(fa::launch_decode_paged_tc(maps, a, G, static_cast<cudaStream_t>(stream)));
+  }
   return launched(fa::launch_decode_paged(a, D, static_cast<cudaStream_t>(stream)));
 }
 

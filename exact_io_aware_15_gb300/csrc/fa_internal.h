@@ -75,6 +75,16 @@ struct PagedDecodeArgs {
 };
 cudaError_t launch_decode_paged(const PagedDecodeArgs& a, int D, cudaStream_t stream);
 
+// Tensor-core paged decode (decode_tc.cu): D = 128, 2 <= H / H_kv <= 16,
+// page_size >= 8.  Maps: q (D, H, B) box (64, 16, 1); k and v pools
+// (D, H_kv, num_pages * page_size) box (64, 1, min(page_size, 128)).
+struct PagedTcMaps {
+  CUtensorMap q, k, v;
+};
+bool decode_paged_tc_supported(int D, int G, int page_size);
+cudaError_t launch_decode_paged_tc(const PagedTcMaps& maps, const PagedDecodeArgs& a, int G,
+                                   cudaStream_t stream);
+
 // Arguments of the backward kernels (dense bf16 [B, H, N, D], D = 64 or 128).
 struct BwdArgs {
   int BH;            // B * H

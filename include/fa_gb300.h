@@ -256,6 +256,12 @@ int fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
  * [0, num_pages)) and reports FA_ERR_DEVICE_BOUNDS through
  * fa_check_device_status instead of reading out of range; such keys are left
  * out of the fold.
+ * With D = 128, 2 <= H / H_kv <= 16 and page_size >= 8 the query heads of a
+ * group share one tensor-core product per 128-key tile (keys in M, the
+ * group's heads in N): each KV row is read once for the whole group.  Chunk
+ * boundaries that fall inside a 128-key tile make both neighbouring chunks
+ * read that tile, so fewer chunks mean less traffic.  Other shapes fold on
+ * the CUDA cores, one query head per warp.
  */
 int fa_decode_paged_splitkv(const void* q, const void* k_pages, const void* v_pages,
                             const int* block_table, const int* seqlens, int num_pages,

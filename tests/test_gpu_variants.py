@@ -88,6 +88,60 @@ def test_paged_decode(fa, H, Hkv, page, S, D):
     assert fa.fa_check_device_status() == fa.FA_OK
 
 
+@pytest.mark.parametrize("H,Hkv,page,S", [(8, 4, 8, 3), (8, 2, 16, 7), (32, 8, 64, 16),
+                                          (16, 2, 128, 5), (16, 1, 256, 2), (12, 3, 32, 1)])
+def test_paged_decode_tensor_core_groups(fa, H, Hkv, page, S):
+    """D = 128 with 2..16 query heads per KV head runs the tensor-core kernel:
+    chunk states against the oracle's, the combined output against decode."""
+    lens = [1, 127, 128, 129, 700, 3001]
+    D = 128
+    case = inp.paged_decode(len(lens), H, Hkv, D, page, seed=H * 3 + page + S, num_splits=S,
+                            lens=lens)
+    args = _paged_gpu(case)
+    pm, pd, po = fa.fa_decode_paged_splitkv(*args, S, case.scale)
+    torch.cuda.synchronize()
+    assert fa.fa_check_device_status() == fa.FA_OK
+    M, Dn, Oc = ora.chunk_states_paged_ref(case.q, case.k_pages, case.v_pages,
+                                           case.block_table, case.seqlens, S, case.scale)
+    full = np.isfinite(M)
+    assert (np64(pm)[~full] == -np.inf).all() and (np64(pd)[~full] == 0).all()
+    assert np.abs(np64(pm)[full] - M[full]).max() <= 1e-4 * max(1.0, np.abs(M[full]).max())
+    assert np.abs(np64(pd)[full] / Dn[full] - 1).max() <= 1e-4
+    O, L = ora.decode_paged_ref(case.q, case.k_pages, case.v_pages, case.block_table,
+                                case.seqlens, case.scale)
+    o32, lse = fa.fa_combine_states(pm, pd, po, o_dtype=torch.float32)
+    check_o_f32(np64(o32), O, "paged decode (tensor cores)")
+    check_lse(np64(lse), L)
+
+
+def test_paged_tensor_core_stale_tail_rows(fa):
+    """Rows past a sequence's end inside its last page hold NaN: they must not
+    reach the output."""
+    lens = [200, 70]
+    case = inp.paged_decode(len(lens), 8, 2, 128, 64, seed=41, num_splits=2, lens=lens)
+    kp, vp = case.k_pages.clone(), case.v_pages.clone()
+    for b, L in enumerate(lens):
+        last = int(case.block_table[b, (L - 1) // 64])
+        kp[last, L % 64:] = float("nan")
+        vp[last, L % 64:] = float("nan")
+    q, _, _, table, sl = _paged_gpu(case)
+    pm, pd, po = fa.fa_decode_paged_splitkv(q, kp.cuda(), vp.cuda(), table, sl, 2, case.scale)
+    o32, lse = fa.fa_combine_states(pm, pd, po, o_dtype=torch.float32)
+    O, L = ora.decode_paged_ref(case.q, case.k_pages, case.v_pages, case.block_table,
+                                case.seqlens, case.scale)
+    check_o_f32(np64(o32), O, "stale tail rows")
+    check_lse(np64(lse), L)
+
+
+def test_paged_tensor_core_bad_page_reported(fa):
+    case = inp.paged_decode(2, 8, 2, 128, 16, seed=43, num_splits=4, lens=[300, 90])
+    q, kp, vp, table, sl = _paged_gpu(case)
+    table[0, 3] = case.meta["pages"] + 7  # past the pool
+    fa.fa_decode_paged_splitkv(q, kp, vp, table, sl, 4, case.scale)
+    assert fa.fa_check_device_status() == fa.FA_ERR_DEVICE_BOUNDS
+    assert fa.fa_check_device_status() == fa.FA_OK
+
+
 def test_paged_identity_layout_equals_packed_decode(fa):
     """Pages laid out in order with one KV head per query head hold the same
     keys as a packed cache: the two entry points give the same bits."""
