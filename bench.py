@@ -554,7 +554,9 @@ def run_profile_case(args):
     """Only one workload, W + K launches, nothing else: the command the ncu
     captures run.  prefill = the full causal N=16384 prefill (537 MB of
     inputs); bwd = its backward (Delta, dK/dV, dQ kernels); rowstats = the
-    LayerNorm statistics of 65536 x 4096 bf16; decode = split-KV decode on the first 8 sequences of the decode
+    LayerNorm statistics of 65536 x 4096 bf16; paged = the paged GQA decode
+    (B=64, H=32 over H_kv=8, pages of 64, 4.7 GB of KV); scan = prefix
+    attention over the decode workload's caches; decode = split-KV decode on the first 8 sequences of the decode
     workload (about 2.2 GB of KV cache, larger than L2, small enough for a
     multi-pass capture)."""
     import exact_io_aware_15_gb300 as fa
@@ -574,6 +576,18 @@ def run_profile_case(args):
         grads = [torch.empty_like(c.q) for _ in range(3)]
         ws = torch.empty(P["B"] * P["H"] * P["N"], dtype=torch.float32, device="cuda")
         run = lambda: fa.fa_bwd(c.q, c.k, c.v, o, dout, lse, c.scale, True, *grads, ws)
+    elif args.profile_case == "paged":
+        pc = inp.paged_decode(64, 32, 8, 128, 64, seed=4, num_splits=4, device="cuda")
+        tab, sl = pc.block_table.cuda(), pc.seqlens.cuda()
+        run = lambda: fa.fa_combine_states(*fa.fa_decode_paged_splitkv(
+            pc.q, pc.k_pages, pc.v_pages, tab, sl, 4, pc.scale))
+    elif args.profile_case == "scan":
+        pc = inp.decode(DECODE["B"], DECODE["H"], DECODE["D"], seed=4, num_splits=DECODE["S"],
+                        device="cuda")
+        cu = pc.cu_seqlens_k.cuda()
+        po = torch.empty_like(pc.k_cache)
+        pl = torch.empty((DECODE["H"], pc.meta["T"]), dtype=torch.float32, device="cuda")
+        run = lambda: fa.fa_prefix_attention(pc.q, pc.k_cache, pc.v_cache, cu, pc.scale, po, pl)
     elif args.profile_case == "rowstats":
         x = inp.stats_rows(ROWSTATS["R"], ROWSTATS["C"], seed=11, loc=0.5, std=1.0,
                            row_spread=1.0, device="cuda")
@@ -602,7 +616,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-other-configs", action="store_true")
-    ap.add_argument("--profile-case", choices=["prefill", "decode", "bwd", "rowstats"],
+    ap.add_argument("--profile-case", choices=["prefill", "decode", "bwd", "rowstats", "paged",
+                                                        "scan"],
                     default=None)
     args = ap.parse_args(argv)
     if args.profile_case:
