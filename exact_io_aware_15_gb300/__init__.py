@@ -1,4 +1,4 @@
-"""Exact tiled attention forward for GB300 (sm_103a): Python binding.
+"""Exact tiled attention for GB300 (sm_103a): Python binding.
 
 A thin ctypes layer over the C ABI in ``include/fa_gb300.h`` (library
 ``_lib/libfa_gb300.so``, built by ``build.build()``).  Each function here has

@@ -38,6 +38,7 @@
 // returns.
 
 #include <cuda.h>
+#include <atomic>
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -663,18 +664,18 @@ static_assert(DqCfg<64>::SMEM_BYTES <= 232448, "dQ shared memory");
 
 template <int D>
 cudaError_t launch_impl(const BwdMaps& m, const BwdArgs& a, cudaStream_t stream) {
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];  // per device: attribute already set
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+  if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(DkdvCfg<D>::SMEM_BYTES));
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(fa_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(DqCfg<D>::SMEM_BYTES));
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_release);
   }
   fa_bwd_delta_kernel<D><<<static_cast<unsigned>((a.rows + 7) / 8), 256, 0, stream>>>(a);
   e = cudaGetLastError();

@@ -30,6 +30,7 @@
 // it.  Every wait is bounded.
 
 #include <cuda.h>
+#include <atomic>
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -406,15 +407,15 @@ bool decode_paged_tc_supported(int D, int G, int page_size) {
 
 cudaError_t launch_decode_paged_tc(const PagedTcMaps& maps, const PagedDecodeArgs& a, int G,
                                    cudaStream_t stream) {
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];  // per device: attribute already set
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+  if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(fa_decode_paged_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_release);
   }
   const int page_shift = __builtin_ctz(static_cast<unsigned>(a.page_size));
   dim3 grid(static_cast<unsigned>(a.S), static_cast<unsigned>(a.Hkv),

@@ -35,6 +35,7 @@
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256), O [256, 256 + D).
 
 #include <cuda.h>
+#include <atomic>
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -484,15 +485,15 @@ static cudaError_t launch_tc_impl(const TcMaps& maps, const TcFwdArgs& a, int gr
                                   cudaStream_t stream) {
   using C = TcCfg<D>;
   // The shared-memory opt-in is a per-device attribute of the function.
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];  // per device: attribute already set
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+  if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::SMEM_BYTES));
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_release);
   }
   dim3 grid(static_cast<unsigned>(grid_x * a.num_mblocks));
   fa_fwd_tc_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(maps.q, maps.k, maps.v, a);

@@ -165,7 +165,11 @@ __global__ void __launch_bounds__(256, 2) fa_prefix_scan_kernel(const ScanArgs a
     const int k0 = w0 + warp * kKeysPerWarp;  // this warp's first key
     const int nk = max(0, min(kKeysPerWarp, L - k0));
     // phase A: scores and the segment total
-    float sg[kKeysPerWarp];
+    // Dot products: each lane's partial sums of the 16 keys, reduced across
+    // the warp by halving -- at offset 16 a lane keeps 8 keys and adds its
+    // partner's partials of those, at 8 it keeps 4, ... -- so that lane l
+    // ends with the full sum of key l >> 1; then every lane takes all 16.
+    float v[kKeysPerWarp];
 #pragma unroll
     for (int i = 0; i < kKeysPerWarp; ++i) {
       float x[VPL];
@@ -173,8 +177,23 @@ __global__ void __launch_bounds__(256, 2) fa_prefix_scan_kernel(const ScanArgs a
       float s = 0.f;
 #pragma unroll
       for (int j = 0; j < VPL; ++j) s = fmaf(q[j], x[j], s);
+      v[i] = s;
+    }
 #pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    for (int w = kKeysPerWarp / 2, off = 16; w >= 1; w >>= 1, off >>= 1) {
+      const bool hi = (lane & off) != 0;
+#pragma unroll
+      for (int i = 0; i < w; ++i) {
+        const float send = hi ? v[i] : v[i + w];
+        const float keep = hi ? v[i + w] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+      }
+    }
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+    float sg[kKeysPerWarp];
+#pragma unroll
+    for (int i = 0; i < kKeysPerWarp; ++i) {
+      const float s = __shfl_sync(0xffffffffu, v[0], 2 * i);
       sg[i] = i < nk ? s * c : -INFINITY;
     }
     load_rows(kr, kp, w0 + kWindow);

@@ -1,5 +1,6 @@
 /*
- * fa_gb300.h - C ABI of the exact tiled attention forward for GB300 (sm_103a).
+ * fa_gb300.h - C ABI of exact tiled attention for GB300 (sm_103a): forward,
+ * backward, split-KV and paged decode, prefix attention and row statistics.
  *
  * What is computed.  For every query row i of every (batch, head):
  *     s_j = scale * <q_i, k_j>,     O_i = sum_j e^{s_j} v_j / sum_j e^{s_j},
