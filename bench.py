@@ -236,11 +236,11 @@ def oracle_sample_step(q, k, v, scale, head: int, rows):
     return float(sum(4.0 * D * (int(r) + 1) for r in rows))
 
 
-def cpu_sample_inputs():
-    """Two heads of the prefill workload, drawn on the CPU generator with the
-    prefill seed, as float64 (rows sampled per step)."""
+def cpu_sample_inputs(heads: int = 2):
+    """The first `heads` heads of the prefill workload, drawn on the CPU
+    generator with the prefill seed, as float64 (rows sampled per step)."""
     import numpy as np
-    c = inp.dense(1, 2, PREFILL["N"], PREFILL["D"], seed=3, causal=True, qk_std=3.0)
+    c = inp.dense(1, heads, PREFILL["N"], PREFILL["D"], seed=3, causal=True, qk_std=3.0)
     f = lambda t: t[0].to(torch.float64).numpy()
     return f(c.q), f(c.k), f(c.v), c.scale, np
 
@@ -279,20 +279,22 @@ def run_reference(args, rank, world):
 
 def cpu_baseline_leg():
     """The oracle as it stands on this host's cores, on a bounded sample
-    (about 10 s): the last 2048 query rows of 2 heads of the prefill workload."""
-    q, k, v, scale, np = cpu_sample_inputs()
+    (about 10 s): full causal attention of 10 of the prefill workload's 32
+    heads, every query row, in chunks of 2048 rows."""
+    heads = 10
+    q, k, v, scale, np = cpu_sample_inputs(heads)
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     N = PREFILL["N"]
-    rows = np.arange(N - 2048, N)
-    oracle_sample_step(q, k, v, scale, 0, rows[:32])
+    oracle_sample_step(q, k, v, scale, 0, np.arange(N - 32, N))
     t0 = time.perf_counter()
     flops = 0.0
-    for h in range(2):
-        flops += oracle_sample_step(q, k, v, scale, h, rows)
+    for h in range(heads):
+        for r0 in range(0, N, 2048):
+            flops += oracle_sample_step(q, k, v, scale, h, np.arange(r0, min(N, r0 + 2048)))
     dt = time.perf_counter() - t0
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"last {len(rows)} query rows of 2 heads, N={N} D=128 causal, float64 "
-                      f"NumPy ({dt:.1f} s)"}
+            "sample": f"all {N} query rows of {heads} of the 32 heads, N={N} D=128 causal, "
+                      f"float64 NumPy ({dt:.1f} s)"}
 
 
 # ------------------------------------------------------------------ GPU arm
