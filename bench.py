@@ -355,6 +355,20 @@ def other_configs(fa):
     out["bwd_B1_H32_N16384_D128_causal"] = {
         "tflops": 2.5 * prefill_flops(1, 32, 16384, 128) / (ms * 1e-3) / 1e12, "ms": ms}
     del cb, dout, ob, lb, gq, gk, gv, ws
+    # backward over the packed varlen workload (65536 tokens, H=16, D=128)
+    c5 = inp.config5(128, device="cuda")
+    cu = c5.cu_seqlens.cuda()
+    o5, l5 = fa.fa_fwd_varlen(c5.q, c5.k, c5.v, cu, c5.max_seqlen, c5.scale, True)
+    d5 = inp.output_grad(tuple(c5.q.shape), seed=7, device="cuda")
+    g5 = [torch.empty_like(c5.q) for _ in range(3)]
+    w5 = torch.empty(fa.fa_bwd_workspace_bytes(1, 16, c5.q.shape[0]) // 4, dtype=torch.float32,
+                     device="cuda")
+    ms = _time_launches(lambda: fa.fa_bwd_varlen(c5.q, c5.k, c5.v, o5, d5, l5, cu, c5.max_seqlen,
+                                                 c5.scale, True, *g5, w5), 10)
+    vf = sum(2.0 * 16 * L * L * 128 for L in c5.meta["lens"])
+    out["bwd_varlen_T65536_H16_D128_causal"] = {"tflops": 2.5 * vf / (ms * 1e-3) / 1e12,
+                                                "ms": ms}
+    del c5, o5, l5, d5, g5, w5
     # Welford row statistics: LayerNorm statistics of 4 x 16384 tokens at
     # hidden size 4096 (bf16, 512 MiB, larger than L2), and the split-K pair
     # on 64 rows of 2^22 fp32 values in 128 chunks

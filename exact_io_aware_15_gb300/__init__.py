@@ -49,6 +49,8 @@ SIGNATURES = {
     "fa_row_stats_partials": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P]),
     "fa_row_stats_combine": (_I, [_P, _P, _P, _I, _I, _F, _P, _P, _P, _P]),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_bwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F,
+                           _I, _P]),
     "fa_decode_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
     "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
     "fa_combine_states": (_I, [_P, _P, _P, _I, _I, _I, _P, _I, _P, _P]),
@@ -295,6 +297,34 @@ def fa_row_stats_combine(part_n, part_mu, part_m2, eps=0.0):
     return tuple(out)
 
 
+def fa_bwd_varlen(q, k, v, o, do, lse, cu_seqlens, max_seqlen, scale=None, causal=True,
+                  dq=None, dk=None, dv=None, workspace=None):
+    """Backward over packed sequences (fa_bwd_varlen): q, k, v, o, do
+    [T, H, D] bf16, lse [H, T] fp32 from fa_fwd_varlen, cu_seqlens int32
+    [num_seqs + 1] on the device.  Returns dq, dk, dv [T, H, D] bf16."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
+        _need(t, n, torch.bfloat16, 3)
+        if t.shape != q.shape:
+            raise ValueError(f"{n} must have the shape of q [T, H, D]")
+    T, H, D = q.shape
+    _need(lse, "lse", torch.float32, 2)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    if tuple(lse.shape) != (H, T):
+        raise ValueError("lse must be [H, T]")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty(max(1, fa_bwd_workspace_bytes(1, H, T) // 4),
+                                dtype=torch.float32, device=q.device)
+    rc = load_library().fa_bwd_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+        _ptr(workspace), _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, int(max_seqlen), H, D,
+        _scale(scale, D), int(bool(causal)), _stream(q))
+    _check(rc, "fa_bwd_varlen")
+    return dq, dk, dv
+
+
 def fa_fwd_f32(q, k, v, scale=None, causal=False, o=None, lse=None):
     """Dense fp32 forward on the CUDA cores (fa_fwd_f32)."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
@@ -478,6 +508,7 @@ def decode(q, k_cache, v_cache, cu_seqlens_k, num_splits=16, scale=None,
 
 __all__ = [
     "fa_fwd", "fa_fwd_f32", "fa_fwd_ex", "fa_fwd_window", "fa_fwd_varlen", "fa_bwd",
+    "fa_bwd_varlen",
     "fa_bwd_workspace_bytes", "fa_decode_workspace_bytes", "fa_row_stats",
     "fa_row_stats_workspace_bytes", "fa_row_stats_partials", "fa_row_stats_combine",
     "fa_prefix_attention",

@@ -143,6 +143,56 @@ __device__ __forceinline__ void tile_of(int nt, int BH, int& bh, int& rank) {
   bh = g * 4 + rr % gsize;
 }
 
+// Where one (sequence, head) of the problem lives.  Dense: [B, H, N, D]
+// tensors, LSE / Delta [B, H, N].  Varlen: packed [T, H, D] tensors,
+// LSE / Delta [H, T], sequence s owning tokens [cu[s], cu[s+1]).
+struct SeqView {
+  bool ok;        // offsets passed the bounds check
+  int L;          // positions of the sequence
+  int h, tok0;    // varlen: head and first token
+  size_t lse0;    // index of position 0 in LSE / Delta
+  size_t row0;    // row of position 0 in the [., D] tensors
+  size_t rstep;   // rows between consecutive positions
+};
+
+template <bool VAR>
+__device__ __forceinline__ SeqView seq_of(const BwdArgs& a, int bh) {
+  SeqView v;
+  if constexpr (VAR) {
+    const int seq = bh / a.H;
+    v.h = bh % a.H;
+    const int b0 = __ldg(a.cu_seqlens + seq), b1 = __ldg(a.cu_seqlens + seq + 1);
+    v.ok = b0 >= 0 && b1 >= b0 && b1 <= a.total_tokens && b1 - b0 <= a.max_seqlen;
+    v.L = v.ok ? b1 - b0 : 0;
+    v.tok0 = v.ok ? b0 : 0;
+    v.lse0 = static_cast<size_t>(v.h) * a.total_tokens + v.tok0;
+    v.row0 = static_cast<size_t>(v.tok0) * a.H + v.h;
+    v.rstep = static_cast<size_t>(a.H);
+  } else {
+    v.ok = true;
+    v.L = a.N;
+    v.h = 0;
+    v.tok0 = 0;
+    v.lse0 = static_cast<size_t>(bh) * a.N;
+    v.row0 = v.lse0;
+    v.rstep = 1;
+  }
+  return v;
+}
+
+// TMA box origin of 128 rows from sequence position `pos`, column half c:
+// dense maps are (D, N, B*H), varlen maps (D, H, T).
+template <bool VAR>
+__device__ __forceinline__ void tile_load(const CUtensorMap* map, uint32_t dst, uint32_t bar,
+                                          int halves, const SeqView& v, int bh, int pos) {
+  for (int c = 0; c < halves; ++c) {
+    if constexpr (VAR)
+      tma_load_3d(dst + c * kHalfBytes, map, bar, c * 64, v.h, v.tok0 + pos);
+    else
+      tma_load_3d(dst + c * kHalfBytes, map, bar, c * 64, pos, bh);
+  }
+}
+
 // ============================================================ dK / dV
 
 template <int D>
@@ -171,7 +221,10 @@ struct DkdvCfg {
 };
 
 // One CTA per (head, 128-key tile n), in tile_of's order.
-template <int D>
+// VAR: packed sequences (rows past a sequence's end belong to the next one
+// and are masked); dense tensors instead zero-fill rows past N, whose
+// contributions vanish without a mask.
+template <int D, bool VAR>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -187,12 +240,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int N = args.N;
   const int nt = args.num_tiles;
-  int bh, n;  // key tile n sees query tiles n..nt-1 under causal masking
+  int bh, n;  // key tile n sees query tiles n..ntl-1 under causal masking
   tile_of(nt, args.BH, bh, n);
+  const SeqView sv = seq_of<VAR>(args, bh);
+  if (!sv.ok) {
+    if (threadIdx.x == 0) atomicOr(args.status, kStatusBounds);
+    return;
+  }
+  const int ntl = (sv.L + kBM - 1) / kBM;  // tiles of this sequence
+  if (n >= ntl) return;
   const int t_begin = args.causal ? n : 0;  // first query tile that sees key tile n
-  const int count = nt - t_begin;
+  const int count = ntl - t_begin;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_A_FULL), 1);
@@ -222,9 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ============================ TMA producer ============================
     if (lane == 0) {
       auto load = [&](const CUtensorMap* map, uint32_t dst, uint32_t fb, int row0) {
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(dst + c * kHalfBytes, map, fb, c * 64, row0, bh);
+        tile_load<VAR>(map, dst, fb, D / 64, sv, bh, row0);
       };
       const uint32_t ab = bar(C::B_A_FULL);
       mbar_arrive_expect_tx(ab, 2 * C::TILE);
@@ -295,7 +352,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quarter * 32 + lane;  // TMEM lane = key row of the tile
     const int kj = n * kBM + r;         // key position
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const size_t head = static_cast<size_t>(bh) * N;
     // this warp's copy of the query tile's -LSE2 and -Delta
     float* vec = reinterpret_cast<float*>(smem + C::OFF_VEC) + (warp - 2) * 256;
     const uint32_t s_t = tmem + lane_off + C::TM_S;
@@ -308,14 +364,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = 0; u < 4; ++u) {
         const int i = lane + 32 * u;
         const int ig = tg * kBM + i;
-        vec[i] = ig < N ? -args.lse[head + ig] * kLog2e : 0.f;
-        vec[128 + i] = ig < N ? -args.delta[head + ig] : 0.f;
+        vec[i] = ig < sv.L ? -args.lse[sv.lse0 + ig] * kLog2e : 0.f;
+        vec[128 + i] = ig < sv.L ? -args.delta[sv.lse0 + ig] : 0.f;
       }
       __syncwarp();
-      // Query columns past N and key rows past N read zero-filled tiles: P
-      // there meets dO = 0 and Delta = 0 or a key row that is not stored, so
-      // only the causal diagonal tile needs a mask.
+      // Masked: the causal diagonal tile, and query columns past the
+      // sequence end (next sequence's rows when packed; key rows past the
+      // end are not stored).
       const bool diag = args.causal && tg == n;
+      const int qlim = VAR ? sv.L - tg * kBM : kBM;  // visible query columns: col < qlim
+      const bool masked = diag || qlim < kBM;
+      const int clo = diag ? r : 0;  // visible query columns: clo <= col < qlim
       const bool w1 = mbar_wait(bar(C::B_S_FULL), t & 1, abort_flag, args.status);
       if (__any_sync(0xffffffffu, !w1)) {
         ok = false;
@@ -335,7 +394,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 x = __ffma2_rn(
               make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), cc, nl);
           float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
-          if (diag) {  // query tg*128+col sees key n*128+r iff col >= r
+          if constexpr (VAR) {
+            if (masked) {
+              if (col < clo || col >= qlim) p0 = 0.f;
+              if (col + 1 < clo || col + 1 >= qlim) p1 = 0.f;
+            }
+          } else if (diag) {  // query tg*128+col sees key n*128+r iff col >= r
             if (col < r) p0 = 0.f;
             if (col + 1 < r) p1 = 0.f;
           }
@@ -381,9 +445,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool w3 = mbar_wait(bar(C::B_ACC_DONE), 0, abort_flag, args.status);
       if (!__any_sync(0xffffffffu, !w3)) {
         tc_fence_after();
-        const bool store = kj < N;
-        store_row<D>(tmem + lane_off + C::TM_DV, args.dv, head + kj, store, 1.f);
-        store_row<D>(tmem + lane_off + C::TM_DK, args.dk, head + kj, store, args.scale);
+        const bool store = kj < sv.L;
+        const size_t row = sv.row0 + static_cast<size_t>(kj) * sv.rstep;
+        store_row<D>(tmem + lane_off + C::TM_DV, args.dv, row, store, 1.f);
+        store_row<D>(tmem + lane_off + C::TM_DK, args.dk, row, store, args.scale);
       }
     }
     tc_fence_before();
@@ -426,7 +491,7 @@ struct DqCfg {
 };
 
 // One CTA per (head, 128-query tile m), in tile_of's order.
-template <int D>
+template <int D, bool VAR>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
@@ -442,12 +507,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int N = args.N;
   const int nt = args.num_tiles;
   int bh, rank;  // query tile m sees key tiles 0..m under causal masking
   tile_of(nt, args.BH, bh, rank);
   const int m = nt - 1 - rank;
-  const int count = args.causal ? m + 1 : nt;  // key tiles 0 .. count-1
+  const SeqView sv = seq_of<VAR>(args, bh);
+  if (!sv.ok) {
+    if (threadIdx.x == 0) atomicOr(args.status, kStatusBounds);
+    return;
+  }
+  const int ntl = (sv.L + kBM - 1) / kBM;  // tiles of this sequence
+  if (m >= ntl) return;
+  const int count = args.causal ? m + 1 : ntl;  // key tiles 0 .. count-1
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_A_FULL), 1);
@@ -481,9 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ============================ TMA producer ============================
     if (lane == 0) {
       auto load = [&](const CUtensorMap* map, uint32_t dst, uint32_t fb, int row0) {
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(dst + c * kHalfBytes, map, fb, c * 64, row0, bh);
+        tile_load<VAR>(map, dst, fb, D / 64, sv, bh, row0);
       };
       const uint32_t ab = bar(C::B_A_FULL);
       mbar_arrive_expect_tx(ab, 2 * C::TILE);
@@ -557,18 +626,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quarter * 32 + lane;  // TMEM lane = query row of the tile
     const int qi = m * kBM + r;         // query position
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const size_t head = static_cast<size_t>(bh) * N;
-    const float nl2 = qi < N ? -args.lse[head + qi] * kLog2e : 0.f;
-    const float ndl = qi < N ? -args.delta[head + qi] : 0.f;
+    const float nl2 = qi < sv.L ? -args.lse[sv.lse0 + qi] * kLog2e : 0.f;
+    const float ndl = qi < sv.L ? -args.delta[sv.lse0 + qi] : 0.f;
     const float2 cc = make_float2(args.scale_log2, args.scale_log2);
     const float2 nl = make_float2(nl2, nl2), nd = make_float2(ndl, ndl);
     const uint32_t dp_t = tmem + lane_off + C::TM_DP;
     bool ok = true;
     for (int t = 0; t < count; ++t) {
       const uint32_t s_t = tmem + lane_off + C::TM_S0 + 128u * (t & 1);
-      // Key columns past N read zero-filled K and V rows, and their dS
-      // multiplies a zero K row: only the causal diagonal tile needs a mask.
+      // Masked: the causal diagonal tile, and key columns past the sequence
+      // end (next sequence's rows when packed).
       const bool diag = args.causal && t == m;
+      const int klim = VAR ? sv.L - t * kBM : kBM;  // visible key columns: col < klim
+      const bool masked = diag || klim < kBM;
+      const int khi = diag ? min(klim, r + 1) : klim;  // visible key columns: col < khi
       const bool w1 =
           mbar_wait(bar(C::B_S_FULL + (t & 1)), (t >> 1) & 1, abort_flag, args.status);
       if (__any_sync(0xffffffffu, !w1)) {
@@ -587,7 +658,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 x = __ffma2_rn(
               make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), cc, nl);
           float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
-          if (diag) {  // key t*128+col is visible iff col <= r
+          if constexpr (VAR) {
+            if (masked) {
+              if (col >= khi) p0 = 0.f;
+              if (col + 1 >= khi) p1 = 0.f;
+            }
+          } else if (diag) {  // key t*128+col is visible iff col <= r
             if (col > r) p0 = 0.f;
             if (col + 1 > r) p1 = 0.f;
           }
@@ -625,7 +701,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool w3 = mbar_wait(bar(C::B_ACC_DONE), 0, abort_flag, args.status);
       if (!__any_sync(0xffffffffu, !w3)) {
         tc_fence_after();
-        store_row<D>(tmem + lane_off + C::TM_DQ, args.dq, head + qi, qi < N, args.scale);
+        store_row<D>(tmem + lane_off + C::TM_DQ, args.dq,
+                     sv.row0 + static_cast<size_t>(qi) * sv.rstep, qi < sv.L, args.scale);
       }
     }
     tc_fence_before();
@@ -654,7 +731,12 @@ __global__ void __launch_bounds__(256) fa_bwd_delta_kernel(const BwdArgs a) {
              __uint_as_float(static_cast<uint32_t>(g[i]) << 16), s);
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-  if (lane == 0) a.delta[row] = s;
+  if (lane == 0) {
+    // dense: Delta [B, H, N] in row order; packed: row = t * H + h -> [H, T]
+    const long long idx =
+        a.cu_seqlens ? (row % a.H) * a.total_tokens + row / a.H : row;
+    a.delta[idx] = s;
+  }
 }
 
 static_assert(DkdvCfg<128>::SMEM_BYTES <= 232448, "dK/dV shared memory");
@@ -662,17 +744,18 @@ static_assert(DkdvCfg<64>::SMEM_BYTES <= 232448, "dK/dV shared memory");
 static_assert(DqCfg<128>::SMEM_BYTES <= 232448, "dQ shared memory");
 static_assert(DqCfg<64>::SMEM_BYTES <= 232448, "dQ shared memory");
 
-template <int D>
+template <int D, bool VAR>
 cudaError_t launch_impl(const BwdMaps& m, const BwdArgs& a, cudaStream_t stream) {
   static std::atomic<bool> attr_set[64];  // per device: attribute already set
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D, VAR>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(DkdvCfg<D>::SMEM_BYTES));
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(fa_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(fa_bwd_dq_kernel<D, VAR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(DqCfg<D>::SMEM_BYTES));
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_release);
@@ -681,11 +764,11 @@ cudaError_t launch_impl(const BwdMaps& m, const BwdArgs& a, cudaStream_t stream)
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const unsigned blocks = static_cast<unsigned>(static_cast<long long>(a.BH) * a.num_tiles);
-  fa_bwd_dkdv_kernel<D>
+  fa_bwd_dkdv_kernel<D, VAR>
       <<<blocks, kThreads, DkdvCfg<D>::SMEM_BYTES, stream>>>(m.q, m.k, m.v, m.dout, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  fa_bwd_dq_kernel<D>
+  fa_bwd_dq_kernel<D, VAR>
       <<<blocks, kThreads, DqCfg<D>::SMEM_BYTES, stream>>>(m.q, m.k, m.v, m.dout, a);
   return cudaGetLastError();
 }
@@ -693,8 +776,10 @@ cudaError_t launch_impl(const BwdMaps& m, const BwdArgs& a, cudaStream_t stream)
 }  // namespace
 
 cudaError_t launch_bwd(const BwdMaps& maps, const BwdArgs& a, int D, cudaStream_t stream) {
-  if (D == 128) return launch_impl<128>(maps, a, stream);
-  return launch_impl<64>(maps, a, stream);
+  const bool var = a.cu_seqlens != nullptr;
+  if (D == 128) return var ? launch_impl<128, true>(maps, a, stream)
+                           : launch_impl<128, false>(maps, a, stream);
+  return var ? launch_impl<64, true>(maps, a, stream) : launch_impl<64, false>(maps, a, stream);
 }
 
 }  // namespace fa

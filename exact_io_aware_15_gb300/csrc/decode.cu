@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(256) fa_decode_paged_kernel(const PagedDecodeA
   const int h = blockIdx.y * 8 + warp;
   const int b = blockIdx.z;
   const int L = __ldg(a.seqlens + b);
-  if (L < 0 || L > a.max_blocks * a.page_size) {
+  if (L < 0 || static_cast<long long>(L) > static_cast<long long>(a.max_blocks) * a.page_size) {
     if (threadIdx.x == 0) atomicOr(a.status, kStatusBounds);
     return;
   }

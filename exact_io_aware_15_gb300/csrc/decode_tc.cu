@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(192, 1)
   const int P = 1 << page_shift;
 
   int L = __ldg(a.seqlens + b);
-  if (L < 0 || L > a.max_blocks * P) {
+  if (L < 0 || static_cast<long long>(L) > static_cast<long long>(a.max_blocks) * P) {
     if (threadIdx.x == 0) atomicOr(a.status, kStatusBounds);
     L = 0;
   }

@@ -264,6 +264,57 @@ int row_stats(const void* x, int R, int C, int dtype, int S, float eps, float* p
   return launched(fa::launch_row_stats(a, static_cast<cudaStream_t>(stream)));
 }
 
+int bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dout,
+               const float* lse, void* dq, void* dk, void* dv, float* workspace,
+               const int* cu_seqlens, int num_seqs, int total_tokens, int max_seqlen, int H,
+               int D, float scale, int causal, void* stream) {
+  if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0 || H < 0 || (D != 64 && D != 128) ||
+      !good_scale(scale))
+    return FA_ERR_INVALID_ARG;
+  if (num_seqs == 0 || H == 0 || total_tokens == 0) return FA_OK;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned4(lse) ||
+      !aligned4(workspace) || !aligned4(cu_seqlens))
+    return FA_ERR_INVALID_ARG;
+  const long long BH = static_cast<long long>(num_seqs) * H;
+  const long long tiles = (static_cast<long long>(max_seqlen) + 127) / 128;
+  if (max_seqlen < 1 || BH * tiles > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  unsigned int* status = nullptr;
+  int rc = current_device(&status);
+  if (rc != FA_OK) return rc;
+  rc = get_encoder();
+  if (rc != FA_OK) return rc;
+  fa::BwdMaps maps;
+  const uint64_t rs = static_cast<uint64_t>(D) * 2u;
+  const uint64_t ts = rs * static_cast<uint64_t>(H);
+  if (encode_map(&maps.q, q, D, H, total_tokens, rs, ts, 1u, 128u) != FA_OK ||
+      encode_map(&maps.k, k, D, H, total_tokens, rs, ts, 1u, 128u) != FA_OK ||
+      encode_map(&maps.v, v, D, H, total_tokens, rs, ts, 1u, 128u) != FA_OK ||
+      encode_map(&maps.dout, dout, D, H, total_tokens, rs, ts, 1u, 128u) != FA_OK)
+    return FA_ERR_DRIVER;
+  fa::BwdArgs a{};
+  a.BH = static_cast<int>(BH);
+  a.N = 0;
+  a.num_tiles = static_cast<int>(tiles);
+  a.causal = causal ? 1 : 0;
+  a.rows = static_cast<long long>(total_tokens) * H;
+  a.scale = scale;
+  a.scale_log2 = scale_log2(scale);
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  a.delta = workspace;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.status = status;
+  a.cu_seqlens = cu_seqlens;
+  a.total_tokens = total_tokens;
+  a.H = H;
+  a.max_seqlen = max_seqlen;
+  return launched(fa::launch_bwd(maps, a, D, static_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 
 int fa::checked_current_device(unsigned int** status) { return current_device(status); }
@@ -355,6 +406,14 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            int N, int D, float scale, int causal, void* stream) {
   return bwd_bf16(q, k, v, o, dout, lse, dq, dk, dv, workspace, B, H, N, D, scale, causal,
                   stream);
+}
+
+int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                  const float* lse, void* dq, void* dk, void* dv, float* workspace,
+                  const int* cu_seqlens, int num_seqs, int total_tokens, int max_seqlen, int H,
+                  int D, float scale, int causal, void* stream) {
+  return bwd_varlen(q, k, v, o, dout, lse, dq, dk, dv, workspace, cu_seqlens, num_seqs,
+                    total_tokens, max_seqlen, H, D, scale, causal, stream);
 }
 
 size_t fa_decode_workspace_bytes(int B, int H, int D, int num_splits) {

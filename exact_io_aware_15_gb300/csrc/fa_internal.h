@@ -102,6 +102,12 @@ struct BwdArgs {
   void* dk;
   void* dv;
   unsigned int* status;
+  // packed sequences (NULL cu_seqlens: dense [B, H, N, D]); BH is then
+  // num_seqs * H and num_tiles covers max_seqlen
+  const int* cu_seqlens;
+  int total_tokens;
+  int H;
+  int max_seqlen;
 };
 
 struct BwdMaps {

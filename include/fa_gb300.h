@@ -142,6 +142,24 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            int B, int H, int N, int D, float scale, int causal, void* stream);
 
 /*
+ * Backward of the variable-length forward (fa_fwd_varlen) over packed
+ * sequences, by the same recomputation.
+ *   q, k, v, o, dout : bf16 [total_tokens, H, D]; sequence s owns tokens
+ *                      [cu_seqlens[s], cu_seqlens[s+1])
+ *   lse              : f32 [H, total_tokens], as fa_fwd_varlen wrote it
+ *   dq, dk, dv       : bf16 [total_tokens, H, D] (written)
+ *   workspace        : f32, fa_bwd_workspace_bytes(1, H, total_tokens) bytes
+ *   cu_seqlens       : int32 [num_seqs + 1] DEVICE array; max_seqlen >= every
+ *                      length (sizes the grid).  Offsets that fail the device's
+ *                      bounds check are reported as FA_ERR_DEVICE_BOUNDS.
+ * Positions restart at 0 in every sequence; tiles never mix sequences.
+ */
+int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                  const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                  float* workspace, const int* cu_seqlens, int num_seqs, int total_tokens,
+                  int max_seqlen, int H, int D, float scale, int causal, void* stream);
+
+/*
  * Row statistics as a monoid reduction: per row of a [R, C] matrix, the
  * Welford state (n, mu, M2) of "Learning FlashAttention the Hard Way -
  * Part 1", section "The Same Move: Welford's Variance" (a sample injects as

@@ -516,3 +516,23 @@ def prefix_attention_ref(q, k_cache, v_cache, cu_seqlens_k, scale, batch=None, h
                 O[a + i, h] = (w @ vc[a:a + i + 1, h]) / w.sum()
                 LSE[h, a + i] = m + math.log(w.sum())
     return O, LSE
+
+
+def attention_bwd_varlen_ref(q, k, v, do, cu_seqlens, scale, causal):
+    """Backward over packed sequences: q, k, v, do [T, H, D]; sequence s owns
+    tokens [cu[s], cu[s+1]).  Every (sequence, head) is an independent head
+    of attention_bwd_head_ref.  Returns dq, dk, dv [T, H, D] and Delta [H, T]
+    in float64."""
+    q, k, v, do = to_f64(q), to_f64(k), to_f64(v), to_f64(do)
+    cu = [int(x) for x in np.asarray(cu_seqlens).tolist()]
+    T, H, D = q.shape
+    dq, dk, dv = (np.zeros((T, H, D)) for _ in range(3))
+    delta = np.zeros((H, T))
+    for s in range(len(cu) - 1):
+        a, e = cu[s], cu[s + 1]
+        if e == a:
+            continue
+        for h in range(H):
+            g = attention_bwd_head_ref(q[a:e, h], k[a:e, h], v[a:e, h], do[a:e, h], scale, causal)
+            dq[a:e, h], dk[a:e, h], dv[a:e, h], delta[h, a:e] = g
+    return dq, dk, dv, delta

@@ -129,3 +129,56 @@ def test_bwd_invalid_args(fa):
     assert lib.fa_bwd(None, None, None, None, None, None, None, None, None, None,
                       1, 1, 0, 128, 0.1, 1, s) == fa.FA_OK
     assert lib.fa_bwd_workspace_bytes(2, 3, 5) == 2 * 3 * 5 * 4
+
+
+# --- packed sequences -------------------------------------------------------------
+
+def _varlen_run(fa, case, do, causal):
+    cu = case.cu_seqlens.cuda()
+    q, k, v = case.q.cuda(), case.k.cuda(), case.v.cuda()
+    o, lse = fa.fa_fwd_varlen(q, k, v, cu, case.max_seqlen, case.scale, causal)
+    g = fa.fa_bwd_varlen(q, k, v, o, do.cuda(), lse, cu, case.max_seqlen, case.scale, causal)
+    torch.cuda.synchronize()
+    assert fa.fa_check_device_status() == fa.FA_OK
+    return g
+
+
+@pytest.mark.parametrize("D,causal", [(64, True), (128, True), (128, False)])
+def test_bwd_varlen(fa, D, causal):
+    """Sequences of 1, 100, 128, 129 and 300 tokens packed together: every
+    tile boundary case, rows of the next sequence inside tail tiles."""
+    lens = [1, 100, 128, 129, 300]
+    case = inp.varlen(lens, H=2, D=D, seed=970 + D, causal=causal)
+    do = inp.output_grad(tuple(case.q.shape), seed=971)
+    dq, dk, dv = _varlen_run(fa, case, do, causal)
+    rq, rk, rv, _ = ora.attention_bwd_varlen_ref(case.q, case.k, case.v, do, case.cu_seqlens,
+                                                 case.scale, causal)
+    check_grad(np64(dq), rq, f"varlen dq D={D}")
+    check_grad(np64(dk), rk, f"varlen dk D={D}")
+    check_grad(np64(dv), rv, f"varlen dv D={D}")
+
+
+def test_bwd_varlen_one_sequence_equals_dense(fa):
+    """One packed sequence runs the same tiles in the same order as the dense
+    backward: the gradients agree bit for bit."""
+    N, H, D = 333, 2, 128
+    case = inp.varlen([N], H=H, D=D, seed=975, causal=True)
+    do = inp.output_grad((N, H, D), seed=976)
+    a = _varlen_run(fa, case, do, True)
+    dense = lambda t: t.permute(1, 0, 2).unsqueeze(0).contiguous().cuda()
+    q, k, v = dense(case.q), dense(case.k), dense(case.v)
+    o, lse = fa.fa_fwd(q, k, v, case.scale, True)
+    b = fa.fa_bwd(q, k, v, o, dense(do), lse, case.scale, True)
+    for x, y in zip(a, b):
+        assert torch.equal(x.permute(1, 0, 2).unsqueeze(0), y)
+
+
+def test_bwd_varlen_bad_offsets_reported(fa):
+    case = inp.varlen([50, 70], H=2, D=64, seed=977, causal=True)
+    q, k, v = case.q.cuda(), case.k.cuda(), case.v.cuda()
+    cu = case.cu_seqlens.cuda()
+    o, lse = fa.fa_fwd_varlen(q, k, v, cu, case.max_seqlen, case.scale, True)
+    bad = torch.tensor([0, 50, 400], dtype=torch.int32, device="cuda")  # past T = 120
+    fa.fa_bwd_varlen(q, k, v, o, torch.zeros_like(q), lse, bad, 400, case.scale, True)
+    assert fa.fa_check_device_status() == fa.FA_ERR_DEVICE_BOUNDS
+    assert fa.fa_check_device_status() == fa.FA_OK

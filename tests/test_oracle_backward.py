@@ -86,3 +86,27 @@ def test_sampled_equals_full(causal):
     np.testing.assert_allclose(sq, dq[rows], rtol=1e-11, atol=1e-13)
     np.testing.assert_allclose(sk, dk[cols], rtol=1e-11, atol=1e-13)
     np.testing.assert_allclose(sv, dv[cols], rtol=1e-11, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_backward_is_per_sequence(causal):
+    """One packed sequence equals the dense backward of that sequence; the
+    gradients of a sequence do not depend on its neighbours."""
+    rng = np.random.default_rng(30 + causal)
+    lens = [7, 1, 12]
+    T, H, D = sum(lens), 2, 4
+    q, k, v, do = (rng.standard_normal((T, H, D)) for _ in range(4))
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    dq, dk, dv, delta = ora.attention_bwd_varlen_ref(q, k, v, do, cu, 0.5, causal)
+    a, e = cu[2], cu[3]
+    sl = lambda x: x[a:e].transpose(1, 0, 2)[None]
+    rq, rk, rv, rd = ora.attention_bwd_ref(sl(q), sl(k), sl(v), sl(do), 0.5, causal)
+    np.testing.assert_allclose(dq[a:e].transpose(1, 0, 2), rq[0], rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(dk[a:e].transpose(1, 0, 2), rk[0], rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(dv[a:e].transpose(1, 0, 2), rv[0], rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(delta[:, a:e], rd[0], rtol=1e-13, atol=1e-14)
+    q2 = q.copy()
+    q2[:cu[2]] = rng.standard_normal((cu[2], H, D))  # change the other sequences
+    g2 = ora.attention_bwd_varlen_ref(q2, k, v, do, cu, 0.5, causal)
+    np.testing.assert_array_equal(g2[0][a:e], dq[a:e])
+    np.testing.assert_array_equal(g2[1][a:e], dk[a:e])
