@@ -18,8 +18,8 @@
 //      earlier windows (+) the totals of the warps to its left, in index
 //      order; then it rescans its 16 keys from registers, emitting
 //      O_i = o / d and LSE_i = ln2 (m + log2 d) for every key.
-// The carry then absorbs all 8 totals (every warp computes the same value
-// in the same order) and the next window starts.  K and V are read from HBM
+// The carry of the next window is warp 7's running state after its rescan
+// (the carry (+) every key of the window), shared through shared memory.  K and V are read from HBM
 // once; the depth per window is that of a two-level scan (16 sequential
 // steps per warp, 8 totals across warps).
 
@@ -101,6 +101,8 @@ __global__ void __launch_bounds__(256, 2) fa_prefix_scan_kernel(const ScanArgs a
   constexpr int VPL = D / 32;
   __shared__ float tot_m[8], tot_d[8];
   __shared__ __align__(16) float tot_o[8][D];
+  __shared__ float car_m, car_d;  // carry of the windows so far (written by warp 7)
+  __shared__ __align__(16) float car_o[D];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = a.H;
   const int h = static_cast<int>(blockIdx.x) % H;
@@ -254,10 +256,21 @@ __global__ void __launch_bounds__(256, 2) fa_prefix_scan_kernel(const ScanArgs a
       }
     }
     load_rows(vr, vp, w0 + kWindow);
-    // carry of this window: every warp folds all 8 totals in the same order
-#pragma unroll 1
-    for (int w = 0; w < 8; ++w) merge_into<VPL>(cm, cd, co, tot_m[w], tot_d[w], &tot_o[w][lane * VPL]);
+    // The carry of the next window is warp 7's running state after its
+    // rescan: the carry in (+) every key of this window.
+    if (warp == 7) {
+      if (lane == 0) {
+        car_m = m;
+        car_d = d;
+      }
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) car_o[lane * VPL + j] = o[j];
+    }
     __syncthreads();  // the totals are rewritten by the next window
+    cm = car_m;
+    cd = car_d;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) co[j] = car_o[lane * VPL + j];
   }
 }
 
