@@ -326,7 +326,28 @@ def other_configs(fa):
     c2 = inp.config2(device="cuda")
     ms = _time_launches(lambda: fa.fa_fwd(c2.q, c2.k, c2.v, c2.scale, True), 20)
     out["dense_B4_H16_N2048_D128_causal"] = {
-        "tflops": prefill_flops(4, 16, 2048, 128) / (ms * 1e-3) / 1e12, "ms": ms}
+        "tflops": prefill_flops(4, 16, 2048, 128) / (ms * 1e-3) / 1e12, "ms": ms,
+        "l2": "hot (inputs of 134 MB stay in the 129 MB L2 between launches)"}
+    # the same with L2 flushed before every launch: a 512 MB write between
+    # launches, each launch timed alone
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    st = torch.cuda.current_stream()
+    times = []
+    for it in range(23):
+        flush.fill_(float(it))
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        fa.fa_fwd(c2.q, c2.k, c2.v, c2.scale, True)
+        b.record(st)
+        b.synchronize()
+        if it >= 3:
+            times.append(a.elapsed_time(b))
+    ms_cold = sum(times) / len(times)
+    out["dense_B4_H16_N2048_D128_causal_cold_l2"] = {
+        "tflops": prefill_flops(4, 16, 2048, 128) / (ms_cold * 1e-3) / 1e12, "ms": ms_cold,
+        "l2": "flushed by a 512 MB write before each launch"}
+    del flush
     for D in (64, 128):
         c5 = inp.config5(D, device="cuda")
         cu = c5.cu_seqlens.cuda()
