@@ -422,6 +422,17 @@ def other_configs(fa):
     out["prefix_scan_B64_H32_D128_L1024-32768"] = {"gbs": sb / (ms * 1e-3) / 1e9, "ms": ms,
                                                    "bytes": sb}
     del pc, po, pl
+    # few long rows (B=2, H=4, 262144 keys each): every row cut into 64
+    # chunks scanned at once
+    lc = inp.decode(2, 4, 128, seed=5, num_splits=64, lens=[262144, 262144], device="cuda")
+    lcu = lc.cu_seqlens_k.cuda()
+    ms = _time_launches(lambda: fa.fa_prefix_attention_chunked(lc.q, lc.k_cache, lc.v_cache, lcu,
+                                                               64, lc.scale), 5)
+    T = lc.meta["T"]
+    lb = float(T) * 4 * 128 * 2 * 3 + float(T) * 4 * 4
+    out["prefix_scan_chunked_B2_H4_L262144_S64"] = {"gbs": lb / (ms * 1e-3) / 1e9, "ms": ms,
+                                                    "bytes": lb}
+    del lc
     # paged KV decode with grouped query heads: the decode lengths, H=32 over
     # H_kv=8, pages of 64 keys
     # (4 KV chunks per sequence: B * H_kv * 4 = 2048 CTAs of 128-key tiles)

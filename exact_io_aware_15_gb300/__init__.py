@@ -45,6 +45,8 @@ SIGNATURES = {
     "fa_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I]),
     "fa_row_stats": (_I, [_P, _I, _I, _I, _F, _P, _P, _P, _P]),
     "fa_prefix_attention": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P]),
+    "fa_prefix_attention_chunked": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P,
+                                         _P, _P, _P]),
     "fa_row_stats_workspace_bytes": (ctypes.c_size_t, [_I, _I]),
     "fa_row_stats_partials": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P]),
     "fa_row_stats_combine": (_I, [_P, _P, _P, _I, _I, _F, _P, _P, _P, _P]),
@@ -244,6 +246,32 @@ def fa_prefix_attention(q, k_cache, v_cache, cu_seqlens_k, scale=None, o=None, l
                                             _ptr(cu_seqlens_k), T, B, H, D, _scale(scale, D),
                                             _ptr(o), _ptr(lse), _stream(q))
     _check(rc, "fa_prefix_attention")
+    return o, lse
+
+
+def fa_prefix_attention_chunked(q, k_cache, v_cache, cu_seqlens_k, num_splits, scale=None,
+                                o=None, lse=None):
+    """Prefix attention with every row cut into num_splits chunks scanned at
+    once (fa_prefix_attention_chunked); the chunks' split-KV states go to a
+    workspace allocated here.  Returns o [T, H, D] bf16 and lse [H, T]."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 3)
+    _need(v_cache, "v_cache", torch.bfloat16, 3)
+    _need(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+    B, H, D = q.shape
+    T = k_cache.shape[0]
+    if k_cache.shape[1:] != (H, D) or v_cache.shape != k_cache.shape or \
+            cu_seqlens_k.numel() != B + 1:
+        raise ValueError("shapes: q [B, H, D], caches [T, H, D], cu_seqlens_k [B + 1]")
+    S = int(num_splits)
+    parts = [torch.empty(s, dtype=torch.float32, device=q.device)
+             for s in ((B, H, S), (B, H, S), (B, H, S, D))]
+    o = torch.empty_like(k_cache) if o is None else o
+    lse = torch.empty((H, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    rc = load_library().fa_prefix_attention_chunked(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_k), T, B, H, D, S,
+        _scale(scale, D), *(_ptr(p) for p in parts), _ptr(o), _ptr(lse), _stream(q))
+    _check(rc, "fa_prefix_attention_chunked")
     return o, lse
 
 
@@ -511,7 +539,7 @@ __all__ = [
     "fa_bwd_varlen",
     "fa_bwd_workspace_bytes", "fa_decode_workspace_bytes", "fa_row_stats",
     "fa_row_stats_workspace_bytes", "fa_row_stats_partials", "fa_row_stats_combine",
-    "fa_prefix_attention",
+    "fa_prefix_attention", "fa_prefix_attention_chunked",
     "fa_decode_splitkv", "fa_combine_states", "fa_decode_splitkv_noalloc",
     "fa_decode_paged_splitkv",
     "fa_check_device_status",

@@ -582,6 +582,16 @@ int fa_row_stats_combine(const float* part_n, const float* part_mu, const float*
 int fa_prefix_attention(const void* q, const void* k_cache, const void* v_cache,
                         const int* cu_seqlens_k, int total_kv_tokens, int B, int H, int D,
                         float scale, void* o, float* lse, void* stream) {
+  return fa_prefix_attention_chunked(q, k_cache, v_cache, cu_seqlens_k, total_kv_tokens, B, H,
+                                     D, 1, scale, nullptr, nullptr, nullptr, o, lse, stream);
+}
+
+int fa_prefix_attention_chunked(const void* q, const void* k_cache, const void* v_cache,
+                                const int* cu_seqlens_k, int total_kv_tokens, int B, int H,
+                                int D, int num_splits, float scale, float* part_m,
+                                float* part_d, float* part_o, void* o, float* lse,
+                                void* stream) {
+  if (num_splits < 1 || num_splits > 256) return FA_ERR_INVALID_ARG;
   if (B < 0 || H < 0 || total_kv_tokens < 0 || (D != 64 && D != 128) || !good_scale(scale))
     return FA_ERR_INVALID_ARG;
   if (B == 0 || H == 0) return FA_OK;
@@ -589,10 +599,31 @@ int fa_prefix_attention(const void* q, const void* k_cache, const void* v_cache,
   if (total_kv_tokens > 0 && (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
                               !aligned4(lse)))
     return FA_ERR_INVALID_ARG;
-  if (static_cast<long long>(B) * H > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H * num_splits > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  if (num_splits > 1 && (!aligned4(part_m) || !aligned4(part_d) || !aligned16(part_o) ||
+                         B > 65535 || H > 8 * 65535))
+    return FA_ERR_INVALID_ARG;
   unsigned int* status = nullptr;
   int rc = current_device(&status);
   if (rc != FA_OK) return rc;
+  if (num_splits > 1) {  // the chunks' states: the split-KV first pass
+    fa::DecodeArgs d{};
+    d.q = q;
+    d.k_cache = k_cache;
+    d.v_cache = v_cache;
+    d.cu_seqlens_k = cu_seqlens_k;
+    d.total_kv = total_kv_tokens;
+    d.B = B;
+    d.H = H;
+    d.S = num_splits;
+    d.scale_log2 = scale_log2(scale);
+    d.part_m = part_m;
+    d.part_d = part_d;
+    d.part_o = part_o;
+    d.status = status;
+    rc = launched(fa::launch_decode_splitkv(d, D, static_cast<cudaStream_t>(stream)));
+    if (rc != FA_OK) return rc;
+  }
   fa::ScanArgs a{};
   a.q = q;
   a.k_cache = k_cache;
@@ -605,6 +636,10 @@ int fa_prefix_attention(const void* q, const void* k_cache, const void* v_cache,
   a.o = o;
   a.lse = lse;
   a.status = status;
+  a.S = num_splits;
+  a.part_m = part_m;
+  a.part_d = part_d;
+  a.part_o = part_o;
   return launched(fa::launch_prefix_scan(a, D, static_cast<cudaStream_t>(stream)));
 }
 

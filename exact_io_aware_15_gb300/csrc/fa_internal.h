@@ -167,6 +167,10 @@ struct ScanArgs {
   void* o;                  // [T, H, D] bf16
   float* lse;               // [H, T]
   unsigned int* status;
+  int S;                    // chunks per row (1: one CTA walks the whole row)
+  const float* part_m;      // S > 1: the chunks' split-KV states [B, H, S] ...
+  const float* part_d;
+  const float* part_o;      // ... and [B, H, S, D]
 };
 cudaError_t launch_prefix_scan(const ScanArgs& a, int D, cudaStream_t stream);
 

@@ -19,7 +19,13 @@
 //      order; then it rescans its 16 keys from registers, emitting
 //      O_i = o / d and LSE_i = ln2 (m + log2 d) for every key.
 // The carry of the next window is warp 7's running state after its rescan
-// (the carry (+) every key of the window), shared through shared memory.  K and V are read from HBM
+// (the carry (+) every key of the window), shared through shared memory.
+//
+// Chunked rows (S > 1): the row's keys are cut into S chunks with the
+// split-KV chunking; the chunks' states come from the split-KV first pass,
+// and CTA (row, c) starts from the fold of chunks 0..c-1 and scans chunk c
+// only, so S CTAs work on one row at once (depth L/S windows + S merges
+// instead of L windows, for two reads of K and V instead of one).  K and V are read from HBM
 // once; the depth per window is that of a two-level scan (16 sequential
 // steps per warp, 8 totals across warps).
 
@@ -105,11 +111,14 @@ __global__ void __launch_bounds__(256, 2) fa_prefix_scan_kernel(const ScanArgs a
   __shared__ __align__(16) float car_o[D];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = a.H;
-  const int h = static_cast<int>(blockIdx.x) % H;
+  const int S = a.S;                                  // chunks per row
+  const int chunk = static_cast<int>(blockIdx.x) % S;
+  const int rowid = static_cast<int>(blockIdx.x) / S;
+  const int h = rowid % H;
   // Longest sequences first (ties by index), so the longest rows do not
   // start last: with up to kRankedSeqs sequences every CTA ranks the lengths
   // itself (a permutation for any values read); beyond that, index order.
-  int b = static_cast<int>(blockIdx.x) / H;
+  int b = rowid / H;
   if (a.B <= kRankedSeqs) {
     __shared__ int s_len[kRankedSeqs];
     __shared__ int s_seq;
@@ -132,6 +141,9 @@ __global__ void __launch_bounds__(256, 2) fa_prefix_scan_kernel(const ScanArgs a
     return;
   }
   const int L = k_end - k_begin;
+  // this CTA's keys: chunk `chunk` of S, [k0, k1) (the split-KV chunking)
+  const int csize = (L + S - 1) / S;
+  const int k0 = min(L, chunk * csize), k1 = min(L, (chunk + 1) * csize);
   const size_t stride = static_cast<size_t>(H) * D;
   const size_t col0 = static_cast<size_t>(h) * D + lane * VPL;
   const uint16_t* kp = static_cast<const uint16_t*>(a.k_cache) + k_begin * stride + col0;
@@ -146,26 +158,33 @@ __global__ void __launch_bounds__(256, 2) fa_prefix_scan_kernel(const ScanArgs a
     to_f32<VPL>(qc, q);
   }
   const float c = a.scale_log2;
-  // carry of all earlier windows
+  // carry of all earlier keys: the fold of the earlier chunks' states (the
+  // split-KV first pass), then of the earlier windows
   float cm = -INFINITY, cd = 0.f, co[VPL];
 #pragma unroll
   for (int j = 0; j < VPL; ++j) co[j] = 0.f;
+  if (chunk > 0) {
+    const size_t row = (static_cast<size_t>(b) * H + h) * S;
+    for (int c2 = 0; c2 < chunk; ++c2)
+      merge_into<VPL>(cm, cd, co, a.part_m[row + c2], a.part_d[row + c2],
+                      a.part_o + (row + c2) * D + lane * VPL);
+  }
 
   // This warp's rows of window w0: K is consumed by the scores and V by the
   // rescan, so the next window's K is loaded right after the scores and its
   // V right after the rescan (the loads overlap the rest of the window).
   Cols<VPL> kr[kKeysPerWarp], vr[kKeysPerWarp];
   auto load_rows = [&](Cols<VPL>(&r)[kKeysPerWarp], const uint16_t* base, int w0) {
-    const int k0 = w0 + warp * kKeysPerWarp;
+    const int kw = w0 + warp * kKeysPerWarp;
 #pragma unroll
     for (int i = 0; i < kKeysPerWarp; ++i)
-      if (k0 + i < L) r[i] = ld_cols<VPL>(base + static_cast<size_t>(k0 + i) * stride);
+      if (kw + i < k1) r[i] = ld_cols<VPL>(base + static_cast<size_t>(kw + i) * stride);
   };
-  load_rows(kr, kp, 0);
-  load_rows(vr, vp, 0);
-  for (int w0 = 0; w0 < L; w0 += kWindow) {
-    const int k0 = w0 + warp * kKeysPerWarp;  // this warp's first key
-    const int nk = max(0, min(kKeysPerWarp, L - k0));
+  load_rows(kr, kp, k0);
+  load_rows(vr, vp, k0);
+  for (int w0 = k0; w0 < k1; w0 += kWindow) {
+    const int kw = w0 + warp * kKeysPerWarp;  // this warp's first key
+    const int nk = max(0, min(kKeysPerWarp, k1 - kw));
     // phase A: scores and the segment total
     // Dot products: each lane's partial sums of the 16 keys, reduced across
     // the warp by halving -- at offset 16 a lane keeps 8 keys and adds its
@@ -246,13 +265,13 @@ __global__ void __launch_bounds__(256, 2) fa_prefix_scan_kernel(const ScanArgs a
           pk[j / 2] = pack_bf16x2(o[j] * inv, o[j + 1] * inv);
         }
         m = mn;
-        uint16_t* dst = op + static_cast<size_t>(k0 + i) * stride;
+        uint16_t* dst = op + static_cast<size_t>(kw + i) * stride;
         if constexpr (VPL == 4) {
           *reinterpret_cast<uint2*>(dst) = make_uint2(pk[0], pk[1]);
         } else {
           *reinterpret_cast<uint32_t*>(dst) = pk[0];
         }
-        if (lane == 0) lp[k0 + i] = kLn2 * (m + __log2f(d));
+        if (lane == 0) lp[kw + i] = kLn2 * (m + __log2f(d));
       }
     }
     load_rows(vr, vp, w0 + kWindow);
@@ -277,7 +296,7 @@ __global__ void __launch_bounds__(256, 2) fa_prefix_scan_kernel(const ScanArgs a
 }  // namespace
 
 cudaError_t launch_prefix_scan(const ScanArgs& a, int D, cudaStream_t stream) {
-  const unsigned blocks = static_cast<unsigned>(static_cast<long long>(a.B) * a.H);
+  const unsigned blocks = static_cast<unsigned>(static_cast<long long>(a.B) * a.H * a.S);
   if (D == 128)
     fa_prefix_scan_kernel<128><<<blocks, 256, 0, stream>>>(a);
   else

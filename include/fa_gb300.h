@@ -232,6 +232,21 @@ int fa_prefix_attention(const void* q, const void* k_cache, const void* v_cache,
                         float scale, void* o, float* lse, void* stream);
 
 /*
+ * Prefix attention with each row cut into num_splits chunks (1..256), for
+ * few long rows: a split-KV first pass (as fa_decode_splitkv, same chunking)
+ * writes every chunk's state to part_m / part_d / part_o (caller-owned,
+ * fa_decode_workspace_bytes(B, H, D, num_splits) bytes), then chunk c of a
+ * row scans its own keys starting from the fold of chunks 0..c-1, all
+ * chunks at once.  K and V are read twice.  Outputs as fa_prefix_attention;
+ * num_splits = 1 is fa_prefix_attention.
+ */
+int fa_prefix_attention_chunked(const void* q, const void* k_cache, const void* v_cache,
+                                const int* cu_seqlens_k, int total_kv_tokens, int B, int H,
+                                int D, int num_splits, float scale, float* part_m,
+                                float* part_d, float* part_o, void* o, float* lse,
+                                void* stream);
+
+/*
  * Bytes of the partial-state workspace fa_decode_splitkv writes:
  * part_m and part_d f32 [B, H, num_splits], part_o f32 [B, H, num_splits, D].
  * Returns 0 for invalid sizes.

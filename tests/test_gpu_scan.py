@@ -95,3 +95,40 @@ def test_bad_offsets_report_bounds(fa):
                            case.scale)
     assert fa.fa_check_device_status() == fa.FA_ERR_DEVICE_BOUNDS
     assert fa.fa_check_device_status() == fa.FA_OK
+
+
+@pytest.mark.parametrize("D,S", [(64, 2), (128, 7), (128, 16)])
+def test_chunked_every_position(fa, D, S):
+    """Rows cut into S chunks scanned at once from the split-KV states of the
+    earlier chunks: every position against the oracle, empty chunks incl."""
+    lens = [1, 5, 0, 127, 300, 1000]
+    case = inp.decode(len(lens), 4, D, seed=90 + S, num_splits=S, lens=lens)
+    cu = case.cu_seqlens_k.cuda()
+    o, lse = fa.fa_prefix_attention_chunked(case.q.cuda(), case.k_cache.cuda(),
+                                            case.v_cache.cuda(), cu, S, case.scale)
+    torch.cuda.synchronize()
+    assert fa.fa_check_device_status() == fa.FA_OK
+    O, L = ora.prefix_attention_ref(case.q, case.k_cache, case.v_cache, case.cu_seqlens_k,
+                                    case.scale)
+    check_o_bf16(np64(o), O, f"chunked S={S}")
+    check_lse(np64(lse), L)
+
+
+def test_chunked_long_row(fa):
+    """One long sequence (2 heads, 200000 keys) in 64 chunks: sampled positions
+    at chunk edges and inside, against the oracle."""
+    L_ = 200000
+    case = inp.decode(1, 2, 128, seed=95, num_splits=64, lens=[L_], device="cuda")
+    cu = case.cu_seqlens_k.cuda()
+    o, lse = fa.fa_prefix_attention_chunked(case.q, case.k_cache, case.v_cache, cu, 64,
+                                            case.scale)
+    torch.cuda.synchronize()
+    assert fa.fa_check_device_status() == fa.FA_OK
+    csize = -(-L_ // 64)
+    rng = np.random.default_rng(3)
+    pos = sorted(set([0, 1, csize - 1, csize, csize + 1, 31 * csize, L_ - 1]) |
+                 set(rng.integers(0, L_, 8).tolist()))
+    O, L = ora.prefix_attention_ref(case.q.cpu(), case.k_cache.cpu(), case.v_cache.cpu(),
+                                    case.cu_seqlens_k, case.scale, positions={0: pos})
+    check_o_bf16(np64(o[pos]), O[pos], "long row")
+    check_lse(np64(lse[:, pos]), L[:, pos])
