@@ -375,7 +375,14 @@ def other_configs(fa):
                                           gq, gk, gv, ws), 10)
     out["bwd_B1_H32_N16384_D128_causal"] = {
         "tflops": 2.5 * prefill_flops(1, 32, 16384, 128) / (ms * 1e-3) / 1e12, "ms": ms}
-    del cb, dout, ob, lb, gq, gk, gv, ws
+    # backward of the causal sliding window 4096 on the same tensors
+    ow, lw = fa.fa_fwd_window(cb.q, cb.k, cb.v, 4096, cb.scale)
+    ms = _time_launches(lambda: fa.fa_bwd_window(cb.q, cb.k, cb.v, ow, dout, lw, 4096, cb.scale,
+                                                 gq, gk, gv, ws), 10)
+    wf = 32 * 4.0 * 128 * sum(min(i + 1, 4096) for i in range(16384))
+    out["bwd_window4096_B1_H32_N16384_D128"] = {"tflops": 2.5 * wf / (ms * 1e-3) / 1e12,
+                                                "ms": ms}
+    del cb, dout, ob, lb, gq, gk, gv, ws, ow, lw
     # backward over the packed varlen workload (65536 tokens, H=16, D=128)
     c5 = inp.config5(128, device="cuda")
     cu = c5.cu_seqlens.cuda()

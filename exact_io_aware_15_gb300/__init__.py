@@ -51,6 +51,8 @@ SIGNATURES = {
     "fa_row_stats_partials": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P]),
     "fa_row_stats_combine": (_I, [_P, _P, _P, _I, _I, _F, _P, _P, _P, _P]),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_bwd_window": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I,
+                           _P]),
     "fa_bwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F,
                            _I, _P]),
     "fa_decode_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
@@ -325,6 +327,29 @@ def fa_row_stats_combine(part_n, part_mu, part_m2, eps=0.0):
     return tuple(out)
 
 
+def fa_bwd_window(q, k, v, o, do, lse, window, scale=None, dq=None, dk=None, dv=None,
+                  workspace=None):
+    """Backward of the causal sliding-window forward (fa_bwd_window): query i
+    sees keys i-window+1 .. i.  Same layouts as fa_bwd."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
+        _need(t, n, torch.bfloat16, 4)
+        if t.shape != q.shape:
+            raise ValueError(f"{n} must have the shape of q [B, H, N, D]")
+    B, H, N, D = q.shape
+    _need(lse, "lse", torch.float32, 3)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty(max(1, fa_bwd_workspace_bytes(B, H, N) // 4),
+                                dtype=torch.float32, device=q.device)
+    rc = load_library().fa_bwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
+                                      _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), B, H, N, D,
+                                      _scale(scale, D), int(window), _stream(q))
+    _check(rc, "fa_bwd_window")
+    return dq, dk, dv
+
+
 def fa_bwd_varlen(q, k, v, o, do, lse, cu_seqlens, max_seqlen, scale=None, causal=True,
                   dq=None, dk=None, dv=None, workspace=None):
     """Backward over packed sequences (fa_bwd_varlen): q, k, v, o, do
@@ -536,7 +561,7 @@ def decode(q, k_cache, v_cache, cu_seqlens_k, num_splits=16, scale=None,
 
 __all__ = [
     "fa_fwd", "fa_fwd_f32", "fa_fwd_ex", "fa_fwd_window", "fa_fwd_varlen", "fa_bwd",
-    "fa_bwd_varlen",
+    "fa_bwd_varlen", "fa_bwd_window",
     "fa_bwd_workspace_bytes", "fa_decode_workspace_bytes", "fa_row_stats",
     "fa_row_stats_workspace_bytes", "fa_row_stats_partials", "fa_row_stats_combine",
     "fa_prefix_attention", "fa_prefix_attention_chunked",

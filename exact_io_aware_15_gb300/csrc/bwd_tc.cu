@@ -221,10 +221,13 @@ struct DkdvCfg {
 };
 
 // One CTA per (head, 128-key tile n), in tile_of's order.
-// VAR: packed sequences (rows past a sequence's end belong to the next one
-// and are masked); dense tensors instead zero-fill rows past N, whose
-// contributions vanish without a mask.
-template <int D, bool VAR>
+// Problem modes of the tile kernels: dense tensors zero-fill rows past N,
+// whose contributions vanish without a mask; packed sequences mask the rows
+// of the next sequence in a tail tile; the causal sliding window skips the
+// tiles outside every row's window and masks the edge tiles.
+constexpr int kDense = 0, kVarlen = 1, kWindow = 2;
+
+template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -243,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nt = args.num_tiles;
   int bh, n;  // key tile n sees query tiles n..ntl-1 under causal masking
   tile_of(nt, args.BH, bh, n);
+  constexpr bool VAR = MODE == kVarlen, WIN = MODE == kWindow;
   const SeqView sv = seq_of<VAR>(args, bh);
   if (!sv.ok) {
     if (threadIdx.x == 0) atomicOr(args.status, kStatusBounds);
@@ -251,7 +255,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntl = (sv.L + kBM - 1) / kBM;  // tiles of this sequence
   if (n >= ntl) return;
   const int t_begin = args.causal ? n : 0;  // first query tile that sees key tile n
-  const int count = ntl - t_begin;
+  // last query tile that sees key tile n: query i sees key j iff
+  // j <= i < j + window under the window
+  const int t_last =
+      WIN ? min(ntl - 1, (n * kBM + kBM - 1 + args.window - 1) / kBM) : ntl - 1;
+  const int count = t_last - t_begin + 1;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_A_FULL), 1);
@@ -372,9 +380,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // sequence end (next sequence's rows when packed; key rows past the
       // end are not stored).
       const bool diag = args.causal && tg == n;
-      const int qlim = VAR ? sv.L - tg * kBM : kBM;  // visible query columns: col < qlim
-      const bool masked = diag || qlim < kBM;
-      const int clo = diag ? r : 0;  // visible query columns: clo <= col < qlim
+      // visible query columns: clo <= col < qlim (window: i - j < window,
+      // i = tg*128 + col, j = n*128 + r)
+      const int qlim = VAR ? sv.L - tg * kBM
+                           : (WIN ? min(kBM, r + args.window - (tg - n) * kBM) : kBM);
+      const bool masked =
+          diag || (VAR && qlim < kBM) || (WIN && (tg - n) * kBM + kBM - 1 >= args.window);
+      const int clo = diag ? r : 0;
       const bool w1 = mbar_wait(bar(C::B_S_FULL), t & 1, abort_flag, args.status);
       if (__any_sync(0xffffffffu, !w1)) {
         ok = false;
@@ -394,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 x = __ffma2_rn(
               make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), cc, nl);
           float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
-          if constexpr (VAR) {
+          if constexpr (VAR || WIN) {
             if (masked) {
               if (col < clo || col >= qlim) p0 = 0.f;
               if (col + 1 < clo || col + 1 >= qlim) p1 = 0.f;
@@ -491,7 +503,7 @@ struct DqCfg {
 };
 
 // One CTA per (head, 128-query tile m), in tile_of's order.
-template <int D, bool VAR>
+template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
@@ -511,6 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int bh, rank;  // query tile m sees key tiles 0..m under causal masking
   tile_of(nt, args.BH, bh, rank);
   const int m = nt - 1 - rank;
+  constexpr bool VAR = MODE == kVarlen, WIN = MODE == kWindow;
   const SeqView sv = seq_of<VAR>(args, bh);
   if (!sv.ok) {
     if (threadIdx.x == 0) atomicOr(args.status, kStatusBounds);
@@ -518,7 +531,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int ntl = (sv.L + kBM - 1) / kBM;  // tiles of this sequence
   if (m >= ntl) return;
-  const int count = args.causal ? m + 1 : ntl;  // key tiles 0 .. count-1
+  // key tiles j0 .. j0 + count - 1: under the window, query rows
+  // m*128 .. m*128+127 see no key below m*128 - window + 1
+  const int wlo = m * kBM - args.window + 1;
+  const int j0 = (WIN && wlo > 0) ? wlo / kBM : 0;
+  const int count = (args.causal ? m + 1 : ntl) - j0;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_A_FULL), 1);
@@ -565,14 +582,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             !mbar_wait(bar(C::B_K_EMPTY + ks), ((t / C::KS) - 1) & 1, abort_flag, args.status))
           break;
         mbar_arrive_expect_tx(bar(C::B_K_FULL + ks), C::TILE);
-        load(&tm_k, sbase + C::OFF_K + ks * C::TILE, bar(C::B_K_FULL + ks), t * kBM);
+        load(&tm_k, sbase + C::OFF_K + ks * C::TILE, bar(C::B_K_FULL + ks), (j0 + t) * kBM);
         k_issued = t + 1;
         const int vs = t % C::VS;
         if (t >= C::VS &&
             !mbar_wait(bar(C::B_V_EMPTY + vs), ((t / C::VS) - 1) & 1, abort_flag, args.status))
           break;
         mbar_arrive_expect_tx(bar(C::B_V_FULL + vs), C::TILE);
-        load(&tm_v, sbase + C::OFF_V + vs * C::TILE, bar(C::B_V_FULL + vs), t * kBM);
+        load(&tm_v, sbase + C::OFF_V + vs * C::TILE, bar(C::B_V_FULL + vs), (j0 + t) * kBM);
         v_issued = t + 1;
       }
       if (*abort_flag) {
@@ -636,10 +653,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t s_t = tmem + lane_off + C::TM_S0 + 128u * (t & 1);
       // Masked: the causal diagonal tile, and key columns past the sequence
       // end (next sequence's rows when packed).
-      const bool diag = args.causal && t == m;
-      const int klim = VAR ? sv.L - t * kBM : kBM;  // visible key columns: col < klim
-      const bool masked = diag || klim < kBM;
-      const int khi = diag ? min(klim, r + 1) : klim;  // visible key columns: col < khi
+      const int kt = j0 + t;  // key tile
+      const bool diag = args.causal && kt == m;
+      const int klim = VAR ? sv.L - kt * kBM : kBM;
+      // visible key columns: klo <= col < khi (window: i - j < window,
+      // i = m*128 + r, j = kt*128 + col)
+      const int khi = diag ? min(klim, r + 1) : klim;
+      const int klo = WIN ? (m - kt) * kBM + r - args.window + 1 : 0;
+      const bool masked =
+          diag || (VAR && klim < kBM) || (WIN && (m - kt) * kBM + kBM - 1 >= args.window);
       const bool w1 =
           mbar_wait(bar(C::B_S_FULL + (t & 1)), (t >> 1) & 1, abort_flag, args.status);
       if (__any_sync(0xffffffffu, !w1)) {
@@ -658,10 +680,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 x = __ffma2_rn(
               make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), cc, nl);
           float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
-          if constexpr (VAR) {
+          if constexpr (VAR || WIN) {
             if (masked) {
-              if (col >= khi) p0 = 0.f;
-              if (col + 1 >= khi) p1 = 0.f;
+              if (col < klo || col >= khi) p0 = 0.f;
+              if (col + 1 < klo || col + 1 >= khi) p1 = 0.f;
             }
           } else if (diag) {  // key t*128+col is visible iff col <= r
             if (col > r) p0 = 0.f;
@@ -744,18 +766,18 @@ static_assert(DkdvCfg<64>::SMEM_BYTES <= 232448, "dK/dV shared memory");
 static_assert(DqCfg<128>::SMEM_BYTES <= 232448, "dQ shared memory");
 static_assert(DqCfg<64>::SMEM_BYTES <= 232448, "dQ shared memory");
 
-template <int D, bool VAR>
+template <int D, int MODE>
 cudaError_t launch_impl(const BwdMaps& m, const BwdArgs& a, cudaStream_t stream) {
   static std::atomic<bool> attr_set[64];  // per device: attribute already set
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D, VAR>,
+    e = cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D, MODE>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(DkdvCfg<D>::SMEM_BYTES));
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(fa_bwd_dq_kernel<D, VAR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(fa_bwd_dq_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(DqCfg<D>::SMEM_BYTES));
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_release);
@@ -764,11 +786,11 @@ cudaError_t launch_impl(const BwdMaps& m, const BwdArgs& a, cudaStream_t stream)
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const unsigned blocks = static_cast<unsigned>(static_cast<long long>(a.BH) * a.num_tiles);
-  fa_bwd_dkdv_kernel<D, VAR>
+  fa_bwd_dkdv_kernel<D, MODE>
       <<<blocks, kThreads, DkdvCfg<D>::SMEM_BYTES, stream>>>(m.q, m.k, m.v, m.dout, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  fa_bwd_dq_kernel<D, VAR>
+  fa_bwd_dq_kernel<D, MODE>
       <<<blocks, kThreads, DqCfg<D>::SMEM_BYTES, stream>>>(m.q, m.k, m.v, m.dout, a);
   return cudaGetLastError();
 }
@@ -776,10 +798,15 @@ cudaError_t launch_impl(const BwdMaps& m, const BwdArgs& a, cudaStream_t stream)
 }  // namespace
 
 cudaError_t launch_bwd(const BwdMaps& maps, const BwdArgs& a, int D, cudaStream_t stream) {
-  const bool var = a.cu_seqlens != nullptr;
-  if (D == 128) return var ? launch_impl<128, true>(maps, a, stream)
-                           : launch_impl<128, false>(maps, a, stream);
-  return var ? launch_impl<64, true>(maps, a, stream) : launch_impl<64, false>(maps, a, stream);
+  const int mode = a.cu_seqlens != nullptr ? kVarlen : (a.window > 0 ? kWindow : kDense);
+  if (D == 128) {
+    if (mode == kVarlen) return launch_impl<128, kVarlen>(maps, a, stream);
+    if (mode == kWindow) return launch_impl<128, kWindow>(maps, a, stream);
+    return launch_impl<128, kDense>(maps, a, stream);
+  }
+  if (mode == kVarlen) return launch_impl<64, kVarlen>(maps, a, stream);
+  if (mode == kWindow) return launch_impl<64, kWindow>(maps, a, stream);
+  return launch_impl<64, kDense>(maps, a, stream);
 }
 
 }  // namespace fa

@@ -184,7 +184,7 @@ int fwd_f32(const void* q, const void* k, const void* v, void* o, float* lse, in
 
 int bwd_bf16(const void* q, const void* k, const void* v, const void* o, const void* dout,
              const float* lse, void* dq, void* dk, void* dv, float* workspace, int B, int H,
-             int N, int D, float scale, int causal, void* stream) {
+             int N, int D, float scale, int causal, void* stream, int window = 0) {
   if (B >= 0 && H >= 0 && N >= 0 && (B == 0 || H == 0 || N == 0) &&
       (D == 64 || D == 128) && good_scale(scale))
     return FA_OK;  // empty problem: nothing to read or write
@@ -226,6 +226,7 @@ int bwd_bf16(const void* q, const void* k, const void* v, const void* o, const v
   a.dk = dk;
   a.dv = dv;
   a.status = status;
+  a.window = window;
   return launched(fa::launch_bwd(maps, a, D, static_cast<cudaStream_t>(stream)));
 }
 
@@ -406,6 +407,14 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            int N, int D, float scale, int causal, void* stream) {
   return bwd_bf16(q, k, v, o, dout, lse, dq, dk, dv, workspace, B, H, N, D, scale, causal,
                   stream);
+}
+
+int fa_bwd_window(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                  const float* lse, void* dq, void* dk, void* dv, float* workspace, int B, int H,
+                  int N, int D, float scale, int window, void* stream) {
+  if (window < 1) return FA_ERR_INVALID_ARG;
+  return bwd_bf16(q, k, v, o, dout, lse, dq, dk, dv, workspace, B, H, N, D, scale, 1, stream,
+                  window);
 }
 
 int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dout,

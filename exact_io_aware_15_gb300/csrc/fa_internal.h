@@ -108,6 +108,7 @@ struct BwdArgs {
   int total_tokens;
   int H;
   int max_seqlen;
+  int window;  // > 0 (dense, causal): causal sliding window
 };
 
 struct BwdMaps {

@@ -142,6 +142,17 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            int B, int H, int N, int D, float scale, int causal, void* stream);
 
 /*
+ * Backward of the causal sliding-window forward (fa_fwd_window): same layouts
+ * and workspace as fa_bwd, query i sees keys max(0, i - window + 1) .. i
+ * (window >= 1; window >= N is fa_bwd with causal = 1).  Tiles outside
+ * every row's window are skipped; the edge tiles are masked.
+ */
+int fa_bwd_window(const void* q, const void* k, const void* v, const void* o,
+                  const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                  float* workspace, int B, int H, int N, int D, float scale, int window,
+                  void* stream);
+
+/*
  * Backward of the variable-length forward (fa_fwd_varlen) over packed
  * sequences, by the same recomputation.
  *   q, k, v, o, dout : bf16 [total_tokens, H, D]; sequence s owns tokens

@@ -111,20 +111,23 @@ def attention_ref(q, k, v, scale, causal, rows=None, window=None):
     return O, L
 
 
-def attention_bwd_head_ref(q, k, v, do, scale, causal):
+def attention_bwd_head_ref(q, k, v, do, scale, causal, window=None):
     """Gradients of one head's attention with respect to q, k, v, given the
     output gradient do (all [N, D] float64).  Recomputation, as the tiled
     backward does it: P is rebuilt from the scores and the row log-sum-exp
     (P = e^{S - LSE}), never stored.  With O = P V and S = scale Q K^T:
         dV = P^T dO,  dP = dO V^T,  Delta_i = sum_j P_ij dP_ij = dO_i . O_i,
         dS = P * (dP - Delta),  dQ = scale dS K,  dK = scale dS^T Q.
+    ``window`` (with causal): the sliding window of attention_head_ref.
     Returns dq, dk, dv and Delta."""
     q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
     n = q.shape[0]
-    o, lse = attention_head_ref(q, k, v, scale, causal)
+    o, lse = attention_head_ref(q, k, v, scale, causal, window=window)
     s = scores(q, k, scale)
     if causal:
         s = causal_mask(s, np.arange(n), np.arange(k.shape[0]))
+    if window is not None:
+        s = window_mask(s, np.arange(n), np.arange(k.shape[0]), window)
     p = np.exp(s - lse[:, None])  # rows with no visible key do not occur
     dv = p.T @ do
     dp = do @ v.T
@@ -135,7 +138,8 @@ def attention_bwd_head_ref(q, k, v, do, scale, causal):
     return dq, dk, dv, delta
 
 
-def attention_bwd_sampled_ref(q, k, v, do, scale, causal, rows, cols, chunk=1024):
+def attention_bwd_sampled_ref(q, k, v, do, scale, causal, rows, cols, chunk=1024,
+                              window=None):
     """Selected gradient rows of one head, for heads too long for the full
     matrices: dq at the query rows `rows`, dk and dv at the key rows `cols`.
     O and LSE of every query row come from attention_head_ref over row
@@ -149,13 +153,15 @@ def attention_bwd_sampled_ref(q, k, v, do, scale, causal, rows, cols, chunk=1024
     lse = np.zeros(n)
     for r0 in range(0, n, chunk):
         r = np.arange(r0, min(n, r0 + chunk))
-        o[r], lse[r] = attention_head_ref(q, k, v, scale, causal, rows=r)
+        o[r], lse[r] = attention_head_ref(q, k, v, scale, causal, rows=r, window=window)
     delta = (do * o).sum(axis=1)
     pos = np.arange(n)
     dq = np.zeros((len(rows), q.shape[1]))
     for t, i in enumerate(rows):
         s = scale * (k @ q[i])
         vis = pos <= i if causal else np.ones(n, dtype=bool)
+        if window is not None:
+            vis = vis & (pos > i - window)
         p = np.where(vis, np.exp(s - lse[i]), 0.0)
         ds = p * (v @ do[i] - delta[i])
         dq[t] = scale * (ds @ k)
@@ -164,6 +170,8 @@ def attention_bwd_sampled_ref(q, k, v, do, scale, causal, rows, cols, chunk=1024
     for t, j in enumerate(cols):
         s = scale * (q @ k[j])
         vis = pos >= j if causal else np.ones(n, dtype=bool)
+        if window is not None:
+            vis = vis & (pos < j + window)
         p = np.where(vis, np.exp(s - lse), 0.0)
         ds = p * (do @ v[j] - delta)
         dv[t] = p @ do
@@ -171,7 +179,7 @@ def attention_bwd_sampled_ref(q, k, v, do, scale, causal, rows, cols, chunk=1024
     return dq, dk, dv
 
 
-def attention_bwd_ref(q, k, v, do, scale, causal):
+def attention_bwd_ref(q, k, v, do, scale, causal, window=None):
     """[B, H, N, D] inputs (any dtype, converted exactly to float64); returns
     dq, dk, dv [B, H, N, D] and Delta [B, H, N] in float64."""
     q, k, v, do = to_f64(q), to_f64(k), to_f64(v), to_f64(do)
@@ -181,7 +189,7 @@ def attention_bwd_ref(q, k, v, do, scale, causal):
     for b in range(B):
         for h in range(H):
             dq[b, h], dk[b, h], dv[b, h], delta[b, h] = attention_bwd_head_ref(
-                q[b, h], k[b, h], v[b, h], do[b, h], scale, causal)
+                q[b, h], k[b, h], v[b, h], do[b, h], scale, causal, window=window)
     return dq, dk, dv, delta
 
 

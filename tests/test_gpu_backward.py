@@ -182,3 +182,56 @@ def test_bwd_varlen_bad_offsets_reported(fa):
     fa.fa_bwd_varlen(q, k, v, o, torch.zeros_like(q), lse, bad, 400, case.scale, True)
     assert fa.fa_check_device_status() == fa.FA_ERR_DEVICE_BOUNDS
     assert fa.fa_check_device_status() == fa.FA_OK
+
+
+# --- causal sliding window ------------------------------------------------------------
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("w", [1, 37, 128, 129, 300, 600])
+def test_bwd_window(fa, D, w):
+    N = 517
+    case = inp.dense(1, 2, N, D, seed=980 + w, causal=True)
+    do = inp.output_grad((1, 2, N, D), seed=981 + w)
+    q, k, v = case.q.cuda(), case.k.cuda(), case.v.cuda()
+    o, lse = fa.fa_fwd_window(q, k, v, w, case.scale)
+    g = fa.fa_bwd_window(q, k, v, o, do.cuda(), lse, w, case.scale)
+    torch.cuda.synchronize()
+    assert fa.fa_check_device_status() == fa.FA_OK
+    refs = ora.attention_bwd_ref(case.q, case.k, case.v, do, case.scale, True, window=w)[:3]
+    for name, x, ref in zip(("dq", "dk", "dv"), g, refs):
+        check_grad(np64(x), ref, f"window {w} D={D} {name}")
+
+
+def test_bwd_window_at_least_n_equals_causal(fa):
+    """A window of N or more is causal attention: the same gradients bit for
+    bit as fa_bwd (no edge tile exists, so the same products run)."""
+    N = 300
+    case = inp.dense(1, 2, N, 128, seed=985, causal=True)
+    do = inp.output_grad((1, 2, N, 128), seed=986).cuda()
+    q, k, v = case.q.cuda(), case.k.cuda(), case.v.cuda()
+    o, lse = fa.fa_fwd(q, k, v, case.scale, True)
+    a = fa.fa_bwd(q, k, v, o, do, lse, case.scale, True)
+    b = fa.fa_bwd_window(q, k, v, o, do, lse, N, case.scale)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_bwd_window_full_size_sampled(fa):
+    """B=1 H=32 N=16384 D=128, window 4096: heads 0 and 31 on sampled rows."""
+    B, H, N, D, w = 1, 32, 16384, 128, 4096
+    case = inp.dense(B, H, N, D, seed=987, causal=True)
+    do = inp.output_grad((B, H, N, D), seed=988)
+    q, k, v = case.q.cuda(), case.k.cuda(), case.v.cuda()
+    o, lse = fa.fa_fwd_window(q, k, v, w, case.scale)
+    dq, dk, dv = fa.fa_bwd_window(q, k, v, o, do.cuda(), lse, w, case.scale)
+    torch.cuda.synchronize()
+    assert fa.fa_check_device_status() == fa.FA_OK
+    rng = np.random.default_rng(989)
+    picks = sorted(set([0, 127, 128, w - 1, w, 8191, N - 1]) | set(rng.integers(0, N, 13).tolist()))
+    for h in (0, H - 1):
+        rq, rk, rv = ora.attention_bwd_sampled_ref(case.q[0, h], case.k[0, h], case.v[0, h],
+                                                   do[0, h], case.scale, True, picks, picks,
+                                                   window=w)
+        check_grad(np64(dq[0, h, picks]), rq, f"window dq head {h}")
+        check_grad(np64(dk[0, h, picks]), rk, f"window dk head {h}")
+        check_grad(np64(dv[0, h, picks]), rv, f"window dv head {h}")

@@ -110,3 +110,45 @@ def test_varlen_backward_is_per_sequence(causal):
     g2 = ora.attention_bwd_varlen_ref(q2, k, v, do, cu, 0.5, causal)
     np.testing.assert_array_equal(g2[0][a:e], dq[a:e])
     np.testing.assert_array_equal(g2[1][a:e], dk[a:e])
+
+
+@pytest.mark.parametrize("w", [1, 2, 4])
+def test_window_finite_differences(w):
+    """The sliding-window backward against central differences of the
+    windowed forward oracle."""
+    q, k, v, do = _case(6, 3, 40 + w, std=1.5)
+    scale = 0.7
+    dq, dk, dv, _ = ora.attention_bwd_head_ref(q, k, v, do, scale, True, window=w)
+    h = 1e-6
+
+    def loss():
+        o, _ = ora.attention_head_ref(q, k, v, scale, True, window=w)
+        return float((o * do).sum())
+    for x, g in ((q, dq), (k, dk), (v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            old = x[idx]
+            x[idx] = old + h
+            lp = loss()
+            x[idx] = old - h
+            lm = loss()
+            x[idx] = old
+            num[idx] = (lp - lm) / (2 * h)
+        np.testing.assert_allclose(g, num, rtol=1e-6, atol=1e-8)
+
+
+def test_window_at_least_n_and_sampled():
+    """window >= N is the causal backward; the sampled form equals the full
+    one with a window."""
+    q, k, v, do = _case(40, 4, 50, std=1.2)
+    a = ora.attention_bwd_head_ref(q, k, v, do, 0.5, True)
+    b = ora.attention_bwd_head_ref(q, k, v, do, 0.5, True, window=40)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+    full = ora.attention_bwd_head_ref(q, k, v, do, 0.5, True, window=7)
+    pick = [0, 5, 6, 7, 20, 39]
+    sq, sk, sv = ora.attention_bwd_sampled_ref(q, k, v, do, 0.5, True, pick, pick, chunk=16,
+                                               window=7)
+    np.testing.assert_allclose(sq, full[0][pick], rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(sk, full[1][pick], rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(sv, full[2][pick], rtol=1e-11, atol=1e-13)
