@@ -455,9 +455,24 @@ def other_configs(fa):
     out["paged_gqa_decode_B64_H32_Hkv8_page64"] = {"gbs": kvb / (ms * 1e-3) / 1e9, "ms": ms,
                                                   "kv_bytes": kvb}
     del pc
+    # A launch of this size takes less device time than a Python call, so
+    # 100 launches are captured in a CUDA graph and the replays timed: the
+    # device time per launch, not the host's call rate.
     c1 = inp.config1(device="cuda")
-    ms = _time_launches(lambda: fa.fa_fwd_f32(c1.q, c1.k, c1.v, c1.scale, False), 200)
-    out["fp32_B1_H1_N256_D64"] = {"us": ms * 1e3,
+    o1 = torch.empty_like(c1.q)
+    l1 = torch.empty((1, 1, 256), dtype=torch.float32, device="cuda")
+    f1 = lambda: fa.fa_fwd_f32(c1.q, c1.k, c1.v, c1.scale, False, o=o1, lse=l1)
+    s1 = torch.cuda.Stream()
+    s1.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s1):
+        f1()
+    torch.cuda.current_stream().wait_stream(s1)
+    g1 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g1):
+        for _ in range(100):
+            f1()
+    ms = _time_launches(g1.replay, 10) / 100
+    out["fp32_B1_H1_N256_D64"] = {"us": ms * 1e3, "timing": "CUDA graph of 100 launches",
                                   "gflops": 4.0 * 256 * 256 * 64 / (ms * 1e-3) / 1e9}
     return out
 
@@ -632,8 +647,10 @@ def run_profile_case(args):
     inputs); bwd = its backward (Delta, dK/dV, dQ kernels); rowstats = the
     LayerNorm statistics of 65536 x 4096 bf16; paged = the paged GQA decode
     (B=64, H=32 over H_kv=8, pages of 64, 4.7 GB of KV); scan = prefix
-    attention over the decode workload's caches; decode = split-KV decode on the first 8 sequences of the decode
-    workload (about 2.2 GB of KV cache, larger than L2, small enough for a
+    attention over the decode workload's caches; scan_small = the same on
+    its first 8 sequences with every row cut into 4 chunks (about 2.2 GB of
+    caches and 1.1 GB of output, 1024 CTAs); decode = split-KV decode on the
+    first 8 sequences of the decode workload (about 2.2 GB of KV cache, larger than L2, small enough for a
     multi-pass capture)."""
     import exact_io_aware_15_gb300 as fa
     fa.load_library()
@@ -664,6 +681,16 @@ def run_profile_case(args):
         po = torch.empty_like(pc.k_cache)
         pl = torch.empty((DECODE["H"], pc.meta["T"]), dtype=torch.float32, device="cuda")
         run = lambda: fa.fa_prefix_attention(pc.q, pc.k_cache, pc.v_cache, cu, pc.scale, po, pl)
+    elif args.profile_case == "scan_small":
+        g = torch.Generator().manual_seed(4)
+        lens = torch.randint(1024, 32769, (64,), generator=g).tolist()[:8]
+        pc = inp.decode(8, DECODE["H"], DECODE["D"], seed=4, num_splits=4, lens=lens,
+                        device="cuda")
+        cu = pc.cu_seqlens_k.cuda()
+        po = torch.empty_like(pc.k_cache)
+        pl = torch.empty((DECODE["H"], pc.meta["T"]), dtype=torch.float32, device="cuda")
+        run = lambda: fa.fa_prefix_attention_chunked(pc.q, pc.k_cache, pc.v_cache, cu, 4,
+                                                     pc.scale, po, pl)
     elif args.profile_case == "rowstats":
         x = inp.stats_rows(ROWSTATS["R"], ROWSTATS["C"], seed=11, loc=0.5, std=1.0,
                            row_spread=1.0, device="cuda")
@@ -693,7 +720,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-other-configs", action="store_true")
     ap.add_argument("--profile-case", choices=["prefill", "decode", "bwd", "rowstats", "paged",
-                                                        "scan"],
+                                                "scan", "scan_small"],
                     default=None)
     args = ap.parse_args(argv)
     if args.profile_case:

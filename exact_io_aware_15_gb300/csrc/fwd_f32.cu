@@ -3,11 +3,13 @@
 //
 // Same fold as the tensor-core kernel ("Learning FlashAttention the Hard Way -
 // Part 1": "The State", "The Merge, and the Twist", "Alternative Twist:
-// Base 2"): a CTA of 128 threads owns 64 query rows of one (batch, head); two
-// threads share a row, each holding half of q and of the unnormalised output
-// o.  Key/value tiles of 32 rows are staged in shared memory; each tile is
-// folded into the row state (m, d, o) by one merge, masked keys entering as
-// the identity (sigma = -inf).  The divide o / d is deferred to the end.
+// Base 2"): a CTA of 128 threads owns 128/TPR query rows of one (batch,
+// head); TPR threads share a row, each holding D/TPR columns of q and of the
+// unnormalised output o (TPR = 2 when the grid fills the GPU, 8 for small
+// problems, whose latency the shorter per-thread chains cut).  Key/value
+// tiles of 32 rows are staged in shared memory; each tile is folded into the
+// row state (m, d, o) by one merge, masked keys entering as the identity
+// (sigma = -inf).  The divide o / d is deferred to the end.
 
 #include <cuda_runtime.h>
 #include <math.h>
@@ -18,20 +20,20 @@
 
 namespace fa {
 
-template <int D>
+template <int D, int TPR>
 __global__ void __launch_bounds__(128) fa_fwd_f32_kernel(const F32FwdArgs a) {
-  constexpr int ROWS = 64;
+  constexpr int ROWS = 128 / TPR;
   constexpr int KT = 32;
-  constexpr int HD = D / 2;
-  constexpr int PAD = HD + 4;  // second half offset: avoids a 2-way bank conflict
-  __shared__ __align__(16) float ks[KT][2 * PAD];
-  __shared__ __align__(16) float vs[KT][2 * PAD];
+  constexpr int HD = D / TPR;
+  constexpr int PAD = HD + 4;  // part offset: avoids bank conflicts between the parts
+  __shared__ __align__(16) float ks[KT][TPR * PAD];
+  __shared__ __align__(16) float vs[KT][TPR * PAD];
 
   const int bh = blockIdx.x;
   const int mb = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);
   const int tid = threadIdx.x;
-  const int row = tid >> 1;
-  const int half = tid & 1;
+  const int row = tid / TPR;
+  const int half = tid % TPR;  // this thread's part of the row
   const int N = a.N;
   const int qpos = mb * ROWS + row;
   const bool valid = qpos < N;
@@ -68,7 +70,7 @@ __global__ void __launch_bounds__(128) fa_fwd_f32_kernel(const F32FwdArgs a) {
         kx = *reinterpret_cast<const float4*>(a.k + (head + key) * D + cc);
         vx = *reinterpret_cast<const float4*>(a.v + (head + key) * D + cc);
       }
-      const int col = (cc < HD) ? cc : cc - HD + PAD;
+      const int col = (cc / HD) * PAD + cc % HD;
       *reinterpret_cast<float4*>(&ks[rr][col]) = kx;
       *reinterpret_cast<float4*>(&vs[rr][col]) = vx;
     }
@@ -87,7 +89,8 @@ __global__ void __launch_bounds__(128) fa_fwd_f32_kernel(const F32FwdArgs a) {
         part = fmaf(qr[i + 2], x.z, part);
         part = fmaf(qr[i + 3], x.w, part);
       }
-      part += __shfl_xor_sync(0xffffffffu, part, 1);
+#pragma unroll
+      for (int off = 1; off < TPR; off <<= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
       const int key = k0 + kk;
       const bool vis = key < N && (!a.causal || key <= qpos);
       t[kk] = vis ? part * c : -INFINITY;
@@ -145,11 +148,21 @@ __global__ void __launch_bounds__(128) fa_fwd_f32_kernel(const F32FwdArgs a) {
 }
 
 cudaError_t launch_fwd_f32(const F32FwdArgs& a, int D, cudaStream_t stream) {
-  dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>((a.N + 63) / 64));
-  if (D == 128)
-    fa_fwd_f32_kernel<128><<<grid, 128, 0, stream>>>(a);
-  else
-    fa_fwd_f32_kernel<64><<<grid, 128, 0, stream>>>(a);
+  // two threads per row when that grid fills the GPU twice over, else eight
+  const long long ctas2 = static_cast<long long>(a.BH) * ((a.N + 63) / 64);
+  if (ctas2 >= 304) {
+    dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>((a.N + 63) / 64));
+    if (D == 128)
+      fa_fwd_f32_kernel<128, 2><<<grid, 128, 0, stream>>>(a);
+    else
+      fa_fwd_f32_kernel<64, 2><<<grid, 128, 0, stream>>>(a);
+  } else {
+    dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>((a.N + 15) / 16));
+    if (D == 128)
+      fa_fwd_f32_kernel<128, 8><<<grid, 128, 0, stream>>>(a);
+    else
+      fa_fwd_f32_kernel<64, 8><<<grid, 128, 0, stream>>>(a);
+  }
   return cudaGetLastError();
 }
 

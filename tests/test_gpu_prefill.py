@@ -47,6 +47,16 @@ def test_fp32_shapes(fa, N, D, causal):
     assert np.abs(np64(lse) - L).max() <= TOL_F32
 
 
+def test_fp32_large_grid(fa):
+    """A grid that fills the GPU runs two threads per row (small problems
+    eight): both against the oracle on sampled heads."""
+    case = inp.dense(4, 8, 640, 64, seed=77, causal=True, dtype=torch.float32)
+    o, lse = fa.fa_fwd_f32(*_dense_gpu(case), case.scale, True)
+    O, L = ora.attention_ref(case.q[:1, :2], case.k[:1, :2], case.v[:1, :2], case.scale, True)
+    assert np.abs(np64(o[:1, :2]) - O).max() <= TOL_F32
+    assert np.abs(np64(lse[:1, :2]) - L).max() <= TOL_F32
+
+
 # --- bf16 tensor-core path -------------------------------------------------------
 
 SHAPES = [
