@@ -12,27 +12,44 @@
 // pads the ragged tail).  The output division o / d and the log-sum-exp are
 // deferred to the epilogue.  S and P live only in tensor memory.
 //
-// Roles (192 threads):
-//   warp 0      TMA producer: Q once, then K_j and V_j into a ring of stages.
-//   warp 1      MMA issuer (one thread): S_b = Q K_j^T into TMEM buffer
-//               b = j % 2 (SS form), then O += P_j V_j with P_j read from
-//               TMEM (TS form).  Issue order QK_0, QK_1, PV_0, QK_2, PV_1, ...
-//               so QK_{j+1} overlaps the softmax of tile j.
+// Roles (352 threads):
+//   warp 0      TMA producer: Q once, then K and V tiles into two rings of
+//               stages, in the order the MMA issuer consumes them
+//               (K_0, K_1, then V_j, K_{j+2} for each j).
+//   warp 1      QK issuer (one thread): S = Q K_j^T into the one TMEM S
+//               buffer (SS form), once K_j has landed, the softmax warps have
+//               loaded S_{j-1} into registers, and P_{j-4} V_{j-4} has
+//               finished with P buffer j % 4.  QK_{j+1} runs during the
+//               softmax of tile j.
+//   warp 6      PV issuer (one thread): O += P_j V_j with P_j read from TMEM
+//               (TS form, P_j in TMEM buffer j % 4) once the softmax has
+//               written P_j and the correction warps have rescaled O.
+//               Two issuing threads keep the tensor pipe fed: one thread
+//               issues an M=128 K=16 product about every 80-90 cycles at best,
+//               while two threads together reach one per ~65 cycles at
+//               N = 128, the pipe's own rate.
 //   warps 2..5  softmax: thread t owns row 32*(warp%4) + lane; per tile it
-//               loads its raw S row, masks, takes the row max (3-input max
-//               instructions, four independent chains), computes
-//               p = 2^(s c - m_new) with one packed fused multiply-add per
-//               pair of columns, rounds P to bf16 into TMEM (over the first
-//               half of its S buffer), sums p with packed adds, and, when a
-//               row of its warp raised its maximum, waits for PV_{j-1} and
-//               rescales its O row in TMEM by 2^(m_old - m_new); then signals.
+//               loads its raw S row (then releases the S buffer), masks,
+//               takes the row max (3-input max instructions, four independent
+//               chains), computes p = 2^(s c - m_new) with one packed fused
+//               multiply-add per pair of columns, rounds P to bf16 into TMEM
+//               buffer j % 4 (free: S_j was issued after the product that
+//               last read it had finished), sums p with packed adds, leaves
+//               the rescale factor alpha_j = 2^(m_old - m_new) in shared
+//               memory and signals P_j.
+//   warps 7..10 correction: thread t owns the same row as its softmax thread;
+//               per tile, when a row of its warp raised its maximum, it waits
+//               for P_{j-1} V_{j-1} and rescales its O row in TMEM by alpha_j
+//               (the rescale half of the merge), then signals that O is ready
+//               for P_j V_j.  The softmax warps never wait on the products.
 //               Epilogue: O / d in fp32, LSE = ln2 (m + log2 d), stores.
 //
-// Shared memory (1024-byte aligned): Q tile, STAGES x (K tile, V tile), the
-// mbarriers.  A 128 x D bf16 tile is stored as D/64 column halves of
+// Shared memory (1024-byte aligned): Q tile, KS K tiles, VS V tiles, the
+// mbarriers, the rescale factors (NP x 128 floats).  A 128 x D bf16 tile is stored as D/64 column halves of
 // 128 rows x 128 bytes, 128-byte swizzled (the TMA box layout and the
 // canonical K-major / MN-major tcgen05 operand layouts).
-// Tensor memory (512 columns): S0 [0,128), S1 [128,256), O [256, 256 + D).
+// Tensor memory (512 columns): S [0,128), O [128, 128 + D), P_0..P_3 at
+// [256 + 64 i, 320 + 64 i) (bf16 pairs, 64 columns per 128 keys).
 
 #include <cuda.h>
 #include <atomic>
@@ -51,28 +68,38 @@ struct TcCfg {
   static constexpr int HALVES = D / 64;
   static constexpr uint32_t HALF_BYTES = 128u * 128u;
   static constexpr uint32_t TILE_BYTES = HALVES * HALF_BYTES;
-  static constexpr int STAGES = (D == 128) ? 3 : 4;
+  static constexpr int KS = 2;  // K ring stages
+  static constexpr int VS = 3;  // V ring stages
+  static constexpr int NP = 4;  // P buffers in TMEM
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;
-  static constexpr uint32_t OFF_V = OFF_K + STAGES * TILE_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_V + STAGES * TILE_BYTES;
-  // barrier indices
+  static constexpr uint32_t OFF_V = OFF_K + KS * TILE_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_V + VS * TILE_BYTES;
+  // barrier indices.  V_EMPTY(s) completes when the P V product that read V
+  // stage s has finished; PV_DONE(i) when the one that read P buffer i has
+  // (P_j V_j has finished: O holds it and P buffer j % NP is free).
   static constexpr int B_Q_FULL = 0;
   static constexpr int B_K_FULL = 1;
-  static constexpr int B_V_FULL = B_K_FULL + STAGES;
-  static constexpr int B_KV_EMPTY = B_V_FULL + STAGES;
-  static constexpr int B_S_FULL = B_KV_EMPTY + STAGES;
-  static constexpr int B_P_FULL = B_S_FULL + 2;
-  static constexpr int B_O_DONE = B_P_FULL + 2;
-  static constexpr int B_DRAIN = B_O_DONE + 1;
-  static constexpr int NUM_BARS = B_DRAIN + 1;
-  static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int B_V_FULL = B_K_FULL + KS;
+  static constexpr int B_K_EMPTY = B_V_FULL + VS;
+  static constexpr int B_V_EMPTY = B_K_EMPTY + KS;
+  static constexpr int B_S_FULL = B_V_EMPTY + VS;
+  static constexpr int B_S_FREE = B_S_FULL + 1;  // S loaded by the softmax warps
+  static constexpr int B_P_FULL = B_S_FREE + 1;  // one per P buffer
+  static constexpr int B_PV_DONE = B_P_FULL + NP;
+  static constexpr int B_O_READY = B_PV_DONE + NP;  // O rescaled for P_j V_j
+  static constexpr int B_DRAIN = B_O_READY + NP;  // one per issuing thread
+  static constexpr int NUM_BARS = B_DRAIN + 2;
+  static constexpr uint32_t OFF_ALPHA = OFF_BAR + NUM_BARS * 8;
+  static constexpr uint32_t OFF_MISC = OFF_ALPHA + NP * 128 * 4;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t TMEM_S0 = 0;
-  static constexpr uint32_t TMEM_S1 = 128;
-  static constexpr uint32_t TMEM_O = 256;
-  static constexpr int THREADS = 192;
+  static constexpr uint32_t TMEM_S = 0;
+  static constexpr uint32_t TMEM_O = 128;
+  static constexpr uint32_t TMEM_P = 256;  // buffer i at TMEM_P + 64 i
+  static constexpr int THREADS = 352;
+  static constexpr int WARP_PV = 6;
+  static constexpr int WARP_CORR = 7;  // warps 7..10
   static constexpr int SOFTMAX_THREADS = 128;
 };
 
@@ -158,17 +185,23 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_Q_FULL), 1);
-    for (int s = 0; s < C::STAGES; ++s) {
+    for (int s = 0; s < C::KS; ++s) {
       mbar_init(bar(C::B_K_FULL + s), 1);
+      mbar_init(bar(C::B_K_EMPTY + s), 1);
+    }
+    for (int s = 0; s < C::VS; ++s) {
       mbar_init(bar(C::B_V_FULL + s), 1);
-      mbar_init(bar(C::B_KV_EMPTY + s), 1);
+      mbar_init(bar(C::B_V_EMPTY + s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(C::B_S_FULL + b), 1);
+    mbar_init(bar(C::B_S_FULL), 1);
+    mbar_init(bar(C::B_S_FREE), C::SOFTMAX_THREADS);
+    for (int b = 0; b < C::NP; ++b) {
       mbar_init(bar(C::B_P_FULL + b), C::SOFTMAX_THREADS);
+      mbar_init(bar(C::B_PV_DONE + b), 1);
+      mbar_init(bar(C::B_O_READY + b), C::SOFTMAX_THREADS);
     }
-    mbar_init(bar(C::B_O_DONE), 1);
     mbar_init(bar(C::B_DRAIN), 1);
+    mbar_init(bar(C::B_DRAIN + 1), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -202,7 +235,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
   if (warp == 0) {
     // ======================= TMA producer =======================
     if (lane == 0) {
-      int issued = 0;
+      int k_issued = 0, v_issued = 0;
       {
         const uint32_t qb = bar(C::B_Q_FULL);
         mbar_arrive_expect_tx(qb, C::TILE_BYTES);
@@ -213,85 +246,60 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
           tma_load_3d(sbase + C::OFF_Q + c * C::HALF_BYTES, &tm_q, qb, c0, c1, c2);
         }
       }
-      for (int j = 0; j < n_kv; ++j) {
-        const int st = j % C::STAGES;
-        if (j >= C::STAGES) {
-          if (!mbar_wait(bar(C::B_KV_EMPTY + st), ((j / C::STAGES) - 1) & 1, abort_flag,
-                         args.status))
-            break;
-        }
-        const uint32_t kb = bar(C::B_K_FULL + st);
-        const uint32_t vb = bar(C::B_V_FULL + st);
-        mbar_arrive_expect_tx(kb, C::TILE_BYTES);
+      // One tile of K (is_v false) or V into its ring, after the product
+      // that read the stage's previous tile has finished.
+      auto load = [&](bool is_v, int j) -> bool {
+        const int S = is_v ? C::VS : C::KS;
+        const int st = j % S;
+        if (j >= S && !mbar_wait(bar((is_v ? C::B_V_EMPTY : C::B_K_EMPTY) + st),
+                                 ((j / S) - 1) & 1, abort_flag, args.status))
+          return false;
+        const uint32_t fb = bar((is_v ? C::B_V_FULL : C::B_K_FULL) + st);
+        const uint32_t dst = sbase + (is_v ? C::OFF_V : C::OFF_K) + st * C::TILE_BYTES;
+        mbar_arrive_expect_tx(fb, C::TILE_BYTES);
 #pragma unroll
         for (int c = 0; c < C::HALVES; ++c) {
           int c0, c1, c2;
           tile_coords(c, (j0 + j) * C::BN, c0, c1, c2);
-          tma_load_3d(sbase + C::OFF_K + st * C::TILE_BYTES + c * C::HALF_BYTES, &tm_k, kb,
-                      c0, c1, c2);
+          tma_load_3d(dst + c * C::HALF_BYTES, is_v ? &tm_v : &tm_k, fb, c0, c1, c2);
         }
-        mbar_arrive_expect_tx(vb, C::TILE_BYTES);
-#pragma unroll
-        for (int c = 0; c < C::HALVES; ++c) {
-          int c0, c1, c2;
-          tile_coords(c, (j0 + j) * C::BN, c0, c1, c2);
-          tma_load_3d(sbase + C::OFF_V + st * C::TILE_BYTES + c * C::HALF_BYTES, &tm_v, vb,
-                      c0, c1, c2);
-        }
-        issued = j + 1;
+        if (is_v) v_issued = j + 1; else k_issued = j + 1;
+        return true;
+      };
+      bool ok = load(false, 0) && (n_kv < 2 || load(false, 1));
+      for (int j = 0; ok && j < n_kv; ++j) {
+        ok = load(true, j) && (j + 2 >= n_kv || load(false, j + 2));
       }
       if (*abort_flag) {
         // Let every copy this thread started land before the CTA exits.
         mbar_wait_unwind(bar(C::B_Q_FULL), 0);
-        for (int j = max(0, issued - C::STAGES); j < issued; ++j) {
-          const int st = j % C::STAGES;
-          mbar_wait_unwind(bar(C::B_K_FULL + st), (j / C::STAGES) & 1);
-          mbar_wait_unwind(bar(C::B_V_FULL + st), (j / C::STAGES) & 1);
-        }
+        for (int j = max(0, k_issued - C::KS); j < k_issued; ++j)
+          mbar_wait_unwind(bar(C::B_K_FULL + j % C::KS), (j / C::KS) & 1);
+        for (int j = max(0, v_issued - C::VS); j < v_issued; ++j)
+          mbar_wait_unwind(bar(C::B_V_FULL + j % C::VS), (j / C::VS) & 1);
       }
     }
   } else if (warp == 1) {
-    // ======================= MMA issuer =======================
+    // ======================= QK issuer =======================
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
       const uint32_t q_s = sbase + C::OFF_Q;
-
-      auto issue_pv = [&](int i) -> bool {
-        const int b = i & 1;
-        const int st = i % C::STAGES;
-        if (!mbar_wait(bar(C::B_P_FULL + b), (i >> 1) & 1, abort_flag, args.status))
-          return false;
-        if (!mbar_wait(bar(C::B_V_FULL + st), (i / C::STAGES) & 1, abort_flag, args.status))
-          return false;
-        tc_fence_after();
-        const uint32_t v_s = sbase + C::OFF_V + st * C::TILE_BYTES;
-        const uint32_t p_t = tmem + (b ? C::TMEM_S1 : C::TMEM_S0);
-#pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk) {
-          // B = V_j as an MN-major operand: N = D (64-column halves
-          // HALF_BYTES apart), K = 16 keys starting at key 16*kk.
-          const uint64_t bdesc = sdesc_sw128(v_s + kk * 16u * 128u, C::HALF_BYTES, 1024u);
-          tc_mma_ts(tmem + C::TMEM_O, p_t + kk * 8u, bdesc, idesc_pv,
-                    (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc_commit(bar(C::B_O_DONE));
-        tc_commit(bar(C::B_KV_EMPTY + st));
-        return true;
-      };
-
       bool ok = mbar_wait(bar(C::B_Q_FULL), 0, abort_flag, args.status);
-      tc_fence_after();
       for (int j = 0; ok && j < n_kv; ++j) {
-        const int st = j % C::STAGES;
-        const int b = j & 1;
-        if (!mbar_wait(bar(C::B_K_FULL + st), (j / C::STAGES) & 1, abort_flag, args.status)) {
+        // The S buffer is free once the softmax warps have loaded S_{j-1};
+        // P buffer j % 4, which the softmax of tile j writes, once
+        // P_{j-4} V_{j-4} has finished.
+        if (!mbar_wait(bar(C::B_K_FULL + j % C::KS), (j / C::KS) & 1, abort_flag,
+                       args.status) ||
+            (j >= 1 && !mbar_wait(bar(C::B_S_FREE), (j - 1) & 1, abort_flag, args.status)) ||
+            (j >= C::NP && !mbar_wait(bar(C::B_PV_DONE + j % C::NP), ((j - C::NP) / C::NP) & 1,
+                                      abort_flag, args.status))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t k_s = sbase + C::OFF_K + st * C::TILE_BYTES;
-        const uint32_t s_t = tmem + (b ? C::TMEM_S1 : C::TMEM_S0);
+        const uint32_t k_s = sbase + C::OFF_K + (j % C::KS) * C::TILE_BYTES;
+        const uint32_t s_t = tmem + C::TMEM_S;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           // 16-column slice kk of the head dimension: half kk/4, 32 bytes
@@ -300,14 +308,76 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
           tc_mma_ss(s_t, sdesc_sw128(q_s + off, 16u, 1024u), sdesc_sw128(k_s + off, 16u, 1024u),
                     idesc_qk, kk > 0 ? 1u : 0u);
         }
-        tc_commit(bar(C::B_S_FULL + b));
-        if (j >= 1 && !issue_pv(j - 1)) ok = false;
+        tc_commit(bar(C::B_S_FULL));
+        tc_commit(bar(C::B_K_EMPTY + j % C::KS));
       }
-      if (ok) issue_pv(n_kv - 1);
       // Every MMA this thread issued completes before TMEM is released.
       tc_commit(bar(C::B_DRAIN));
       mbar_wait_unwind(bar(C::B_DRAIN), 0);
     }
+  } else if (warp == C::WARP_PV) {
+    // ======================= PV issuer =======================
+    if (lane == 0) {
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
+      for (int j = 0; j < n_kv; ++j) {
+        const int sv = j % C::VS;
+        if (!mbar_wait(bar(C::B_P_FULL + j % C::NP), (j / C::NP) & 1, abort_flag, args.status) ||
+            !mbar_wait(bar(C::B_V_FULL + sv), (j / C::VS) & 1, abort_flag, args.status) ||
+            !mbar_wait(bar(C::B_O_READY + j % C::NP), (j / C::NP) & 1, abort_flag, args.status))
+          break;
+        tc_fence_after();
+        const uint32_t v_s = sbase + C::OFF_V + sv * C::TILE_BYTES;
+        const uint32_t p_t = tmem + C::TMEM_P + 64u * (j % C::NP);
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk) {
+          // B = V_j as an MN-major operand: N = D (64-column halves
+          // HALF_BYTES apart), K = 16 keys starting at key 16*kk.
+          const uint64_t bdesc = sdesc_sw128(v_s + kk * 16u * 128u, C::HALF_BYTES, 1024u);
+          tc_mma_ts(tmem + C::TMEM_O, p_t + kk * 8u, bdesc, idesc_pv,
+                    (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(bar(C::B_V_EMPTY + sv));
+        tc_commit(bar(C::B_PV_DONE + j % C::NP));
+      }
+      tc_commit(bar(C::B_DRAIN + 1));
+      mbar_wait_unwind(bar(C::B_DRAIN + 1), 0);
+    }
+  } else if (warp >= C::WARP_CORR) {
+    // ======================= O correction =======================
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t o_t = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + C::TMEM_O;
+    const float* alpha_s = reinterpret_cast<const float*>(smem + C::OFF_ALPHA);
+    for (int j = 0; j < n_kv; ++j) {
+      const int pb = j % C::NP;
+      const bool w = mbar_wait(bar(C::B_P_FULL + pb), (j / C::NP) & 1, abort_flag, args.status);
+      if (__any_sync(0xffffffffu, !w)) break;
+      const float alpha = alpha_s[pb * 128 + r];
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        // o <- alpha * o between P_{j-1} V_{j-1} and P_j V_j.
+        const bool w2 = mbar_wait(bar(C::B_PV_DONE + (j - 1) % C::NP), ((j - 1) / C::NP) & 1,
+                                  abort_flag, args.status);
+        if (__any_sync(0xffffffffu, !w2)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 64) {
+          uint32_t ov[64];
+          tmem_ld64(o_t + c0, ov);
+          uint32_t lo[32], hi[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            lo[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            hi[i] = __float_as_uint(__uint_as_float(ov[32 + i]) * alpha);
+          }
+          tmem_st32(o_t + c0, lo);
+          tmem_st32(o_t + c0 + 32, hi);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      mbar_arrive(bar(C::B_O_READY + pb));
+    }
+    tc_fence_before();
   } else {
     // ======================= softmax / epilogue =======================
     const int quarter = warp & 3;
@@ -321,11 +391,11 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
     float m = -INFINITY;
     float dsum = 0.f;
     bool ok = true;
+    float* alpha_s = reinterpret_cast<float*>(smem + C::OFF_ALPHA);
 
     for (int j = 0; j < n_kv; ++j) {
-      const int b = j & 1;
-      const uint32_t s_t = tmem + lane_off + (b ? C::TMEM_S1 : C::TMEM_S0);
-      const bool w = mbar_wait(bar(C::B_S_FULL + b), (j >> 1) & 1, abort_flag, args.status);
+      const uint32_t s_t = tmem + lane_off + C::TMEM_S;
+      const bool w = mbar_wait(bar(C::B_S_FULL), j & 1, abort_flag, args.status);
       if (__any_sync(0xffffffffu, !w)) {
         ok = false;
         break;
@@ -342,6 +412,9 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 64; ++i) t[64 + i] = __uint_as_float(raw[i]);
       }
+      // S_j is in registers: QK_{j+1} may overwrite the buffer.
+      tc_fence_before();
+      mbar_arrive(bar(C::B_S_FREE));
       const int kbase = (j0 + j) * C::BN;
       const bool win_edge = args.window > 0 && kbase < mb * C::BM + C::BM - args.window;
       if ((args.causal && j0 + j == mb) || kbase + C::BN > L || win_edge) {
@@ -356,21 +429,24 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 128; ++i) t[i] = (t[i] == -INFINITY) ? -INFINITY : 0.f;
       }
-      float mx0 = fmax3(t[0], t[1], t[2]), mx1 = fmax3(t[3], t[4], t[5]);
-      float mx2 = fmax3(t[6], t[7], t[8]), mx3 = fmax3(t[9], t[10], t[11]);
+      // Row max over 128 values in 16 independent chains of 3-input maxima.
+      float q[16];
 #pragma unroll
-      for (int i = 12; i < 124; i += 8) {
-        mx0 = fmax3(mx0, t[i], t[i + 1]);
-        mx1 = fmax3(mx1, t[i + 2], t[i + 3]);
-        mx2 = fmax3(mx2, t[i + 4], t[i + 5]);
-        mx3 = fmax3(mx3, t[i + 6], t[i + 7]);
-      }
-      mx0 = fmax3(mx0, t[124], t[125]);
-      mx1 = fmax3(mx1, t[126], t[127]);
-      const float mx = fmaxf(fmax3(mx0, mx1, mx2), mx3) * c;
+      for (int k = 0; k < 16; ++k) q[k] = fmax3(t[8 * k], t[8 * k + 1], t[8 * k + 2]);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) q[k] = fmax3(q[k], t[8 * k + 3], t[8 * k + 4]);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) q[k] = fmax3(q[k], t[8 * k + 5], t[8 * k + 6]);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) q[k] = fmaxf(q[k], t[8 * k + 7]);
+      const float r0 = fmax3(q[0], q[1], q[2]), r1 = fmax3(q[3], q[4], q[5]);
+      const float r2 = fmax3(q[6], q[7], q[8]), r3 = fmax3(q[9], q[10], q[11]);
+      const float r4 = fmax3(q[12], q[13], q[14]);
+      const float mx = fmaxf(fmax3(r0, r1, r2), fmax3(r3, r4, q[15])) * c;
       const float m_new = fmaxf(m, mx);
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = (m_new == m) ? 1.f : ex2_approx(m - m_use);
+      const uint32_t p_t = tmem + lane_off + C::TMEM_P + 64u * (j % C::NP);
       const float2 cc = make_float2(c, c), nm = make_float2(-m_use, -m_use);
       float2 a0 = make_float2(0.f, 0.f), a1 = a0;
 #pragma unroll
@@ -383,44 +459,21 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
           if (i & 1) a1 = __fadd2_rn(a1, p); else a0 = __fadd2_rn(a0, p);
           pk[i] = pack_bf16x2(p.x, p.y);
         }
-        tmem_st32(s_t + 32u * h, pk);
+        tmem_st32(p_t + 32u * h, pk);
       }
       const float2 aa = __fadd2_rn(a0, a1);
       dsum = dsum * alpha + (aa.x + aa.y);
       m = m_new;
 
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        // o <- alpha * o needs PV_{j-1} to have landed in TMEM.
-        const bool w2 = mbar_wait(bar(C::B_O_DONE), (j - 1) & 1, abort_flag, args.status);
-        if (__any_sync(0xffffffffu, !w2)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          const uint32_t o_t = tmem + lane_off + C::TMEM_O;
-#pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 64) {
-            uint32_t ov[64];
-            tmem_ld64(o_t + c0, ov);
-            uint32_t lo[32], hi[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              lo[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-              hi[i] = __float_as_uint(__uint_as_float(ov[32 + i]) * alpha);
-            }
-            tmem_st32(o_t + c0, lo);
-            tmem_st32(o_t + c0 + 32, hi);
-          }
-        }
-      }
+      alpha_s[(j % C::NP) * 128 + r] = alpha;
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(C::B_P_FULL + b));
+      mbar_arrive(bar(C::B_P_FULL + j % C::NP));
     }
 
     if (ok) {
-      const bool w = mbar_wait(bar(C::B_O_DONE), (n_kv - 1) & 1, abort_flag, args.status);
+      const bool w = mbar_wait(bar(C::B_PV_DONE + (n_kv - 1) % C::NP),
+                               ((n_kv - 1) / C::NP) & 1, abort_flag, args.status);
       if (!__any_sync(0xffffffffu, !w)) {
         tc_fence_after();
         const float inv = dsum > 0.f ? 1.f / dsum : 0.f;
