@@ -578,6 +578,14 @@ def run_gpu(args, rank, world, dist):
     ev_in = [torch.cuda.Event() for _ in range(n_e2e)]
     ev_done = [torch.cuda.Event() for _ in range(n_e2e)]
     ev_out = [torch.cuda.Event() for _ in range(n_e2e)]
+    # two untimed passes of the same loop first (copy engines, pinned pages)
+    for i in range(2):
+        for dst, src in zip(din[i], (hq, hk, hv)):
+            dst.copy_(src, non_blocking=True)
+        fa.fa_fwd(*din[i], pc.scale, True, o=dout[i][0], lse=dout[i][1])
+        ho[i].copy_(dout[i][0], non_blocking=True)
+        hl[i].copy_(dout[i][1], non_blocking=True)
+    torch.cuda.synchronize()
     barrier(dist)
     t0 = time.perf_counter()
     for i in range(n_e2e):
