@@ -37,7 +37,8 @@ def test_config1_fp32(fa):
 
 
 @pytest.mark.parametrize("N,D,causal", [(1, 64, False), (63, 64, True), (200, 128, False),
-                                        (333, 128, True), (129, 64, True)])
+                                        (333, 128, True), (129, 64, True), (70, 64, False),
+                                        (1000, 64, True), (2048, 64, False)])
 def test_fp32_shapes(fa, N, D, causal):
     case = inp.dense(2, 3, N, D, seed=10 + N, causal=causal, dtype=torch.float32,
                      qk_std=2.0)
