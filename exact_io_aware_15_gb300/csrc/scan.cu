@@ -176,9 +176,10 @@ __global__ void __launch_bounds__(256, 2) fa_prefix_scan_kernel(const ScanArgs a
   Cols<VPL> kr[kKeysPerWarp], vr[kKeysPerWarp];
   auto load_rows = [&](Cols<VPL>(&r)[kKeysPerWarp], const uint16_t* base, int w0) {
     const int kw = w0 + warp * kKeysPerWarp;
+    const uint16_t* p = base + static_cast<size_t>(kw) * stride;
 #pragma unroll
-    for (int i = 0; i < kKeysPerWarp; ++i)
-      if (kw + i < k1) r[i] = ld_cols<VPL>(base + static_cast<size_t>(kw + i) * stride);
+    for (int i = 0; i < kKeysPerWarp; ++i, p += stride)
+      if (kw + i < k1) r[i] = ld_cols<VPL>(p);
   };
   load_rows(kr, kp, k0);
   load_rows(vr, vp, k0);
@@ -247,8 +248,12 @@ __global__ void __launch_bounds__(256, 2) fa_prefix_scan_kernel(const ScanArgs a
 #pragma unroll
     for (int j = 0; j < VPL; ++j) o[j] = co[j];
     for (int w = 0; w < warp; ++w) merge_into<VPL>(m, d, o, tot_m[w], tot_d[w], &tot_o[w][lane * VPL]);
+    // Lane i keeps key i's LSE and stores it after the rescan (one coalesced
+    // store instead of a lane-0 store per key).
+    float lse_mine = 0.f;
+    uint16_t* dst = op + static_cast<size_t>(kw) * stride;
 #pragma unroll
-    for (int i = 0; i < kKeysPerWarp; ++i) {
+    for (int i = 0; i < kKeysPerWarp; ++i, dst += stride) {
       if (i < nk) {
         const float mn = fmaxf(m, sg[i]);
         const float al = ex2_approx(m - mn);  // m = -inf before the first key: 0
@@ -265,15 +270,16 @@ __global__ void __launch_bounds__(256, 2) fa_prefix_scan_kernel(const ScanArgs a
           pk[j / 2] = pack_bf16x2(o[j] * inv, o[j + 1] * inv);
         }
         m = mn;
-        uint16_t* dst = op + static_cast<size_t>(kw + i) * stride;
         if constexpr (VPL == 4) {
           *reinterpret_cast<uint2*>(dst) = make_uint2(pk[0], pk[1]);
         } else {
           *reinterpret_cast<uint32_t*>(dst) = pk[0];
         }
-        if (lane == 0) lp[kw + i] = kLn2 * (m + __log2f(d));
+        const float lv = kLn2 * (m + __log2f(d));
+        if (lane == i) lse_mine = lv;
       }
     }
+    if (lane < nk) lp[kw + lane] = lse_mine;
     load_rows(vr, vp, w0 + kWindow);
     // The carry of the next window is warp 7's running state after its
     // rescan: the carry in (+) every key of this window.
