@@ -392,6 +392,9 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_before();
   }
 
+  // Role warps ran their loops in lane 0 alone: reconverge each warp before
+  // the CTA barrier, which counts whole warps.
+  __syncwarp();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();

@@ -183,7 +183,42 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // TMA box origin of a 128-row tile starting at sequence position `row0`,
+  // column half `c`.  Dense maps are (D, N, B*H); varlen maps are (D, H, T).
+  auto tile_coords = [&](int c, int row0, int& c0, int& c1, int& c2) {
+    c0 = c * 64;
+    if (varlen) {
+      c1 = h;
+      c2 = tok0 + row0;
+    } else {
+      c1 = row0;
+      c2 = bh;
+    }
+  };
+  // One tile of K (is_v false) or V into its ring, after the product that
+  // read the stage's previous tile has finished (issued by thread 0 only).
+  auto load = [&](bool is_v, int j) -> bool {
+    const int S = is_v ? C::VS : C::KS;
+    const int st = j % S;
+    if (j >= S && !mbar_wait(bar((is_v ? C::B_V_EMPTY : C::B_K_EMPTY) + st), ((j / S) - 1) & 1,
+                             abort_flag, args.status))
+      return false;
+    const uint32_t fb = bar((is_v ? C::B_V_FULL : C::B_K_FULL) + st);
+    const uint32_t dst = sbase + (is_v ? C::OFF_V : C::OFF_K) + st * C::TILE_BYTES;
+    mbar_arrive_expect_tx(fb, C::TILE_BYTES);
+#pragma unroll
+    for (int c = 0; c < C::HALVES; ++c) {
+      int c0, c1, c2;
+      tile_coords(c, (j0 + j) * C::BN, c0, c1, c2);
+      tma_load_3d(dst + c * C::HALF_BYTES, is_v ? &tm_v : &tm_k, fb, c0, c1, c2);
+    }
+    return true;
+  };
+
   if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
     mbar_init(bar(C::B_Q_FULL), 1);
     for (int s = 0; s < C::KS; ++s) {
       mbar_init(bar(C::B_K_FULL + s), 1);
@@ -204,11 +239,19 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
     mbar_init(bar(C::B_DRAIN + 1), 1);
     *abort_flag = 0;
     fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
+    // The first copies need no free stage: start them before the CTA-wide
+    // setup (TMEM allocation, barrier), so their latency overlaps it.
+    const uint32_t qb = bar(C::B_Q_FULL);
+    mbar_arrive_expect_tx(qb, C::TILE_BYTES);
+#pragma unroll
+    for (int c = 0; c < C::HALVES; ++c) {
+      int c0, c1, c2;
+      tile_coords(c, mb * C::BM, c0, c1, c2);
+      tma_load_3d(sbase + C::OFF_Q + c * C::HALF_BYTES, &tm_q, qb, c0, c1, c2);
+    }
+    load(false, 0);
+    if (n_kv >= 2) load(false, 1);
+    load(true, 0);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
@@ -219,56 +262,20 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  // TMA box origin of a 128-row tile starting at sequence position `row0`,
-  // column half `c`.  Dense maps are (D, N, B*H); varlen maps are (D, H, T).
-  auto tile_coords = [&](int c, int row0, int& c0, int& c1, int& c2) {
-    c0 = c * 64;
-    if (varlen) {
-      c1 = h;
-      c2 = tok0 + row0;
-    } else {
-      c1 = row0;
-      c2 = bh;
-    }
-  };
-
   if (warp == 0) {
     // ======================= TMA producer =======================
     if (lane == 0) {
-      int k_issued = 0, v_issued = 0;
-      {
-        const uint32_t qb = bar(C::B_Q_FULL);
-        mbar_arrive_expect_tx(qb, C::TILE_BYTES);
-#pragma unroll
-        for (int c = 0; c < C::HALVES; ++c) {
-          int c0, c1, c2;
-          tile_coords(c, mb * C::BM, c0, c1, c2);
-          tma_load_3d(sbase + C::OFF_Q + c * C::HALF_BYTES, &tm_q, qb, c0, c1, c2);
+      // Q, K_0, K_1 and V_0 were issued before the CTA barrier.
+      int k_issued = min(n_kv, 2), v_issued = 1;
+      for (int j = 0; j < n_kv; ++j) {
+        if (j > 0) {
+          if (!load(true, j)) break;
+          v_issued = j + 1;
         }
-      }
-      // One tile of K (is_v false) or V into its ring, after the product
-      // that read the stage's previous tile has finished.
-      auto load = [&](bool is_v, int j) -> bool {
-        const int S = is_v ? C::VS : C::KS;
-        const int st = j % S;
-        if (j >= S && !mbar_wait(bar((is_v ? C::B_V_EMPTY : C::B_K_EMPTY) + st),
-                                 ((j / S) - 1) & 1, abort_flag, args.status))
-          return false;
-        const uint32_t fb = bar((is_v ? C::B_V_FULL : C::B_K_FULL) + st);
-        const uint32_t dst = sbase + (is_v ? C::OFF_V : C::OFF_K) + st * C::TILE_BYTES;
-        mbar_arrive_expect_tx(fb, C::TILE_BYTES);
-#pragma unroll
-        for (int c = 0; c < C::HALVES; ++c) {
-          int c0, c1, c2;
-          tile_coords(c, (j0 + j) * C::BN, c0, c1, c2);
-          tma_load_3d(dst + c * C::HALF_BYTES, is_v ? &tm_v : &tm_k, fb, c0, c1, c2);
+        if (j + 2 < n_kv) {
+          if (!load(false, j + 2)) break;
+          k_issued = j + 3;
         }
-        if (is_v) v_issued = j + 1; else k_issued = j + 1;
-        return true;
-      };
-      bool ok = load(false, 0) && (n_kv < 2 || load(false, 1));
-      for (int j = 0; ok && j < n_kv; ++j) {
-        ok = load(true, j) && (j + 2 >= n_kv || load(false, j + 2));
       }
       if (*abort_flag) {
         // Let every copy this thread started land before the CTA exits.
@@ -489,15 +496,16 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
           lidx = orow;
         }
         const uint32_t o_t = tmem + lane_off + C::TMEM_O;
+        // 64 columns per TMEM load (one wait each), then the stores.
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t ov[32];
-          tmem_ld32(o_t + c0, ov);
+        for (int c0 = 0; c0 < D; c0 += 64) {
+          uint32_t ov[64];
+          tmem_ld64(o_t + c0, ov);
           if (store) {
             if (args.o_f32) {
               float4* dst = reinterpret_cast<float4*>(static_cast<float*>(args.o) + orow * D + c0);
 #pragma unroll
-              for (int i = 0; i < 8; ++i)
+              for (int i = 0; i < 16; ++i)
                 dst[i] = make_float4(__uint_as_float(ov[4 * i]) * inv,
                                      __uint_as_float(ov[4 * i + 1]) * inv,
                                      __uint_as_float(ov[4 * i + 2]) * inv,
@@ -505,7 +513,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
             } else {
               uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.o) + orow * D + c0);
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
+              for (int i = 0; i < 8; ++i) {
                 uint4 u;
                 u.x = pack_bf16x2(__uint_as_float(ov[8 * i + 0]) * inv,
                                   __uint_as_float(ov[8 * i + 1]) * inv);
@@ -526,6 +534,9 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
     tc_fence_before();
   }
 
+  // Role warps ran their loops in lane 0 alone: reconverge each warp before
+  // the CTA barrier, which counts whole warps.
+  __syncwarp();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
