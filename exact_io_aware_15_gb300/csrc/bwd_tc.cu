@@ -29,8 +29,12 @@
 // tensor cores run the next tile's products while the warps are busy:
 //   dK/dV:  SS_S(0) SS_dP(0) | TS_dV(t) SS_S(t+1) TS_dK(t) SS_dP(t+1) | ...
 //           TS_dV(t) waits for P(t), TS_dK(t) for dS(t).
-//   dQ:     SS_S(0) SS_dP(0) SS_S(1) | TS_dQ(t) SS_dP(t+1) SS_S(t+2) | ...
-//           with S double-buffered in TMEM; TS_dQ(t) waits for dS(t).
+//   dQ:     warp 1 issues SS_S(0) SS_dP(0) SS_S(1) | SS_dP(t+1) SS_S(t+2) | ...,
+//           warp 6 TS_dQ(t) | ...; S is double-buffered in TMEM and dS(t)
+//           is written over S(t).  TS_dQ(t) and SS_dP(t+1) both wait for
+//           dS(t) (the warps have read dP(t) by then) and run at once, on two
+//           issuing threads; SS_S(t+2) waits until TS_dQ(t) has read dS(t)
+//           out of the buffer it overwrites.
 // tcgen05.mma instructions of one thread execute in issue order, so a
 // product that overwrites a TMEM region never overtakes an earlier one that
 // reads it.  Every wait is bounded: on expiry the kernel records
@@ -51,7 +55,9 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kBM = 128;
 constexpr uint32_t kHalfBytes = 128u * 128u;  // 128 rows x 64 bf16 columns
-constexpr int kThreads = 192;
+constexpr int kThreads = 192;     // dK/dV kernel
+constexpr int kDqThreads = 224;   // dQ kernel: + the warp that issues TS_dQ
+constexpr int kWarpAcc = 6;       // dQ: issues TS_dQ
 constexpr int kElemThreads = 128;
 
 __device__ __forceinline__ void mbar_wait_unwind_b(uint32_t bar, uint32_t parity) {
@@ -495,10 +501,11 @@ struct DqCfg {
   static constexpr int B_V_EMPTY = B_V_FULL + VS;
   static constexpr int B_S_FULL = B_V_EMPTY + VS;  // two, one per S buffer
   static constexpr int B_DP_FULL = B_S_FULL + 2;
-  static constexpr int B_DS_DONE = B_DP_FULL + 1;
-  static constexpr int B_ACC_DONE = B_DS_DONE + 1;
-  static constexpr int B_DRAIN = B_ACC_DONE + 1;
-  static constexpr int NUM_BARS = B_DRAIN + 1;
+  static constexpr int B_DS_DONE = B_DP_FULL + 1;  // two: dS(t) in slot t % 2
+  static constexpr int B_DQ_DONE = B_DS_DONE + 2;  // two: TS_dQ(t) finished, slot t % 2
+  static constexpr int B_ACC_DONE = B_DQ_DONE + 2;
+  static constexpr int B_DRAIN = B_ACC_DONE + 1;   // one per issuing thread
+  static constexpr int NUM_BARS = B_DRAIN + 2;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
   // TMEM columns: S0, S1 (dS over the first 64 of the tile's buffer), dP, dQ
@@ -507,7 +514,7 @@ struct DqCfg {
 
 // One CTA per (head, 128-query tile m), in tile_of's order.
 template <int D, int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kDqThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
@@ -553,9 +560,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(C::B_S_FULL), 1);
     mbar_init(bar(C::B_S_FULL + 1), 1);
     mbar_init(bar(C::B_DP_FULL), 1);
-    mbar_init(bar(C::B_DS_DONE), kElemThreads);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(C::B_DS_DONE + i), kElemThreads);
+      mbar_init(bar(C::B_DQ_DONE + i), 1);
+    }
     mbar_init(bar(C::B_ACC_DONE), 1);
     mbar_init(bar(C::B_DRAIN), 1);
+    mbar_init(bar(C::B_DRAIN + 1), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -628,17 +639,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       bool ok = wait(C::B_A_FULL, 0) && issue_s(0) && issue_dp(0) && (count < 2 || issue_s(1));
-      for (int t = 0; ok && t < count; ++t) {
-        if (!wait(C::B_DS_DONE, t & 1)) break;
-        tc_fence_after();
-        mma_acc<D>(tmem + C::TM_DQ, tmem + C::TM_S0 + 128u * (t & 1), k_of(t), t > 0);
-        tc_commit(bar(C::B_K_EMPTY + t % C::KS));
-        if (t + 1 < count && !issue_dp(t + 1)) break;
-        if (t + 2 < count && !issue_s(t + 2)) break;
+      for (int t = 0; ok && t + 1 < count; ++t) {
+        // dP(t+1) once the warps have turned dP(t) into dS(t); S(t+2) once
+        // TS_dQ(t) has read dS(t) out of S buffer t % 2.
+        if (!wait(C::B_DS_DONE + (t & 1), (t >> 1) & 1) || !issue_dp(t + 1)) break;
+        if (t + 2 < count &&
+            (!wait(C::B_DQ_DONE + (t & 1), (t >> 1) & 1) || !issue_s(t + 2)))
+          break;
       }
-      tc_commit(bar(C::B_ACC_DONE));
       tc_commit(bar(C::B_DRAIN));
       mbar_wait_unwind_b(bar(C::B_DRAIN), 0);
+    }
+  } else if (warp == kWarpAcc) {
+    // ======================= accumulating product =======================
+    if (lane == 0) {
+      auto k_of = [&](int t) { return sbase + C::OFF_K + (t % C::KS) * C::TILE; };
+      for (int t = 0; t < count; ++t) {
+        if (!mbar_wait(bar(C::B_DS_DONE + (t & 1)), (t >> 1) & 1, abort_flag, args.status)) break;
+        tc_fence_after();
+        mma_acc<D>(tmem + C::TM_DQ, tmem + C::TM_S0 + 128u * (t & 1), k_of(t), t > 0);
+        tc_commit(bar(C::B_DQ_DONE + (t & 1)));
+        tc_commit(bar(C::B_K_EMPTY + t % C::KS));
+      }
+      tc_commit(bar(C::B_ACC_DONE));
+      tc_commit(bar(C::B_DRAIN + 1));
+      mbar_wait_unwind_b(bar(C::B_DRAIN + 1), 0);
     }
   } else {
     // ======================= elementwise / epilogue =======================
@@ -719,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(C::B_DS_DONE));
+      mbar_arrive(bar(C::B_DS_DONE + (t & 1)));
     }
 
     if (ok) {
@@ -797,7 +822,7 @@ cudaError_t launch_impl(const BwdMaps& m, const BwdArgs& a, cudaStream_t stream)
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   fa_bwd_dq_kernel<D, MODE>
-      <<<blocks, kThreads, DqCfg<D>::SMEM_BYTES, stream>>>(m.q, m.k, m.v, m.dout, a);
+      <<<blocks, kDqThreads, DqCfg<D>::SMEM_BYTES, stream>>>(m.q, m.k, m.v, m.dout, a);
   return cudaGetLastError();
 }
 
