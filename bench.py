@@ -608,11 +608,38 @@ def run_gpu(args, rank, world, dist):
             ev_out[i].record(s_out)
     torch.cuda.synchronize()
     dt = max_over_ranks(time.perf_counter() - t0, dist)
+    # The host link alone, for context: one step's input copy and output
+    # copy, each timed by itself (after the timed region).
+    h2d_b = 3 * pc.q.numel() * 2
+    d2h_b = o.numel() * 2 + lse.numel() * 4
+
+    def _copy_ms(fn, n=5):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    def _h2d():
+        for dst, src in zip(din[0], (hq, hk, hv)):
+            dst.copy_(src, non_blocking=True)
+
+    def _d2h():
+        ho[0].copy_(dout[0][0], non_blocking=True)
+        hl[0].copy_(dout[0][1], non_blocking=True)
+
+    h2d_gbs = h2d_b / (_copy_ms(_h2d) * 1e-3) / 1e9
+    d2h_gbs = d2h_b / (_copy_ms(_d2h) * 1e-3) / 1e9
     del din, dout
     e2e = {"value": world * flops * n_e2e / dt / 1e12, "unit": "TFLOP/s",
-           "h2d_bytes_per_step": 3 * pc.q.numel() * 2,
-           "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4,
-           "steps": n_e2e, "pipelined": "2 buffer sets, copies on their own streams"}
+           "h2d_bytes_per_step": h2d_b,
+           "d2h_bytes_per_step": d2h_b,
+           "steps": n_e2e, "pipelined": "2 buffer sets, copies on their own streams",
+           "h2d_gbs_alone": h2d_gbs, "d2h_gbs_alone": d2h_gbs}
 
     if rank != 0:
         return 0
