@@ -231,3 +231,34 @@ def test_varlen_bad_offsets_reported(fa):
     fa.fa_fwd_varlen(q, k, v, bad, 150, case.scale, True)
     assert fa.fa_check_device_status() == fa.FA_ERR_DEVICE_BOUNDS
     assert fa.fa_check_device_status() == fa.FA_OK  # the word was cleared
+
+
+# --- run-to-run determinism -------------------------------------------------------
+
+def test_forward_deterministic(fa):
+    """No atomics and a fixed merge order in every path: repeated launches on
+    the same inputs give the same bits (dense causal with a window edge,
+    packed sequences, and the fp32 path)."""
+    case = inp.dense(1, 8, 3000, 128, seed=31, causal=True, qk_std=3.0)
+    q, k, v = _dense_gpu(case)
+    runs = [fa.fa_fwd(q, k, v, case.scale, True) for _ in range(3)]
+    runs += [fa.fa_fwd(q, k, v, case.scale, True) for _ in range(2)]
+    for o, lse in runs[1:]:
+        assert torch.equal(o, runs[0][0]) and torch.equal(lse, runs[0][1])
+    wins = [fa.fa_fwd_window(q, k, v, 700, case.scale) for _ in range(3)]
+    for o, lse in wins[1:]:
+        assert torch.equal(o, wins[0][0]) and torch.equal(lse, wins[0][1])
+
+    vcase = inp.varlen([1, 129, 700, 2048, 5], H=4, D=64, seed=32, causal=True)
+    vq, vk, vv, cu = vcase.q.cuda(), vcase.k.cuda(), vcase.v.cuda(), vcase.cu_seqlens.cuda()
+    vruns = [fa.fa_fwd_varlen(vq, vk, vv, cu, vcase.max_seqlen, vcase.scale, True)
+             for _ in range(3)]
+    for o, lse in vruns[1:]:
+        assert torch.equal(o, vruns[0][0]) and torch.equal(lse, vruns[0][1])
+
+    fcase = inp.dense(2, 3, 700, 64, seed=33, causal=True, dtype=torch.float32)
+    fq, fk, fv = _dense_gpu(fcase)
+    fruns = [fa.fa_fwd_f32(fq, fk, fv, fcase.scale, True) for _ in range(3)]
+    for o, lse in fruns[1:]:
+        assert torch.equal(o, fruns[0][0]) and torch.equal(lse, fruns[0][1])
+    assert fa.fa_check_device_status() == fa.FA_OK
