@@ -12,6 +12,18 @@
 // pads the ragged tail).  The output division o / d and the log-sum-exp are
 // deferred to the epilogue.  S and P live only in tensor memory.
 //
+// Reference maximum.  A state (m, d, o) stands for the same element of the
+// monoid for any reference m (d 2^m and o 2^m do not change; "The Merge, and
+// the Twist"), so a row moves its reference only when a tile's maximum
+// exceeds it by more than kRescaleLog2 = 8 (base 2): every weight p =
+// 2^(sigma - m) stays at most 2^8, which fp32 d, o and bf16 P hold, and the
+// O rescale between two P V products, with its wait, is needed on few tiles.
+// P is rounded to bf16 for the product; a weight that is not 1 then loses up
+// to 2^-9 of itself, which for a row whose weight sits on one key would bias
+// O by that much.  So O is divided by d less, per tile, what rounding took
+// from the tile's largest weight (that weight is recomputed exactly as the
+// tile loop computes it); the log-sum-exp uses d itself.
+//
 // Roles (352 threads):
 //   warp 0      TMA producer: Q once, then K and V tiles into two rings of
 //               stages, in the order the MMA issuer consumes them
@@ -30,19 +42,23 @@
 //               N = 128, the pipe's own rate.
 //   warps 2..5  softmax: thread t owns row 32*(warp%4) + lane; per tile it
 //               loads its raw S row (then releases the S buffer), masks,
-//               takes the row max (3-input max instructions, four independent
-//               chains), computes p = 2^(s c - m_new) with one packed fused
+//               takes the row max (3-input max instructions, sixteen
+//               independent chains), moves its reference maximum if the
+//               tile's exceeds it by more than 8, computes p = 2^(s c - m)
+//               with one packed fused
 //               multiply-add per pair of columns, rounds P to bf16 into TMEM
 //               buffer j % 4 (free: S_j was issued after the product that
 //               last read it had finished), sums p with packed adds, leaves
-//               the rescale factor alpha_j = 2^(m_old - m_new) in shared
-//               memory and signals P_j.
+//               the rescale factor alpha_j = 2^(m_old - m_new) (1 unless the
+//               reference moved) in shared memory and signals P_j.
 //   warps 7..10 correction: thread t owns the same row as its softmax thread;
-//               per tile, when a row of its warp raised its maximum, it waits
-//               for P_{j-1} V_{j-1} and rescales its O row in TMEM by alpha_j
+//               per tile, when a row of its warp moved its reference
+//               maximum, it waits for P_{j-1} V_{j-1} and rescales its O row
+//               in TMEM by alpha_j
 //               (the rescale half of the merge), then signals that O is ready
 //               for P_j V_j.  The softmax warps never wait on the products.
-//               Epilogue: O / d in fp32, LSE = ln2 (m + log2 d), stores.
+//               Epilogue (softmax warps): O / d' in fp32 (d' = d less the
+//               largest weights' rounding), LSE = ln2 (m + log2 d), stores.
 //
 // Shared memory (1024-byte aligned): Q tile, KS K tiles, VS V tiles, the
 // mbarriers, the rescale factors (NP x 128 floats).  A 128 x D bf16 tile is stored as D/64 column halves of
@@ -60,6 +76,10 @@
 #include "fa_internal.h"
 
 namespace fa {
+
+// A row's reference maximum moves only when a tile's maximum exceeds it by
+// more than this (base-2 units).
+constexpr float kRescaleLog2 = 8.f;
 
 template <int D>
 struct TcCfg {
@@ -395,8 +415,9 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
     // -inf, which c = 1 applied to (0 | -inf) reproduces without 0 * inf.
     const bool zero_scale = args.scale_log2 == 0.f;
     const float c = zero_scale ? 1.f : args.scale_log2;
-    float m = -INFINITY;
-    float dsum = 0.f;
+    float m = -INFINITY;  // reference maximum (base 2)
+    float dsum = 0.f;     // sum of the weights (for the log-sum-exp)
+    float dnorm = 0.f;    // the same less the largest weights' rounding (divides O)
     bool ok = true;
     float* alpha_s = reinterpret_cast<float*>(smem + C::OFF_ALPHA);
 
@@ -449,8 +470,9 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
       const float r0 = fmax3(q[0], q[1], q[2]), r1 = fmax3(q[3], q[4], q[5]);
       const float r2 = fmax3(q[6], q[7], q[8]), r3 = fmax3(q[9], q[10], q[11]);
       const float r4 = fmax3(q[12], q[13], q[14]);
-      const float mx = fmaxf(fmax3(r0, r1, r2), fmax3(r3, r4, q[15])) * c;
-      const float m_new = fmaxf(m, mx);
+      const float tmax = fmaxf(fmax3(r0, r1, r2), fmax3(r3, r4, q[15]));
+      const float mx = tmax * c;
+      const float m_new = (mx > m + kRescaleLog2) ? mx : m;  // also moves off -inf
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = (m_new == m) ? 1.f : ex2_approx(m - m_use);
       const uint32_t p_t = tmem + lane_off + C::TMEM_P + 64u * (j % C::NP);
@@ -469,6 +491,11 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
         tmem_st32(p_t + 32u * h, pk);
       }
       const float2 aa = __fadd2_rn(a0, a1);
+      // The tile's largest weight as the loop computed it (same fused
+      // multiply-add, same ex2) and what bf16 rounding took from it.
+      const float pm = ex2_approx(fmaf(tmax, c, -m_use));
+      const float pm_dropped = pm - __uint_as_float(pack_bf16x2(pm, 0.f) << 16);
+      dnorm = dnorm * alpha + ((aa.x + aa.y) - pm_dropped);
       dsum = dsum * alpha + (aa.x + aa.y);
       m = m_new;
 
@@ -483,7 +510,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
                                ((n_kv - 1) / C::NP) & 1, abort_flag, args.status);
       if (!__any_sync(0xffffffffu, !w)) {
         tc_fence_after();
-        const float inv = dsum > 0.f ? 1.f / dsum : 0.f;
+        const float inv = dnorm > 0.f ? 1.f / dnorm : 0.f;
         const float lse = dsum > 0.f ? (m + log2f(dsum)) * 0.69314718055994530942f : -INFINITY;
         const bool store = qpos < L;
         size_t orow, lidx;
