@@ -15,16 +15,21 @@
 // Reference maximum.  A state (m, d, o) stands for the same element of the
 // monoid for any reference m (d 2^m and o 2^m do not change; "The Merge, and
 // the Twist"), so a row moves its reference only when a tile's maximum
-// exceeds it by more than kRescaleLog2 = 8 (base 2): every weight p =
-// 2^(sigma - m) stays at most 2^8, which fp32 d, o and bf16 P hold, and the
-// O rescale between two P V products, with its wait, is needed on few tiles.
+// exceeds it by more than kRescaleLog2 = 32 (base 2).  The reference never
+// exceeds the running maximum, so d >= 1 as with the exact maximum
+// ("Numerical Analysis of the FlashAttention Kernel"), and every weight p =
+// 2^(sigma - m) is at most 2^32: fp32 d and o and bf16 P hold that as long
+// as N * 2^32 * max|V| stays below fp32's range (|V| < 2^82 at N = 2^14).
+// The O rescale between two P V products, which waits for the earlier one,
+// is then needed almost never after a row's first tile, even for scores
+// with a spread of many units (a warp rescales if any of its 32 rows moved).
 // P is rounded to bf16 for the product; a weight that is not 1 then loses up
 // to 2^-9 of itself, which for a row whose weight sits on one key would bias
 // O by that much.  So O is divided by d less, per tile, what rounding took
 // from the tile's largest weight (that weight is recomputed exactly as the
 // tile loop computes it); the log-sum-exp uses d itself.
 //
-// Roles (352 threads):
+// Roles (224 threads):
 //   warp 0      TMA producer: Q once, then K and V tiles into two rings of
 //               stages, in the order the MMA issuer consumes them
 //               (K_0, K_1, then V_j, K_{j+2} for each j).
@@ -35,7 +40,7 @@
 //               softmax of tile j.
 //   warp 6      PV issuer (one thread): O += P_j V_j with P_j read from TMEM
 //               (TS form, P_j in TMEM buffer j % 4) once the softmax has
-//               written P_j and the correction warps have rescaled O.
+//               written P_j (and, on the rare tiles that need it, rescaled O).
 //               Two issuing threads keep the tensor pipe fed: one thread
 //               issues an M=128 K=16 product about every 80-90 cycles at best,
 //               while two threads together reach one per ~65 cycles at
@@ -44,24 +49,20 @@
 //               loads its raw S row (then releases the S buffer), masks,
 //               takes the row max (3-input max instructions, sixteen
 //               independent chains), moves its reference maximum if the
-//               tile's exceeds it by more than 8, computes p = 2^(s c - m)
-//               with one packed fused
-//               multiply-add per pair of columns, rounds P to bf16 into TMEM
-//               buffer j % 4 (free: S_j was issued after the product that
-//               last read it had finished), sums p with packed adds, leaves
-//               the rescale factor alpha_j = 2^(m_old - m_new) (1 unless the
-//               reference moved) in shared memory and signals P_j.
-//   warps 7..10 correction: thread t owns the same row as its softmax thread;
-//               per tile, when a row of its warp moved its reference
-//               maximum, it waits for P_{j-1} V_{j-1} and rescales its O row
-//               in TMEM by alpha_j
-//               (the rescale half of the merge), then signals that O is ready
-//               for P_j V_j.  The softmax warps never wait on the products.
-//               Epilogue (softmax warps): O / d' in fp32 (d' = d less the
-//               largest weights' rounding), LSE = ln2 (m + log2 d), stores.
+//               tile's exceeds it by more than kRescaleLog2, computes p =
+//               2^(s c - m) with one packed fused multiply-add per pair of
+//               columns, rounds P to bf16 into TMEM buffer j % 4 (free: S_j
+//               was issued after the product that last read it had
+//               finished), sums p with packed adds, and, on the rare tiles
+//               where a row of the warp moved its reference, waits for
+//               P_{j-1} V_{j-1} and rescales its O row in TMEM by alpha_j =
+//               2^(m_old - m_new) (the rescale half of the merge); then it
+//               signals P_j.
+//               Epilogue: O / d' in fp32 (d' = d less the largest weights'
+//               rounding), LSE = ln2 (m + log2 d), stores.
 //
 // Shared memory (1024-byte aligned): Q tile, KS K tiles, VS V tiles, the
-// mbarriers, the rescale factors (NP x 128 floats).  A 128 x D bf16 tile is stored as D/64 column halves of
+// mbarriers.  A 128 x D bf16 tile is stored as D/64 column halves of
 // 128 rows x 128 bytes, 128-byte swizzled (the TMA box layout and the
 // canonical K-major / MN-major tcgen05 operand layouts).
 // Tensor memory (512 columns): S [0,128), O [128, 128 + D), P_0..P_3 at
@@ -79,7 +80,7 @@ namespace fa {
 
 // A row's reference maximum moves only when a tile's maximum exceeds it by
 // more than this (base-2 units).
-constexpr float kRescaleLog2 = 8.f;
+constexpr float kRescaleLog2 = 32.f;
 
 template <int D>
 struct TcCfg {
@@ -107,19 +108,16 @@ struct TcCfg {
   static constexpr int B_S_FREE = B_S_FULL + 1;  // S loaded by the softmax warps
   static constexpr int B_P_FULL = B_S_FREE + 1;  // one per P buffer
   static constexpr int B_PV_DONE = B_P_FULL + NP;
-  static constexpr int B_O_READY = B_PV_DONE + NP;  // O rescaled for P_j V_j
-  static constexpr int B_DRAIN = B_O_READY + NP;  // one per issuing thread
+  static constexpr int B_DRAIN = B_PV_DONE + NP;  // one per issuing thread
   static constexpr int NUM_BARS = B_DRAIN + 2;
-  static constexpr uint32_t OFF_ALPHA = OFF_BAR + NUM_BARS * 8;
-  static constexpr uint32_t OFF_MISC = OFF_ALPHA + NP * 128 * 4;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t TMEM_S = 0;
   static constexpr uint32_t TMEM_O = 128;
   static constexpr uint32_t TMEM_P = 256;  // buffer i at TMEM_P + 64 i
-  static constexpr int THREADS = 352;
+  static constexpr int THREADS = 224;
   static constexpr int WARP_PV = 6;
-  static constexpr int WARP_CORR = 7;  // warps 7..10
   static constexpr int SOFTMAX_THREADS = 128;
 };
 
@@ -253,7 +251,6 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
     for (int b = 0; b < C::NP; ++b) {
       mbar_init(bar(C::B_P_FULL + b), C::SOFTMAX_THREADS);
       mbar_init(bar(C::B_PV_DONE + b), 1);
-      mbar_init(bar(C::B_O_READY + b), C::SOFTMAX_THREADS);
     }
     mbar_init(bar(C::B_DRAIN), 1);
     mbar_init(bar(C::B_DRAIN + 1), 1);
@@ -349,8 +346,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
       for (int j = 0; j < n_kv; ++j) {
         const int sv = j % C::VS;
         if (!mbar_wait(bar(C::B_P_FULL + j % C::NP), (j / C::NP) & 1, abort_flag, args.status) ||
-            !mbar_wait(bar(C::B_V_FULL + sv), (j / C::VS) & 1, abort_flag, args.status) ||
-            !mbar_wait(bar(C::B_O_READY + j % C::NP), (j / C::NP) & 1, abort_flag, args.status))
+            !mbar_wait(bar(C::B_V_FULL + sv), (j / C::VS) & 1, abort_flag, args.status))
           break;
         tc_fence_after();
         const uint32_t v_s = sbase + C::OFF_V + sv * C::TILE_BYTES;
@@ -369,42 +365,6 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
       tc_commit(bar(C::B_DRAIN + 1));
       mbar_wait_unwind(bar(C::B_DRAIN + 1), 0);
     }
-  } else if (warp >= C::WARP_CORR) {
-    // ======================= O correction =======================
-    const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;
-    const uint32_t o_t = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + C::TMEM_O;
-    const float* alpha_s = reinterpret_cast<const float*>(smem + C::OFF_ALPHA);
-    for (int j = 0; j < n_kv; ++j) {
-      const int pb = j % C::NP;
-      const bool w = mbar_wait(bar(C::B_P_FULL + pb), (j / C::NP) & 1, abort_flag, args.status);
-      if (__any_sync(0xffffffffu, !w)) break;
-      const float alpha = alpha_s[pb * 128 + r];
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        // o <- alpha * o between P_{j-1} V_{j-1} and P_j V_j.
-        const bool w2 = mbar_wait(bar(C::B_PV_DONE + (j - 1) % C::NP), ((j - 1) / C::NP) & 1,
-                                  abort_flag, args.status);
-        if (__any_sync(0xffffffffu, !w2)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 64) {
-          uint32_t ov[64];
-          tmem_ld64(o_t + c0, ov);
-          uint32_t lo[32], hi[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            lo[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-            hi[i] = __float_as_uint(__uint_as_float(ov[32 + i]) * alpha);
-          }
-          tmem_st32(o_t + c0, lo);
-          tmem_st32(o_t + c0 + 32, hi);
-        }
-        tmem_st_wait();
-      }
-      tc_fence_before();
-      mbar_arrive(bar(C::B_O_READY + pb));
-    }
-    tc_fence_before();
   } else {
     // ======================= softmax / epilogue =======================
     const int quarter = warp & 3;
@@ -419,7 +379,6 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
     float dsum = 0.f;     // sum of the weights (for the log-sum-exp)
     float dnorm = 0.f;    // the same less the largest weights' rounding (divides O)
     bool ok = true;
-    float* alpha_s = reinterpret_cast<float*>(smem + C::OFF_ALPHA);
 
     for (int j = 0; j < n_kv; ++j) {
       const uint32_t s_t = tmem + lane_off + C::TMEM_S;
@@ -499,7 +458,26 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
       dsum = dsum * alpha + (aa.x + aa.y);
       m = m_new;
 
-      alpha_s[(j % C::NP) * 128 + r] = alpha;
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        // o <- alpha * o between P_{j-1} V_{j-1} and P_j V_j (rare: only
+        // when a row of this warp moved its reference maximum).
+        const bool w2 = mbar_wait(bar(C::B_PV_DONE + (j - 1) % C::NP), ((j - 1) / C::NP) & 1,
+                                  abort_flag, args.status);
+        if (__any_sync(0xffffffffu, !w2)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t o_t = tmem + lane_off + C::TMEM_O;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t ov[32];
+          tmem_ld32(o_t + c0, ov);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+          tmem_st32(o_t + c0, ov);
+        }
+      }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(C::B_P_FULL + j % C::NP));

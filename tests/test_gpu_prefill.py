@@ -262,3 +262,37 @@ def test_forward_deterministic(fa):
     for o, lse in fruns[1:]:
         assert torch.equal(o, fruns[0][0]) and torch.equal(lse, fruns[0][1])
     assert fa.fa_check_device_status() == fa.FA_OK
+
+
+# --- the reference maximum: moves, and range -----------------------------------------
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_reference_moves(fa, causal):
+    """Keys that grow along the sequence make later tiles' maxima exceed the
+    reference a row set on its first tile by far more than the move
+    threshold, so rows move their reference (and warps rescale O) many
+    times; the result still matches the oracle."""
+    case = inp.dense(1, 2, 1100, 128, seed=41, causal=causal, qk_std=3.0)
+    ramp = (1.0 + 4.0 * torch.arange(1100, dtype=torch.float32) / 1100).view(1, 1, -1, 1)
+    k = (case.k.float() * ramp).to(torch.bfloat16)
+    o, lse = fa.fa_fwd(case.q.cuda(), k.cuda(), case.v.cuda(), case.scale, causal)
+    O, L = ora.attention_ref(case.q, k, case.v, case.scale, causal)
+    check_o_bf16(np64(o), O, "moving reference")
+    check_lse(np64(lse), L)
+    o32, lse32 = fa.fa_fwd_ex(case.q.cuda(), k.cuda(), case.v.cuda(), case.scale, causal,
+                              o_dtype=torch.float32)
+    check_o_f32(np64(o32), O, "moving reference, fp32 out")
+
+
+def test_large_values_in_range(fa):
+    """|V| around 1e15 at N = 2048 sits far inside the range the lagging
+    reference keeps (N * 2^32 * max|V| below fp32's limit): finite outputs
+    within the relative tolerance of the oracle."""
+    case = inp.dense(1, 2, 2048, 128, seed=42, causal=True, qk_std=3.0, v_std=1e15)
+    o, lse = fa.fa_fwd_ex(case.q.cuda(), case.k.cuda(), case.v.cuda(), case.scale, True,
+                          o_dtype=torch.float32)
+    O, L = ora.attention_ref(case.q, case.k, case.v, case.scale, True)
+    o = np64(o)
+    assert np.isfinite(o).all()
+    assert np.abs(o - O).max() <= 1e-2 * np.abs(O).max()
+    check_lse(np64(lse), L)
