@@ -63,6 +63,10 @@ extern "C" {
  *   B, H, N >= 1; D in {64, 128}; causal != 0 hides keys j > i.
  * Runs the tcgen05 / TMEM / TMA kernel; accumulation in fp32, the softmax
  * weights rounded to bf16 (nearest-even) before the P V product.
+ * Range: a row's weights are taken against a reference maximum that may lag
+ * the running maximum by up to 2^32 (base 2), so the unnormalised output
+ * stays finite while N * 2^32 * max|v| is below fp32's range (|v| < 2^82 at
+ * N = 2^14); the same holds for fa_fwd_ex, fa_fwd_window and fa_fwd_varlen.
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int N, int D, float scale, int causal, void* stream);
