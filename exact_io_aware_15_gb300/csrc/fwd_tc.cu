@@ -407,10 +407,16 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
       if ((args.causal && j0 + j == mb) || kbase + C::BN > L || win_edge) {
         int lim = L - kbase;  // keys [lo, lim) of the tile are visible
         if (args.causal) lim = min(lim, qpos - kbase + 1);
-        const int lo = args.window > 0 ? qpos - args.window + 1 - kbase : 0;
+        if (args.window > 0) {
+          const int lo = qpos - args.window + 1 - kbase;
 #pragma unroll
-        for (int i = 0; i < 128; ++i)
-          if (i >= lim || i < lo) t[i] = -INFINITY;
+          for (int i = 0; i < 128; ++i)
+            if (i >= lim || i < lo) t[i] = -INFINITY;
+        } else {
+          // Without a window the visible keys are a prefix: one compare.
+#pragma unroll
+          for (int i = 0; i < 128; ++i) t[i] = i < lim ? t[i] : -INFINITY;
+        }
       }
       if (zero_scale) {
 #pragma unroll
