@@ -129,14 +129,16 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (BH == 0 || N == 0) return FA_OK;
   rc = get_encoder();
   if (rc != FA_OK) return rc;
-  fa::TcMaps maps;
+  fa::TcMaps maps{};
   const uint64_t rs = static_cast<uint64_t>(D) * 2u;
   const uint64_t hs = rs * static_cast<uint64_t>(N);
   if (encode_map(&maps.q, q, D, N, BH, rs, hs, 128u, 1u) != FA_OK ||
       encode_map(&maps.k, k, D, N, BH, rs, hs, 128u, 1u) != FA_OK ||
-      encode_map(&maps.v, v, D, N, BH, rs, hs, 128u, 1u) != FA_OK)
+      encode_map(&maps.v, v, D, N, BH, rs, hs, 128u, 1u) != FA_OK ||
+      (!o_f32 && D == 128 && encode_map(&maps.o, o, D, N, BH, rs, hs, 32u, 1u) != FA_OK))
     return FA_ERR_DRIVER;
   fa::TcFwdArgs a{};
+  a.o_tma = (!o_f32 && D == 128) ? 1 : 0;
   a.H = H;
   a.N = N;
   a.num_mblocks = static_cast<int>(mblocks);
@@ -371,14 +373,16 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
   if (SH == 0 || total_tokens == 0 || max_seqlen == 0) return FA_OK;
   rc = get_encoder();
   if (rc != FA_OK) return rc;
-  fa::TcMaps maps;
+  fa::TcMaps maps{};
   const uint64_t hs = static_cast<uint64_t>(D) * 2u;
   const uint64_t ts = hs * static_cast<uint64_t>(H);
   if (encode_map(&maps.q, q, D, H, total_tokens, hs, ts, 1u, 128u) != FA_OK ||
       encode_map(&maps.k, k, D, H, total_tokens, hs, ts, 1u, 128u) != FA_OK ||
-      encode_map(&maps.v, v, D, H, total_tokens, hs, ts, 1u, 128u) != FA_OK)
+      encode_map(&maps.v, v, D, H, total_tokens, hs, ts, 1u, 128u) != FA_OK ||
+      (D == 128 && encode_map(&maps.o, o, D, H, total_tokens, hs, ts, 1u, 32u) != FA_OK))
     return FA_ERR_DRIVER;
   fa::TcFwdArgs a{};
+  a.o_tma = D == 128 ? 1 : 0;
   a.H = H;
   a.N = 0;
   a.num_mblocks = static_cast<int>(mblocks);

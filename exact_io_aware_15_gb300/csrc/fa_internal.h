@@ -20,13 +20,15 @@ struct TcFwdArgs {
   int max_seqlen;         // varlen: bound checked against every length
   void* o;
   int o_f32;         // 1: o is fp32, 0: bf16
+  int o_tma;         // 1: bf16 O (D = 128) is stored through TcMaps::o (32-row boxes)
   float* lse;
   unsigned int* status;
 };
 
-// Tensor maps of Q, K, V for the tensor-core kernel (3-D, 128-byte swizzle).
+// Tensor maps of Q, K, V (128-row boxes) and of O (32-row boxes, used when
+// TcFwdArgs::o_tma is set) for the tensor-core kernel (3-D, 128-byte swizzle).
 struct TcMaps {
-  CUtensorMap q, k, v;
+  CUtensorMap q, k, v, o;
 };
 
 cudaError_t launch_fwd_tc(const TcMaps& maps, const TcFwdArgs& a, int D, int grid_x,

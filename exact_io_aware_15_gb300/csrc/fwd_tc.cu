@@ -59,7 +59,9 @@
 //               2^(m_old - m_new) (the rescale half of the merge); then it
 //               signals P_j.
 //               Epilogue: O / d' in fp32 (d' = d less the largest weights'
-//               rounding), LSE = ln2 (m + log2 d), stores.
+//               rounding), LSE = ln2 (m + log2 d), stores (bf16 O at
+//               D = 128: staged in Q's buffer, one TMA store per warp and
+//               64-column half).
 //
 // Shared memory (1024-byte aligned): Q tile, KS K tiles, VS V tiles, the
 // mbarriers.  A 128 x D bf16 tile is stored as D/64 column halves of
@@ -142,7 +144,8 @@ template <int D>
 __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const TcFwdArgs args) {
+                     const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_o, const TcFwdArgs args) {
   using C = TcCfg<D>;
   extern __shared__ uint8_t smem_raw[];
 
@@ -507,6 +510,49 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
           lidx = orow;
         }
         const uint32_t o_t = tmem + lane_off + C::TMEM_O;
+        const int wrow0 = mb * C::BM + quarter * 32;  // this warp's first row
+        if (D == 128 && args.o_tma && (varlen ? wrow0 + 32 <= L : wrow0 < L)) {
+          // bf16 O through shared memory and one TMA store per 64-column half
+          // and warp: the rows are staged in Q's buffer (no product reads Q
+          // any more) in the 128-byte-swizzled box layout, and the tensor
+          // map clips rows past the end of a dense sequence.  (A packed
+          // sequence's last rows are followed by the next sequence's, so a
+          // warp with rows past its end stores row by row below.)  At
+          // D = 64 a row is 128 bytes and the row-by-row stores are faster.
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 64) {
+            uint32_t ov[64];
+            tmem_ld64(o_t + c0, ov);
+            uint8_t* row = smem + C::OFF_Q + (c0 / 64) * C::HALF_BYTES + r * 128;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+              uint4 u;
+              u.x = pack_bf16x2(__uint_as_float(ov[8 * ch + 0]) * inv,
+                                __uint_as_float(ov[8 * ch + 1]) * inv);
+              u.y = pack_bf16x2(__uint_as_float(ov[8 * ch + 2]) * inv,
+                                __uint_as_float(ov[8 * ch + 3]) * inv);
+              u.z = pack_bf16x2(__uint_as_float(ov[8 * ch + 4]) * inv,
+                                __uint_as_float(ov[8 * ch + 5]) * inv);
+              u.w = pack_bf16x2(__uint_as_float(ov[8 * ch + 6]) * inv,
+                                __uint_as_float(ov[8 * ch + 7]) * inv);
+              *reinterpret_cast<uint4*>(row + ((ch ^ (r & 7)) << 4)) = u;
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+#pragma unroll
+            for (int c = 0; c < C::HALVES; ++c) {
+              const uint32_t src = sbase + C::OFF_Q + c * C::HALF_BYTES + quarter * 32 * 128;
+              if (varlen)
+                tma_store_3d(&tm_o, src, c * 64, h, tok0 + wrow0);
+              else
+                tma_store_3d(&tm_o, src, c * 64, wrow0, bh);
+            }
+            tma_store_commit_and_wait_read();
+          }
+          __syncwarp();
+        } else {
         // 64 columns per TMEM load (one wait each), then the stores.
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 64) {
@@ -538,6 +584,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
               }
             }
           }
+        }
         }
         if (store) args.lse[lidx] = lse;
       }
@@ -571,7 +618,8 @@ static cudaError_t launch_tc_impl(const TcMaps& maps, const TcFwdArgs& a, int gr
     if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_release);
   }
   dim3 grid(static_cast<unsigned>(grid_x * a.num_mblocks));
-  fa_fwd_tc_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(maps.q, maps.k, maps.v, a);
+  fa_fwd_tc_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(maps.q, maps.k, maps.v, maps.o,
+                                                                   a);
   return cudaGetLastError();
 }
 
