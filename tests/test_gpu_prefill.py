@@ -175,6 +175,45 @@ def test_empty_and_invalid(fa):
     assert (o == 7.0).all()  # nothing launched, output untouched
 
 
+def test_output_tail_untouched(fa):
+    """The O stores stop at the tensor's end: with O the head of a larger
+    buffer, rows past the last sequence (dense N = 300 and 129: the last
+    tile's warps straddle or pass N; varlen: a packed tail) leave the rest of
+    the buffer as it was, and the outputs still match the oracle."""
+    sentinel = 0x7FC1  # a NaN bit pattern no store produces
+    for (B, H, N, D) in [(1, 2, 300, 128), (2, 1, 129, 128), (1, 1, 300, 64)]:
+        case = inp.dense(B, H, N, D, seed=N + D, causal=True)
+        q, k, v = _dense_gpu(case)
+        n = B * H * N * D
+        buf = torch.full((n + 8192,), sentinel, dtype=torch.int16, device="cuda")
+        o = buf[:n].view(torch.bfloat16).view(B, H, N, D)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+        fa.fa_fwd(q, k, v, case.scale, True, o=o, lse=lse)
+        torch.cuda.synchronize()
+        assert bool((buf[n:] == sentinel).all()), f"store past the end {B, H, N, D}"
+        O, L = ora.attention_ref(case.q, case.k, case.v, case.scale, True)
+        check_o_bf16(np64(o), O, f"dense {B, H, N, D}")
+        check_lse(np64(lse), L)
+    for D in (64, 128):
+        case = inp.varlen([300, 129, 37], H=2, D=D, seed=3 * D, causal=True)
+        q, k, v = case.q.cuda(), case.k.cuda(), case.v.cuda()
+        T = sum(case.meta["lens"])
+        n = T * 2 * D
+        buf = torch.full((n + 8192,), sentinel, dtype=torch.int16, device="cuda")
+        o = buf[:n].view(torch.bfloat16).view(T, 2, D)
+        lse = torch.empty((2, T), dtype=torch.float32, device="cuda")
+        fa.fa_fwd_varlen(q, k, v, case.cu_seqlens.cuda(), case.max_seqlen, case.scale, True,
+                         o=o, lse=lse)
+        torch.cuda.synchronize()
+        assert bool((buf[n:] == sentinel).all()), f"varlen store past the end D={D}"
+        ref = ora.varlen_ref(case.q, case.k, case.v, case.cu_seqlens, case.scale, True)
+        cuh = case.cu_seqlens.tolist()
+        for s_, (O, L) in ref.items():
+            check_o_bf16(np64(o[cuh[s_]:cuh[s_ + 1]]), O, f"varlen seq {s_} D={D}")
+            check_lse(np64(lse[:, cuh[s_]:cuh[s_ + 1]]), L)
+    assert fa.fa_check_device_status() == fa.FA_OK
+
+
 # --- varlen -------------------------------------------------------------------------
 
 @pytest.mark.parametrize("D", [64, 128])
