@@ -553,38 +553,40 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
           }
           __syncwarp();
         } else {
-        // 64 columns per TMEM load (one wait each), then the stores.
+          // 64 columns per TMEM load (one wait each), then the stores.
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 64) {
-          uint32_t ov[64];
-          tmem_ld64(o_t + c0, ov);
-          if (store) {
-            if (args.o_f32) {
-              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(args.o) + orow * D + c0);
+          for (int c0 = 0; c0 < D; c0 += 64) {
+            uint32_t ov[64];
+            tmem_ld64(o_t + c0, ov);
+            if (store) {
+              if (args.o_f32) {
+                float4* dst =
+                    reinterpret_cast<float4*>(static_cast<float*>(args.o) + orow * D + c0);
 #pragma unroll
-              for (int i = 0; i < 16; ++i)
-                dst[i] = make_float4(__uint_as_float(ov[4 * i]) * inv,
-                                     __uint_as_float(ov[4 * i + 1]) * inv,
-                                     __uint_as_float(ov[4 * i + 2]) * inv,
-                                     __uint_as_float(ov[4 * i + 3]) * inv);
-            } else {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.o) + orow * D + c0);
+                for (int i = 0; i < 16; ++i)
+                  dst[i] = make_float4(__uint_as_float(ov[4 * i]) * inv,
+                                       __uint_as_float(ov[4 * i + 1]) * inv,
+                                       __uint_as_float(ov[4 * i + 2]) * inv,
+                                       __uint_as_float(ov[4 * i + 3]) * inv);
+              } else {
+                uint4* dst =
+                    reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.o) + orow * D + c0);
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                uint4 u;
-                u.x = pack_bf16x2(__uint_as_float(ov[8 * i + 0]) * inv,
-                                  __uint_as_float(ov[8 * i + 1]) * inv);
-                u.y = pack_bf16x2(__uint_as_float(ov[8 * i + 2]) * inv,
-                                  __uint_as_float(ov[8 * i + 3]) * inv);
-                u.z = pack_bf16x2(__uint_as_float(ov[8 * i + 4]) * inv,
-                                  __uint_as_float(ov[8 * i + 5]) * inv);
-                u.w = pack_bf16x2(__uint_as_float(ov[8 * i + 6]) * inv,
-                                  __uint_as_float(ov[8 * i + 7]) * inv);
-                dst[i] = u;
+                for (int i = 0; i < 8; ++i) {
+                  uint4 u;
+                  u.x = pack_bf16x2(__uint_as_float(ov[8 * i + 0]) * inv,
+                                    __uint_as_float(ov[8 * i + 1]) * inv);
+                  u.y = pack_bf16x2(__uint_as_float(ov[8 * i + 2]) * inv,
+                                    __uint_as_float(ov[8 * i + 3]) * inv);
+                  u.z = pack_bf16x2(__uint_as_float(ov[8 * i + 4]) * inv,
+                                    __uint_as_float(ov[8 * i + 5]) * inv);
+                  u.w = pack_bf16x2(__uint_as_float(ov[8 * i + 6]) * inv,
+                                    __uint_as_float(ov[8 * i + 7]) * inv);
+                  dst[i] = u;
+                }
               }
             }
           }
-        }
         }
         if (store) args.lse[lidx] = lse;
       }
