@@ -24,6 +24,9 @@
  *    at once and reads no pointer (empty tensors may have NULL data).
  *  - Tensors are contiguous, row-major, without padding.  bf16 is IEEE
  *    bfloat16 (uint16 storage), f32 is IEEE binary32.
+ *  - Outputs (o, lse, part_*, gradients, statistics) must not overlap any
+ *    input of the same call: thread blocks write their outputs while other
+ *    blocks still read the inputs, so an overlap gives undefined results.
  *  - stream is a cudaStream_t (NULL = legacy default stream).  Every call
  *    only enqueues work on it and returns: nothing synchronises, so errors
  *    raised on the device appear through fa_check_device_status.
