@@ -214,6 +214,26 @@ def test_output_tail_untouched(fa):
     assert fa.fa_check_device_status() == fa.FA_OK
 
 
+@pytest.mark.parametrize("N,D,causal,qk_std", [(65536, 128, True, 3.0), (32768, 64, False, 1.0)])
+def test_long_sequence_sampled(fa, N, D, causal, qk_std):
+    """Sequences 2-4x config 3's length: sampled rows (the first and last,
+    both sides of tile edges, random ones) of both heads against the oracle.
+    The causal case keeps config 3's score spread, so the lagging reference
+    maximum runs over 512 key tiles."""
+    case = inp.dense(1, 2, N, D, seed=N + D, causal=causal, qk_std=qk_std)
+    q, k, v = _dense_gpu(case)
+    o, lse = fa.fa_fwd(q, k, v, case.scale, causal)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(N)
+    rows = sorted(set([0, 1, 127, 128, 4095, 4096, N // 2, N - 129, N - 128, N - 1])
+                  | set(rng.integers(0, N, 20).tolist()))
+    O, L = ora.attention_ref(case.q, case.k, case.v, case.scale, causal, rows=rows)
+    idx = torch.tensor(rows, device="cuda")
+    check_o_bf16(np64(o[:, :, idx]), O, f"N={N} D={D}")
+    check_lse(np64(lse[:, :, idx]), L)
+    assert fa.fa_check_device_status() == fa.FA_OK
+
+
 # --- varlen -------------------------------------------------------------------------
 
 @pytest.mark.parametrize("D", [64, 128])
