@@ -59,7 +59,8 @@ extern "C" {
 #define FA_DTYPE_F32  1
 
 /*
- * Dense forward, bf16 in and out.
+ * Dense forward, bf16 in and out: the attention defined above ("FlashAttention:
+ * Not So Special"), one (batch, head) per [N, D] slice.
  *   q, k, v : bf16 [B, H, N, D]
  *   o       : bf16 [B, H, N, D]           (written)
  *   lse     : f32  [B, H, N], natural log (written)
@@ -70,6 +71,10 @@ extern "C" {
  * the running maximum by up to 2^32 (base 2), so the unnormalised output
  * stays finite while N * 2^32 * max|v| is below fp32's range (|v| < 2^82 at
  * N = 2^14); the same holds for fa_fwd_ex, fa_fwd_window and fa_fwd_varlen.
+ * Errors: FA_ERR_INVALID_ARG for a negative size, D not in {64, 128}, a bad
+ * scale or a misaligned pointer (nothing launched); FA_ERR_UNSUPPORTED_ARCH
+ * off sm_103; a device-side wait that gave up is reported later by
+ * fa_check_device_status as FA_ERR_DEVICE_TIMEOUT.
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int N, int D, float scale, int causal, void* stream);
