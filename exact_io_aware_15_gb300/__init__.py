@@ -62,6 +62,7 @@ SIGNATURES = {
                                      _P, _P, _P, _P]),
     "fa_decode_splitkv_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _I, _P,
                                        _P]),
+    "fa_fwd_fault_inject": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _I, _P]),
     "fa_check_device_status": (_I, [_P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_last_cuda_error": (_I, []),
@@ -126,6 +127,42 @@ def _need(t: torch.Tensor, name: str, dtype, ndim: int) -> None:
         raise ValueError(f"{name} must be contiguous")
 
 
+def _out(t, name, dtype, shape, device):
+    """A caller-supplied output buffer, checked (dtype, contiguity, exact
+    shape, device), or a new one from torch when t is None.  The kernels write
+    every element of the shape they are given, so a smaller buffer would be
+    written past its end."""
+    shape = tuple(int(x) for x in shape)
+    if t is None:
+        return torch.empty(shape, dtype=dtype, device=device)
+    _need(t, name, dtype, len(shape))
+    if tuple(t.shape) != shape:
+        raise ValueError(f"{name} must have shape {shape}, got {tuple(t.shape)}")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    return t
+
+
+def _workspace(ws, nbytes, device):
+    """The caller's fp32 workspace (checked to hold nbytes) or a new one."""
+    if ws is None:
+        return torch.empty(max(1, (int(nbytes) + 3) // 4), dtype=torch.float32, device=device)
+    _need(ws, "workspace", torch.float32, 1)
+    if ws.numel() * 4 < nbytes:
+        raise ValueError(f"workspace holds {ws.numel() * 4} bytes, needs {nbytes}")
+    if ws.device != device:
+        raise ValueError(f"workspace must be on {device}")
+    return ws
+
+
+def _same_device(*named):
+    """Every tensor on the device of the first one."""
+    dev = named[0][0].device
+    for t, n in named[1:]:
+        if t is not None and t.device != dev:
+            raise ValueError(f"{n} is on {t.device}, expected {dev}")
+
+
 def _scale(scale, D):
     return 1.0 / math.sqrt(D) if scale is None else float(scale)
 
@@ -147,12 +184,9 @@ def fa_fwd_ex(q, k, v, scale=None, causal=False, o_dtype=None, o=None, lse=None)
     o_dtype = in_dtype if o_dtype is None else o_dtype
     if o_dtype not in _DT:
         raise TypeError("o_dtype must be bf16 or fp32")
-    if o is None:
-        o = torch.empty_like(q, dtype=o_dtype)
-    if lse is None:
-        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    _need(o, "o", o_dtype, 4)
-    _need(lse, "lse", torch.float32, 3)
+    _same_device((q, "q"), (k, "k"), (v, "v"))
+    o = _out(o, "o", o_dtype, (B, H, N, D), q.device)
+    lse = _out(lse, "lse", torch.float32, (B, H, N), q.device)
     rc = load_library().fa_fwd_ex(
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, D,
         _scale(scale, D), int(bool(causal)), _DT[in_dtype], _DT[o_dtype],
@@ -168,10 +202,9 @@ def fa_fwd(q, k, v, scale=None, causal=False, o=None, lse=None):
     if k.shape != q.shape or v.shape != q.shape:
         raise ValueError("q, k, v must have the same shape [B, H, N, D]")
     B, H, N, D = q.shape
-    o = torch.empty_like(q) if o is None else o
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
-    _need(o, "o", torch.bfloat16, 4)
-    _need(lse, "lse", torch.float32, 3)
+    _same_device((q, "q"), (k, "k"), (v, "v"))
+    o = _out(o, "o", torch.bfloat16, (B, H, N, D), q.device)
+    lse = _out(lse, "lse", torch.float32, (B, H, N), q.device)
     rc = load_library().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                                B, H, N, D, _scale(scale, D), int(bool(causal)),
                                _stream(q))
@@ -186,10 +219,9 @@ def fa_fwd_window(q, k, v, window, scale=None, o=None, lse=None):
     if k.shape != q.shape or v.shape != q.shape:
         raise ValueError("q, k, v must have the same shape [B, H, N, D]")
     B, H, N, D = q.shape
-    o = torch.empty_like(q) if o is None else o
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
-    _need(o, "o", torch.bfloat16, 4)
-    _need(lse, "lse", torch.float32, 3)
+    _same_device((q, "q"), (k, "k"), (v, "v"))
+    o = _out(o, "o", torch.bfloat16, (B, H, N, D), q.device)
+    lse = _out(lse, "lse", torch.float32, (B, H, N), q.device)
     rc = load_library().fa_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                                       B, H, N, D, _scale(scale, D), int(window), _stream(q))
     _check(rc, "fa_fwd_window")
@@ -208,18 +240,11 @@ def fa_bwd(q, k, v, o, do, lse, scale=None, causal=False, dq=None, dk=None, dv=N
     _need(lse, "lse", torch.float32, 3)
     if tuple(lse.shape) != (B, H, N):
         raise ValueError("lse must be [B, H, N]")
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(q) if dk is None else dk
-    dv = torch.empty_like(q) if dv is None else dv
-    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
-        _need(t, n, torch.bfloat16, 4)
+    _same_device((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do"), (lse, "lse"))
+    dq, dk, dv = (_out(t, n, torch.bfloat16, (B, H, N, D), q.device)
+                  for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")))
     lib = load_library()
-    if workspace is None:
-        workspace = torch.empty(max(1, fa_bwd_workspace_bytes(B, H, N) // 4),
-                                dtype=torch.float32, device=q.device)
-    _need(workspace, "workspace", torch.float32, 1)
-    if workspace.numel() * 4 < lib.fa_bwd_workspace_bytes(B, H, N):
-        raise ValueError("workspace too small")
+    workspace = _workspace(workspace, lib.fa_bwd_workspace_bytes(B, H, N), q.device)
     rc = lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
                     _ptr(dk), _ptr(dv), _ptr(workspace), B, H, N, D, _scale(scale, D),
                     int(bool(causal)), _stream(q))
@@ -242,8 +267,10 @@ def fa_prefix_attention(q, k_cache, v_cache, cu_seqlens_k, scale=None, o=None, l
     T = k_cache.shape[0]
     if k_cache.shape[1:] != (H, D) or cu_seqlens_k.numel() != B + 1:
         raise ValueError("shapes: q [B, H, D], caches [T, H, D], cu_seqlens_k [B + 1]")
-    o = torch.empty_like(k_cache) if o is None else o
-    lse = torch.empty((H, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    _same_device((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"),
+                 (cu_seqlens_k, "cu_seqlens_k"))
+    o = _out(o, "o", torch.bfloat16, (T, H, D), q.device)
+    lse = _out(lse, "lse", torch.float32, (H, T), q.device)
     rc = load_library().fa_prefix_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache),
                                             _ptr(cu_seqlens_k), T, B, H, D, _scale(scale, D),
                                             _ptr(o), _ptr(lse), _stream(q))
@@ -265,11 +292,13 @@ def fa_prefix_attention_chunked(q, k_cache, v_cache, cu_seqlens_k, num_splits, s
     if k_cache.shape[1:] != (H, D) or v_cache.shape != k_cache.shape or \
             cu_seqlens_k.numel() != B + 1:
         raise ValueError("shapes: q [B, H, D], caches [T, H, D], cu_seqlens_k [B + 1]")
+    _same_device((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"),
+                 (cu_seqlens_k, "cu_seqlens_k"))
     S = int(num_splits)
     parts = [torch.empty(s, dtype=torch.float32, device=q.device)
              for s in ((B, H, S), (B, H, S), (B, H, S, D))]
-    o = torch.empty_like(k_cache) if o is None else o
-    lse = torch.empty((H, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    o = _out(o, "o", torch.bfloat16, (T, H, D), q.device)
+    lse = _out(lse, "lse", torch.float32, (H, T), q.device)
     rc = load_library().fa_prefix_attention_chunked(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_k), T, B, H, D, S,
         _scale(scale, D), *(_ptr(p) for p in parts), _ptr(o), _ptr(lse), _stream(q))
@@ -292,8 +321,8 @@ def fa_row_stats(x, eps=0.0, mean=None, var=None, rstd=None):
     bf16 or fp32 matrix (fa_row_stats): Welford states, one pass."""
     dt = _rows_dtype(x)
     R, C = x.shape
-    mk = lambda t: torch.empty(R, dtype=torch.float32, device=x.device) if t is None else t
-    mean, var, rstd = mk(mean), mk(var), mk(rstd)
+    mean, var, rstd = (_out(t, n, torch.float32, (R,), x.device)
+                       for t, n in ((mean, "mean"), (var, "var"), (rstd, "rstd")))
     rc = load_library().fa_row_stats(_ptr(x), R, C, dt, float(eps), _ptr(mean), _ptr(var),
                                      _ptr(rstd), _stream(x))
     _check(rc, "fa_row_stats")
@@ -337,12 +366,12 @@ def fa_bwd_window(q, k, v, o, do, lse, window, scale=None, dq=None, dk=None, dv=
             raise ValueError(f"{n} must have the shape of q [B, H, N, D]")
     B, H, N, D = q.shape
     _need(lse, "lse", torch.float32, 3)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(q) if dk is None else dk
-    dv = torch.empty_like(q) if dv is None else dv
-    if workspace is None:
-        workspace = torch.empty(max(1, fa_bwd_workspace_bytes(B, H, N) // 4),
-                                dtype=torch.float32, device=q.device)
+    if tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse must be [B, H, N]")
+    _same_device((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do"), (lse, "lse"))
+    dq, dk, dv = (_out(t, n, torch.bfloat16, (B, H, N, D), q.device)
+                  for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")))
+    workspace = _workspace(workspace, load_library().fa_bwd_workspace_bytes(B, H, N), q.device)
     rc = load_library().fa_bwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
                                       _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), B, H, N, D,
                                       _scale(scale, D), int(window), _stream(q))
@@ -364,12 +393,11 @@ def fa_bwd_varlen(q, k, v, o, do, lse, cu_seqlens, max_seqlen, scale=None, causa
     _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
     if tuple(lse.shape) != (H, T):
         raise ValueError("lse must be [H, T]")
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(q) if dk is None else dk
-    dv = torch.empty_like(q) if dv is None else dv
-    if workspace is None:
-        workspace = torch.empty(max(1, fa_bwd_workspace_bytes(1, H, T) // 4),
-                                dtype=torch.float32, device=q.device)
+    _same_device((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do"), (lse, "lse"),
+                 (cu_seqlens, "cu_seqlens"))
+    dq, dk, dv = (_out(t, n, torch.bfloat16, (T, H, D), q.device)
+                  for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")))
+    workspace = _workspace(workspace, load_library().fa_bwd_workspace_bytes(1, H, T), q.device)
     rc = load_library().fa_bwd_varlen(
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
         _ptr(workspace), _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, int(max_seqlen), H, D,
@@ -385,10 +413,9 @@ def fa_fwd_f32(q, k, v, scale=None, causal=False, o=None, lse=None):
     if k.shape != q.shape or v.shape != q.shape:
         raise ValueError("q, k, v must have the same shape [B, H, N, D]")
     B, H, N, D = q.shape
-    o = torch.empty_like(q) if o is None else o
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
-    _need(o, "o", torch.float32, 4)
-    _need(lse, "lse", torch.float32, 3)
+    _same_device((q, "q"), (k, "k"), (v, "v"))
+    o = _out(o, "o", torch.float32, (B, H, N, D), q.device)
+    lse = _out(lse, "lse", torch.float32, (B, H, N), q.device)
     rc = load_library().fa_fwd_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                                    B, H, N, D, _scale(scale, D), int(bool(causal)),
                                    _stream(q))
@@ -407,10 +434,9 @@ def fa_fwd_varlen(q, k, v, cu_seqlens, max_seqlen, scale=None, causal=True,
         raise ValueError("q, k, v must have the same shape [T, H, D]")
     _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
     T, H, D = q.shape
-    o = torch.empty_like(q) if o is None else o
-    lse = torch.empty((H, T), dtype=torch.float32, device=q.device) if lse is None else lse
-    _need(o, "o", torch.bfloat16, 3)
-    _need(lse, "lse", torch.float32, 2)
+    _same_device((q, "q"), (k, "k"), (v, "v"), (cu_seqlens, "cu_seqlens"))
+    o = _out(o, "o", torch.bfloat16, (T, H, D), q.device)
+    lse = _out(lse, "lse", torch.float32, (H, T), q.device)
     rc = load_library().fa_fwd_varlen(
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens),
         cu_seqlens.numel() - 1, T, int(max_seqlen), H, D, _scale(scale, D),
@@ -447,12 +473,11 @@ def fa_decode_splitkv(q, k_cache, v_cache, cu_seqlens_k, num_splits, scale=None,
         raise ValueError("cu_seqlens_k must have B + 1 entries")
     S = int(num_splits)
     dev = q.device
-    part_m = torch.empty((B, H, S), dtype=torch.float32, device=dev) if part_m is None else part_m
-    part_d = torch.empty((B, H, S), dtype=torch.float32, device=dev) if part_d is None else part_d
-    part_o = torch.empty((B, H, S, D), dtype=torch.float32, device=dev) if part_o is None else part_o
-    _need(part_m, "part_m", torch.float32, 3)
-    _need(part_d, "part_d", torch.float32, 3)
-    _need(part_o, "part_o", torch.float32, 4)
+    _same_device((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"),
+                 (cu_seqlens_k, "cu_seqlens_k"))
+    part_m = _out(part_m, "part_m", torch.float32, (B, H, S), dev)
+    part_d = _out(part_d, "part_d", torch.float32, (B, H, S), dev)
+    part_o = _out(part_o, "part_o", torch.float32, (B, H, S, D), dev)
     rc = load_library().fa_decode_splitkv(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_k), k_cache.shape[0],
         B, H, D, S, _scale(scale, D), _ptr(part_m), _ptr(part_d), _ptr(part_o),
@@ -480,9 +505,11 @@ def fa_decode_paged_splitkv(q, k_pages, v_pages, block_table, seqlens, num_split
         raise ValueError("block_table and seqlens need one row per sequence")
     S = int(num_splits)
     dev = q.device
-    part_m = torch.empty((B, H, S), dtype=torch.float32, device=dev) if part_m is None else part_m
-    part_d = torch.empty((B, H, S), dtype=torch.float32, device=dev) if part_d is None else part_d
-    part_o = torch.empty((B, H, S, D), dtype=torch.float32, device=dev) if part_o is None else part_o
+    _same_device((q, "q"), (k_pages, "k_pages"), (v_pages, "v_pages"),
+                 (block_table, "block_table"), (seqlens, "seqlens"))
+    part_m = _out(part_m, "part_m", torch.float32, (B, H, S), dev)
+    part_d = _out(part_d, "part_d", torch.float32, (B, H, S), dev)
+    part_o = _out(part_o, "part_o", torch.float32, (B, H, S, D), dev)
     rc = load_library().fa_decode_paged_splitkv(
         _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seqlens), P, page,
         block_table.shape[1], B, H, Hkv, D, S, _scale(scale, D), _ptr(part_m), _ptr(part_d),
@@ -507,8 +534,9 @@ def fa_combine_states(part_m, part_d, part_o, o_dtype=torch.bfloat16, o=None, ls
         rows *= x
     if o_dtype not in _DT:
         raise TypeError("o_dtype must be bf16 or fp32")
-    o = torch.empty(lead + (D,), dtype=o_dtype, device=part_o.device) if o is None else o
-    lse = torch.empty(lead, dtype=torch.float32, device=part_o.device) if lse is None else lse
+    _same_device((part_o, "part_o"), (part_m, "part_m"), (part_d, "part_d"))
+    o = _out(o, "o", o_dtype, lead + (D,), part_o.device)
+    lse = _out(lse, "lse", torch.float32, lead, part_o.device)
     rc = load_library().fa_combine_states(
         _ptr(part_m), _ptr(part_d), _ptr(part_o), rows, S, D, _ptr(o), _DT[o_dtype],
         _ptr(lse), _stream(part_o))
@@ -533,15 +561,35 @@ def fa_decode_splitkv_noalloc(q, k_cache, v_cache, cu_seqlens_k, num_splits, sca
         raise ValueError("cu_seqlens_k must have B + 1 entries")
     if o_dtype not in _DT:
         raise TypeError("o_dtype must be bf16 or fp32")
-    o = torch.empty((B, H, D), dtype=o_dtype, device=q.device) if o is None else o
-    lse = torch.empty((B, H), dtype=torch.float32, device=q.device) if lse is None else lse
-    _need(o, "o", o_dtype, 3)
-    _need(lse, "lse", torch.float32, 2)
+    _same_device((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"),
+                 (cu_seqlens_k, "cu_seqlens_k"))
+    o = _out(o, "o", o_dtype, (B, H, D), q.device)
+    lse = _out(lse, "lse", torch.float32, (B, H), q.device)
     rc = load_library().fa_decode_splitkv_noalloc(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_k), k_cache.shape[0],
         B, H, D, int(num_splits), _scale(scale, D), _ptr(o), _DT[o_dtype], _ptr(lse),
         _stream(q))
     _check(rc, "fa_decode_splitkv_noalloc")
+    return o, lse
+
+
+def fa_fwd_fault_inject(q, k, v, skip_k_tile, wait_limit_us, scale=None, causal=False,
+                        o=None, lse=None):
+    """Test hook of the failure path (fa_fwd_fault_inject): fa_fwd with key
+    tile skip_k_tile never loaded and every device wait limited to
+    wait_limit_us; the timeout shows up in fa_check_device_status."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, 4)
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must have the same shape [B, H, N, D]")
+    B, H, N, D = q.shape
+    _same_device((q, "q"), (k, "k"), (v, "v"))
+    o = _out(o, "o", torch.bfloat16, (B, H, N, D), q.device)
+    lse = _out(lse, "lse", torch.float32, (B, H, N), q.device)
+    rc = load_library().fa_fwd_fault_inject(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, D, _scale(scale, D),
+        int(bool(causal)), int(skip_k_tile), int(wait_limit_us), _stream(q))
+    _check(rc, "fa_fwd_fault_inject")
     return o, lse
 
 
@@ -567,6 +615,6 @@ __all__ = [
     "fa_prefix_attention", "fa_prefix_attention_chunked",
     "fa_decode_splitkv", "fa_combine_states", "fa_decode_splitkv_noalloc",
     "fa_decode_paged_splitkv",
-    "fa_check_device_status",
+    "fa_check_device_status", "fa_fwd_fault_inject",
     "fa_status_string", "decode", "load_library", "FAError", "LIB_PATH",
 ]

@@ -248,11 +248,15 @@ __global__ void __launch_bounds__(256) fa_decode_splitkv_kernel(const DecodeArgs
   const int S = a.S;
   const int H = a.H;
 
-  const int k_begin = __ldg(a.cu_seqlens_k + b);
-  const int k_end = __ldg(a.cu_seqlens_k + b + 1);
+  int k_begin = __ldg(a.cu_seqlens_k + b);
+  int k_end = __ldg(a.cu_seqlens_k + b + 1);
   if (k_begin < 0 || k_end < k_begin || k_end > a.total_kv) {
+    // Offsets out of range: read nothing, report it, and leave the identity
+    // (-inf, 0, 0) in this CTA's states (an empty sequence), so the second
+    // pass never folds a state that this launch did not write.
     if (threadIdx.x == 0) atomicOr(a.status, kStatusBounds);
-    return;
+    k_begin = 0;
+    k_end = 0;
   }
   if (h >= H) return;
   int k0, k1;
@@ -276,10 +280,12 @@ __global__ void __launch_bounds__(256) fa_decode_paged_kernel(const PagedDecodeA
   const int c = blockIdx.x;
   const int h = blockIdx.y * 8 + warp;
   const int b = blockIdx.z;
-  const int L = __ldg(a.seqlens + b);
+  int L = __ldg(a.seqlens + b);
   if (L < 0 || static_cast<long long>(L) > static_cast<long long>(a.max_blocks) * a.page_size) {
+    // A length out of range: report it and write the identity states (as
+    // for an empty sequence) instead of reading anything.
     if (threadIdx.x == 0) atomicOr(a.status, kStatusBounds);
-    return;
+    L = 0;
   }
   if (h >= a.H) return;
   const int hk = h / (a.H / a.Hkv);

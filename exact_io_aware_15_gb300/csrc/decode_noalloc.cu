@@ -30,13 +30,14 @@ void* g_noalloc_addr[kMaxDev] = {};
 int scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return FA_ERR_CUDA;
+  if (e != cudaSuccess) return fa::record_cuda_error(e);
   if (dev < 0 || dev >= kMaxDev) return FA_ERR_UNSUPPORTED_ARCH;
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
   if (g_noalloc_addr[dev] == nullptr) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || p == nullptr) return FA_ERR_CUDA;
+    if (e != cudaSuccess) return fa::record_cuda_error(e);
+    if (p == nullptr) return fa::record_cuda_error(cudaErrorInvalidSymbol);
     g_noalloc_addr[dev] = p;
   }
   *out = g_noalloc_addr[dev];
@@ -94,7 +95,8 @@ extern "C" int fa_decode_splitkv_noalloc(const void* q, const void* k_cache,
   a.part_d = part_d;
   a.part_o = part_o;
   a.status = status;
-  if (fa::launch_decode_splitkv(a, D, st) != cudaSuccess) return FA_ERR_LAUNCH;
+  rc = fa::launch_status(fa::launch_decode_splitkv(a, D, st));
+  if (rc != FA_OK) return rc;
   fa::CombineArgs c{};
   c.part_m = part_m;
   c.part_d = part_d;
@@ -104,6 +106,5 @@ extern "C" int fa_decode_splitkv_noalloc(const void* q, const void* k_cache,
   c.o = o;
   c.o_f32 = o_dtype == FA_DTYPE_F32 ? 1 : 0;
   c.lse = lse;
-  if (fa::launch_combine(c, D, st) != cudaSuccess) return FA_ERR_LAUNCH;
-  return FA_OK;
+  return fa::launch_status(fa::launch_combine(c, D, st));
 }

@@ -112,7 +112,8 @@ int launched(cudaError_t e) {
 }
 
 int fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-             int N, int D, float scale, int causal, int o_f32, void* stream, int window = 0) {
+             int N, int D, float scale, int causal, int o_f32, void* stream, int window = 0,
+             int skip_k_tile = -1, unsigned long long wait_limit_ns = 0) {
   if (B >= 0 && H >= 0 && N >= 0 && (B == 0 || H == 0 || N == 0) &&
       (D == 64 || D == 128) && good_scale(scale))
     return FA_OK;  // empty problem: nothing to read or write
@@ -150,6 +151,8 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, i
   a.o_f32 = o_f32;
   a.lse = lse;
   a.status = status;
+  a.wait_limit_ns = wait_limit_ns;
+  a.skip_k_tile = skip_k_tile;
   return launched(fa::launch_fwd_tc(maps, a, D, static_cast<int>(BH),
                                     static_cast<cudaStream_t>(stream)));
 }
@@ -321,6 +324,8 @@ int bwd_varlen(const void* q, const void* k, const void* v, const void* o, const
 }  // namespace
 
 int fa::checked_current_device(unsigned int** status) { return current_device(status); }
+int fa::record_cuda_error(cudaError_t e) { return record(e); }
+int fa::launch_status(cudaError_t e) { return launched(e); }
 
 extern "C" {
 
@@ -333,6 +338,14 @@ int fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* l
                   int H, int N, int D, float scale, int window, void* stream) {
   if (window < 1) return FA_ERR_INVALID_ARG;
   return fwd_bf16(q, k, v, o, lse, B, H, N, D, scale, 1, 0, stream, window);
+}
+
+int fa_fwd_fault_inject(const void* q, const void* k, const void* v, void* o, float* lse,
+                        int B, int H, int N, int D, float scale, int causal, int skip_k_tile,
+                        int wait_limit_us, void* stream) {
+  if (skip_k_tile < 0 || wait_limit_us < 1 || wait_limit_us > 2000000) return FA_ERR_INVALID_ARG;
+  return fwd_bf16(q, k, v, o, lse, B, H, N, D, scale, causal, 0, stream, 0, skip_k_tile,
+                  static_cast<unsigned long long>(wait_limit_us) * 1000ull);
 }
 
 int fa_fwd_f32(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
@@ -396,6 +409,8 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
   a.o_f32 = 0;
   a.lse = lse;
   a.status = status;
+  a.wait_limit_ns = 0;
+  a.skip_k_tile = -1;
   return launched(fa::launch_fwd_tc(maps, a, D, static_cast<int>(SH),
                                     static_cast<cudaStream_t>(stream)));
 }

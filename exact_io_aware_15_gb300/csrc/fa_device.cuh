@@ -64,17 +64,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase of `bar` with the given parity.  Returns false (without
-// waiting further) once *abort is set by another role, or after kWaitLimitNs,
-// in which case it sets *abort and records kStatusTimeout.
+// waiting further) once *abort is set by another role, or after limit_ns
+// (kWaitLimitNs unless a caller passes a shorter limit), in which case it sets
+// *abort and records kStatusTimeout.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          volatile int* abort, unsigned int* status) {
+                                          volatile int* abort, unsigned int* status,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0u) {
       if (*abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs || it > (1u << 30)) {
+      if (globaltimer_ns() - t0 > limit_ns || it > (1u << 30)) {
         atomicOr(status, kStatusTimeout);
         *abort = 1;
         return false;

@@ -23,6 +23,12 @@ struct TcFwdArgs {
   int o_tma;         // 1: bf16 O (D = 128) is stored through TcMaps::o (32-row boxes)
   float* lse;
   unsigned int* status;
+  // Fault injection, used only by the tests of the timeout path (0 and -1 in
+  // every other call): wait_limit_ns > 0 replaces the limit of every pipeline
+  // wait, and skip_k_tile >= 0 makes the producer leave that key tile
+  // unloaded, so the wait for it runs out and every role unwinds.
+  unsigned long long wait_limit_ns;
+  int skip_k_tile;
 };
 
 // Tensor maps of Q, K, V (128-row boxes) and of O (32-row boxes, used when
@@ -180,5 +186,13 @@ cudaError_t launch_prefix_scan(const ScanArgs& a, int D, cudaStream_t stream);
 // The sm_103 check of the current device and its device status word, as used
 // by every entry point of fa_api.cu (returns an FA_* status code).
 int checked_current_device(unsigned int** status);
+
+// Remember a CUDA runtime error for fa_last_cuda_error() on this thread and
+// return FA_ERR_CUDA.
+int record_cuda_error(cudaError_t e);
+
+// FA_OK for cudaSuccess; otherwise remember the error for fa_last_cuda_error()
+// and return FA_ERR_LAUNCH (the status of a kernel launch).
+int launch_status(cudaError_t e);
 
 }  // namespace fa

@@ -203,6 +203,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const unsigned long long wlim = args.wait_limit_ns ? args.wait_limit_ns : kWaitLimitNs;
 
   // TMA box origin of a 128-row tile starting at sequence position `row0`,
   // column half `c`.  Dense maps are (D, N, B*H); varlen maps are (D, H, T).
@@ -222,8 +223,11 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
     const int S = is_v ? C::VS : C::KS;
     const int st = j % S;
     if (j >= S && !mbar_wait(bar((is_v ? C::B_V_EMPTY : C::B_K_EMPTY) + st), ((j / S) - 1) & 1,
-                             abort_flag, args.status))
+                             abort_flag, args.status, wlim))
       return false;
+    // Fault injection (tests of the timeout path only): this key tile is
+    // never requested, so its full barrier never completes.
+    if (!is_v && j == args.skip_k_tile) return true;
     const uint32_t fb = bar((is_v ? C::B_V_FULL : C::B_K_FULL) + st);
     const uint32_t dst = sbase + (is_v ? C::OFF_V : C::OFF_K) + st * C::TILE_BYTES;
     mbar_arrive_expect_tx(fb, C::TILE_BYTES);
@@ -299,9 +303,12 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
       }
       if (*abort_flag) {
         // Let every copy this thread started land before the CTA exits.
+        // Tiles before the last KS (VS) were waited for by the products
+        // that freed their stages for the later tiles.
         mbar_wait_unwind(bar(C::B_Q_FULL), 0);
         for (int j = max(0, k_issued - C::KS); j < k_issued; ++j)
-          mbar_wait_unwind(bar(C::B_K_FULL + j % C::KS), (j / C::KS) & 1);
+          if (j != args.skip_k_tile)  // never requested: nothing in flight
+            mbar_wait_unwind(bar(C::B_K_FULL + j % C::KS), (j / C::KS) & 1);
         for (int j = max(0, v_issued - C::VS); j < v_issued; ++j)
           mbar_wait_unwind(bar(C::B_V_FULL + j % C::VS), (j / C::VS) & 1);
       }
@@ -311,16 +318,16 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
       const uint32_t q_s = sbase + C::OFF_Q;
-      bool ok = mbar_wait(bar(C::B_Q_FULL), 0, abort_flag, args.status);
+      bool ok = mbar_wait(bar(C::B_Q_FULL), 0, abort_flag, args.status, wlim);
       for (int j = 0; ok && j < n_kv; ++j) {
         // The S buffer is free once the softmax warps have loaded S_{j-1};
         // P buffer j % 4, which the softmax of tile j writes, once
         // P_{j-4} V_{j-4} has finished.
         if (!mbar_wait(bar(C::B_K_FULL + j % C::KS), (j / C::KS) & 1, abort_flag,
                        args.status) ||
-            (j >= 1 && !mbar_wait(bar(C::B_S_FREE), (j - 1) & 1, abort_flag, args.status)) ||
+            (j >= 1 && !mbar_wait(bar(C::B_S_FREE), (j - 1) & 1, abort_flag, args.status, wlim)) ||
             (j >= C::NP && !mbar_wait(bar(C::B_PV_DONE + j % C::NP), ((j - C::NP) / C::NP) & 1,
-                                      abort_flag, args.status))) {
+                                      abort_flag, args.status, wlim))) {
           ok = false;
           break;
         }
@@ -348,8 +355,8 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
       for (int j = 0; j < n_kv; ++j) {
         const int sv = j % C::VS;
-        if (!mbar_wait(bar(C::B_P_FULL + j % C::NP), (j / C::NP) & 1, abort_flag, args.status) ||
-            !mbar_wait(bar(C::B_V_FULL + sv), (j / C::VS) & 1, abort_flag, args.status))
+        if (!mbar_wait(bar(C::B_P_FULL + j % C::NP), (j / C::NP) & 1, abort_flag, args.status, wlim) ||
+            !mbar_wait(bar(C::B_V_FULL + sv), (j / C::VS) & 1, abort_flag, args.status, wlim))
           break;
         tc_fence_after();
         const uint32_t v_s = sbase + C::OFF_V + sv * C::TILE_BYTES;
@@ -385,7 +392,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
 
     for (int j = 0; j < n_kv; ++j) {
       const uint32_t s_t = tmem + lane_off + C::TMEM_S;
-      const bool w = mbar_wait(bar(C::B_S_FULL), j & 1, abort_flag, args.status);
+      const bool w = mbar_wait(bar(C::B_S_FULL), j & 1, abort_flag, args.status, wlim);
       if (__any_sync(0xffffffffu, !w)) {
         ok = false;
         break;
@@ -471,7 +478,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
         // o <- alpha * o between P_{j-1} V_{j-1} and P_j V_j (rare: only
         // when a row of this warp moved its reference maximum).
         const bool w2 = mbar_wait(bar(C::B_PV_DONE + (j - 1) % C::NP), ((j - 1) / C::NP) & 1,
-                                  abort_flag, args.status);
+                                  abort_flag, args.status, wlim);
         if (__any_sync(0xffffffffu, !w2)) {
           ok = false;
           break;
@@ -494,7 +501,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
 
     if (ok) {
       const bool w = mbar_wait(bar(C::B_PV_DONE + (n_kv - 1) % C::NP),
-                               ((n_kv - 1) / C::NP) & 1, abort_flag, args.status);
+                               ((n_kv - 1) / C::NP) & 1, abort_flag, args.status, wlim);
       if (!__any_sync(0xffffffffu, !w)) {
         tc_fence_after();
         const float inv = dnorm > 0.f ? 1.f / dnorm : 0.f;

@@ -35,6 +35,15 @@
  *  - Return value: FA_OK (0) or a negative FA_ERR_* code.  On
  *    FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED_ARCH nothing was launched and no
  *    output was touched.
+ *  - When fa_check_device_status reports FA_ERR_DEVICE_BOUNDS or
+ *    FA_ERR_DEVICE_TIMEOUT, the outputs of the calls enqueued since the last
+ *    check are undefined (the split-KV first passes write the identity
+ *    state (-inf, 0, 0) for a sequence whose offsets or length failed the
+ *    check, but nothing else is promised).
+ *  - The library looks up per-device addresses (its status word, the
+ *    no-allocation scratch) once per device and keeps them for the life of
+ *    the process: after cudaDeviceReset on a device, do not call the library
+ *    on that device again in the same process.
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
@@ -359,9 +368,11 @@ int fa_combine_states(const float* part_m, const float* part_d,
  * refused with FA_ERR_SCRATCH_CAPACITY before anything is launched.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress, no allocation); make that first call before
- *    capturing the stream.
+ *    capturing the stream.  The address is kept until the process exits, so
+ *    this entry point must not be called on a device after cudaDeviceReset.
  *  - Nothing has to be cleared between calls: the first pass writes every
- *    state the second pass reads.
+ *    state the second pass reads, the identity (-inf, 0, 0) for a sequence
+ *    whose cache offsets fail the device's bounds check.
  *  - All calls on a device share the one array, so calls whose work
  *    overlaps on the GPU (different streams, no ordering) race on it.
  * The function calls no cudaMalloc, cudaFree or allocating library routine.
@@ -370,6 +381,22 @@ int fa_decode_splitkv_noalloc(const void* q, const void* k_cache, const void* v_
                               const int* cu_seqlens_k, int total_kv_tokens, int B,
                               int H, int D, int num_splits, float scale, void* o,
                               int o_dtype, float* lse, void* stream);
+
+/*
+ * Test hook for the failure path, not for production use: fa_fwd (bf16 out)
+ * with one fault injected.  The producer leaves key tile skip_k_tile (>= 0,
+ * counted from each query tile's first key tile) unrequested, as if its copy
+ * had been lost, and every pipeline wait gives up after wait_limit_us
+ * microseconds (1 .. 2,000,000) instead of 2 s.  A query tile that reaches
+ * the missing key tile then records FA_ERR_DEVICE_TIMEOUT, lets its issued
+ * copies and products complete, frees its tensor memory and exits, leaving
+ * its rows of o and lse unwritten; fa_check_device_status reports the
+ * timeout and clears it, and the context stays usable.  Other arguments and
+ * errors as fa_fwd.
+ */
+int fa_fwd_fault_inject(const void* q, const void* k, const void* v, void* o, float* lse,
+                        int B, int H, int N, int D, float scale, int causal, int skip_k_tile,
+                        int wait_limit_us, void* stream);
 
 /*
  * Synchronises `stream`, then reads and clears the device status word of the

@@ -79,6 +79,10 @@ def test_host_validation_without_gpu(lib):
     assert lib.fa_decode_paged_splitkv(p, p, p, p, p, 4, 16, 4, 1, 8, 3, 128, 4, 0.1,
                                        p, p, p, null) == -1
     assert lib.fa_fwd_window(p, p, p, p, p, 1, 1, 16, 64, 0.1, 0, null) == -1
+    # the failure-path test hook: a tile index >= 0 and a limit in [1 us, 2 s]
+    assert lib.fa_fwd_fault_inject(p, p, p, p, p, 1, 1, 16, 64, 0.1, 0, -1, 1000, null) == -1
+    assert lib.fa_fwd_fault_inject(p, p, p, p, p, 1, 1, 16, 64, 0.1, 0, 1, 0, null) == -1
+    assert lib.fa_fwd_fault_inject(p, p, p, p, p, 1, 1, 16, 64, 0.1, 0, 1, 2000001, null) == -1
 
 
 def test_binding_exports_exist():

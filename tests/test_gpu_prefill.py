@@ -102,32 +102,6 @@ def test_config2_full(fa):
     check_lse(np64(lse), L)
 
 
-def test_config3_overflow_sampled(fa):
-    """B=1 H=32 N=16384 D=128 causal, Q,K ~ N(0, 9): scaled scores reach the
-    high tens.  Sampled rows of every head against the oracle; d in [1, N]
-    shows up as a finite LSE with LSE >= row max."""
-    case = inp.config3(device="cuda")
-    q, k, v = case.q, case.k, case.v
-    o, lse = fa.fa_fwd(q, k, v, case.scale, True)
-    o32, _ = fa.fa_fwd_ex(q, k, v, case.scale, True, o_dtype=torch.float32)
-    torch.cuda.synchronize()
-    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
-    rng = np.random.default_rng(3)
-    rows = np.unique(np.concatenate([[0, 1, 127, 128, 129, 8191, 16383],
-                                     rng.integers(0, 16384, 57)]))
-    heads = [0, 7, 31]
-    qc, kc, vc = (t[:, heads].cpu() for t in (q, k, v))
-    O, L = ora.attention_ref(qc, kc, vc, case.scale, True, rows=rows)
-    ri = torch.as_tensor(rows, device="cuda")
-    hi = torch.as_tensor(heads, device="cuda")
-    pick = lambda t: t.index_select(1, hi).index_select(2, ri)
-    check_o_bf16(np64(pick(o)), O, "config3 bf16")
-    check_o_f32(np64(pick(o32)), O, "config3 fp32-out")
-    check_lse(np64(pick(lse)), L)
-    # scores really are in the overflow range of a naive exp in fp32
-    assert L.max() > 40.0
-
-
 @pytest.mark.parametrize("c", [-90.0, 50.0, 90.0, 200.0])
 def test_offset_invariance(fa, c):
     """Append a coordinate so every score of a row moves by c (q' = [q, c/scale],
@@ -256,29 +230,6 @@ def test_varlen_small(fa, D):
             assert torch.equal(od[0].permute(1, 0, 2), o[a:b])
             assert torch.equal(ld[0], lse[:, a:b])
     assert fa.fa_check_device_status() == fa.FA_OK
-
-
-@pytest.mark.parametrize("D", [64, 128])
-def test_config5_varlen_sampled(fa, D):
-    """65536 packed tokens, lengths U[1, 8192], H=16, causal: sampled rows of
-    every sequence and head against the oracle."""
-    case = inp.config5(D)
-    q, k, v = case.q.cuda(), case.k.cuda(), case.v.cuda()
-    o, lse = fa.fa_fwd_varlen(q, k, v, case.cu_seqlens.cuda(), case.max_seqlen,
-                              case.scale, True)
-    torch.cuda.synchronize()
-    rng = np.random.default_rng(D)
-    rows = sorted(set([0, 1, 126, 127, 128, 129]) | set(rng.integers(0, 8192, 24).tolist()))
-    cuh = case.cu_seqlens.tolist()
-    for s in range(len(cuh) - 1):
-        a, b = cuh[s], cuh[s + 1]
-        r = [x for x in rows if x < b - a] + [b - a - 1]
-        r = sorted(set(r))
-        Of, Lf = ora.varlen_ref(case.q, case.k, case.v, case.cu_seqlens, case.scale, True,
-                                seqs=[s], rows=r)[s]
-        idx = torch.tensor([a + x for x in r], device="cuda")
-        check_o_bf16(np64(o.index_select(0, idx)), Of, f"seq {s}")
-        check_lse(np64(lse.index_select(1, idx)), Lf)
 
 
 def test_varlen_bad_offsets_reported(fa):
