@@ -454,7 +454,36 @@ def other_configs(fa):
     kvb = float(sum(pc.meta["lens"])) * 8 * 128 * 2 * 2
     out["paged_gqa_decode_B64_H32_Hkv8_page64"] = {"gbs": kvb / (ms * 1e-3) / 1e9, "ms": ms,
                                                   "kv_bytes": kvb}
+
+    def paged16():
+        pm, pd, po = fa.fa_decode_paged_splitkv(pc.q, pc.k_pages, pc.v_pages, tab, sl, 16,
+                                                pc.scale)
+        fa.fa_combine_states(pm, pd, po)
+    ms = _time_launches(paged16, 10)
+    out["paged_gqa_decode_B64_H32_Hkv8_page64_S16"] = {"gbs": kvb / (ms * 1e-3) / 1e9, "ms": ms,
+                                                      "kv_bytes": kvb}
     del pc
+    # the split-KV decode and its combine back to back, nothing between the
+    # two launches (the combine's launch then overlaps the decode's tail)
+    dc = inp.config4(device="cuda")
+    dcu = dc.cu_seqlens_k.cuda()
+    Dd = DECODE
+    pm = torch.empty((Dd["B"], Dd["H"], Dd["S"]), dtype=torch.float32, device="cuda")
+    pd = torch.empty_like(pm)
+    po = torch.empty((Dd["B"], Dd["H"], Dd["S"], Dd["D"]), dtype=torch.float32, device="cuda")
+    od = torch.empty((Dd["B"], Dd["H"], Dd["D"]), dtype=torch.bfloat16, device="cuda")
+    lsed = torch.empty((Dd["B"], Dd["H"]), dtype=torch.float32, device="cuda")
+
+    def dec_pair():
+        fa.fa_decode_splitkv(dc.q, dc.k_cache, dc.v_cache, dcu, Dd["S"], dc.scale, pm, pd, po)
+        fa.fa_combine_states(pm, pd, po, o=od, lse=lsed)
+    ms = _time_launches(dec_pair, 10)
+    alg = float(sum(dc.meta["lens"])) * Dd["H"] * Dd["D"] * 4 + \
+        Dd["B"] * Dd["H"] * (Dd["D"] * 4 + 4)
+    out["splitkv_decode_and_combine_B64_H32_D128_S16"] = {
+        "ms": ms, "gbs": alg / (ms * 1e-3) / 1e9,
+        "bytes": alg, "note": "K, V, q read; O, LSE written; no event between the launches"}
+    del dc, pm, pd, po, od, lsed
     # A launch of this size takes less device time than a Python call, so
     # 100 launches are captured in a CUDA graph and the replays timed: the
     # device time per launch, not the host's call rate.
@@ -663,6 +692,8 @@ def run_gpu(args, rank, world, dist):
                    "frac_of_nominal_8tbs": dec_gbs / 8000.0,
                    "bytes_per_launch": dec_bytes, "kv_tokens": int(sum(lens)),
                    "combine_us": cmb_ms / K * 1e3,
+                   "combine_gbs": cmb_bytes / (cmb_ms / K * 1e-3) / 1e9,
+                   "combine_bytes": cmb_bytes,
                    "end_to_end_gbs": e2e_dec_gbs,
                    "traffic": load_traffic("fa_decode_splitkv_kernel<128>",
                                            "exact_io_aware_15_gb300/csrc/decode.cu")},
@@ -726,6 +757,17 @@ def run_profile_case(args):
         pl = torch.empty((DECODE["H"], pc.meta["T"]), dtype=torch.float32, device="cuda")
         run = lambda: fa.fa_prefix_attention_chunked(pc.q, pc.k_cache, pc.v_cache, cu, 4,
                                                      pc.scale, po, pl)
+    elif args.profile_case == "combine":
+        # the state combine alone on states of the decode workload's shape
+        # (B=64 x H=32 rows, 16 chunks: 17 MB), seeded, with no KV cache
+        B, H, S, D = DECODE["B"], DECODE["H"], DECODE["S"], DECODE["D"]
+        g = torch.Generator(device="cuda").manual_seed(13)
+        pm = torch.randn((B, H, S), generator=g, device="cuda") * 20.0
+        pd = torch.rand((B, H, S), generator=g, device="cuda") * 500.0 + 1.0
+        po = torch.randn((B, H, S, D), generator=g, device="cuda") * 50.0
+        od = torch.empty((B, H, D), dtype=torch.bfloat16, device="cuda")
+        lsed = torch.empty((B, H), dtype=torch.float32, device="cuda")
+        run = lambda: fa.fa_combine_states(pm, pd, po, o=od, lse=lsed)
     elif args.profile_case == "rowstats":
         x = inp.stats_rows(ROWSTATS["R"], ROWSTATS["C"], seed=11, loc=0.5, std=1.0,
                            row_spread=1.0, device="cuda")
@@ -755,7 +797,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-other-configs", action="store_true")
     ap.add_argument("--profile-case", choices=["prefill", "decode", "bwd", "rowstats", "paged",
-                                                "scan", "scan_small"],
+                                                "scan", "scan_small", "combine"],
                     default=None)
     args = ap.parse_args(argv)
     if args.profile_case:

@@ -7,7 +7,9 @@
 // row is read off as o / d ("The State").
 //
 // One warp per row; lane l owns D/32 consecutive columns, so each chunk's
-// partial o row is one coalesced 512-byte (D = 128) read.  Chunks are folded
+// partial o row is one coalesced 512-byte (D = 128) read.  A lane loads the
+// states of 16 chunks at a time before folding them, so a row waits for
+// memory once per 16 chunks rather than once per chunk.  Chunks are folded
 // in index order 0, 1, ..., S-1 starting from the identity, with no atomics,
 // so the result does not depend on the launch.  Every arithmetic step is a
 // single IEEE binary32 operation with round-to-nearest (the __f*_rn
@@ -92,9 +94,15 @@ __device__ __forceinline__ void sw_ln_split(float d, int& e, float& lnx) {
   lnx = __fmul_rn(__fadd_rn(t, t), p);
 }
 
+// Chunks whose states one lane loads before folding them (a batch).
+constexpr int kBatch = 16;
+
 template <int D>
 __global__ void __launch_bounds__(256) fa_combine_kernel(const CombineArgs a) {
   constexpr int VPL = D / 32;  // columns per lane
+  // Launched as a programmatic dependent of the split-KV pass: wait until
+  // that grid has finished and its partial states are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * 8 + warp;
@@ -109,37 +117,50 @@ __global__ void __launch_bounds__(256) fa_combine_kernel(const CombineArgs a) {
 #pragma unroll
   for (int i = 0; i < VPL; ++i) o[i] = 0.0f;
 
-#pragma unroll 4
-  for (int c = 0; c < S; ++c) {
-    const float mb = __ldg(pm + c);
-    const float db = __ldg(pd + c);
-    float ob[VPL];
-    if constexpr (VPL == 4) {
-      const float4 x = __ldg(reinterpret_cast<const float4*>(po + static_cast<size_t>(c) * D));
-      ob[0] = x.x; ob[1] = x.y; ob[2] = x.z; ob[3] = x.w;
-    } else {
-      const float2 x = __ldg(reinterpret_cast<const float2*>(po + static_cast<size_t>(c) * D));
-      ob[0] = x.x; ob[1] = x.y;
+  for (int c0 = 0; c0 < S; c0 += kBatch) {
+    // All loads of the batch first (one memory latency per batch), then the
+    // fold in chunk order.
+    float mb[kBatch], db[kBatch], ob[kBatch][VPL];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      if (c0 + i < S) {
+        const int c = c0 + i;
+        mb[i] = __ldg(pm + c);
+        db[i] = __ldg(pd + c);
+        if constexpr (VPL == 4) {
+          const float4 x =
+              __ldg(reinterpret_cast<const float4*>(po + static_cast<size_t>(c) * D));
+          ob[i][0] = x.x; ob[i][1] = x.y; ob[i][2] = x.z; ob[i][3] = x.w;
+        } else {
+          const float2 x =
+              __ldg(reinterpret_cast<const float2*>(po + static_cast<size_t>(c) * D));
+          ob[i][0] = x.x; ob[i][1] = x.y;
+        }
+      }
     }
-    if (mb == -INFINITY) continue;  // chunk c is the identity
-    if (m == -INFINITY) {           // the running state is the identity
-      m = mb;
-      d = db;
 #pragma unroll
-      for (int i = 0; i < VPL; ++i) o[i] = ob[i];
-      continue;
-    }
-    if (m >= mb) {
-      const float f = sw_exp2(__fsub_rn(mb, m));
-      d = __fmaf_rn(db, f, d);
+    for (int i = 0; i < kBatch; ++i) {
+      if (c0 + i >= S) break;
+      if (mb[i] == -INFINITY) continue;  // chunk c0 + i is the identity
+      if (m == -INFINITY) {              // the running state is the identity
+        m = mb[i];
+        d = db[i];
 #pragma unroll
-      for (int i = 0; i < VPL; ++i) o[i] = __fmaf_rn(ob[i], f, o[i]);
-    } else {
-      const float f = sw_exp2(__fsub_rn(m, mb));
-      d = __fmaf_rn(d, f, db);
+        for (int k = 0; k < VPL; ++k) o[k] = ob[i][k];
+        continue;
+      }
+      if (m >= mb[i]) {
+        const float f = sw_exp2(__fsub_rn(mb[i], m));
+        d = __fmaf_rn(db[i], f, d);
 #pragma unroll
-      for (int i = 0; i < VPL; ++i) o[i] = __fmaf_rn(o[i], f, ob[i]);
-      m = mb;
+        for (int k = 0; k < VPL; ++k) o[k] = __fmaf_rn(ob[i][k], f, o[k]);
+      } else {
+        const float f = sw_exp2(__fsub_rn(m, mb[i]));
+        d = __fmaf_rn(d, f, db[i]);
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) o[k] = __fmaf_rn(o[k], f, ob[i][k]);
+        m = mb[i];
+      }
     }
   }
 
@@ -174,12 +195,22 @@ __global__ void __launch_bounds__(256) fa_combine_kernel(const CombineArgs a) {
 }  // namespace
 
 cudaError_t launch_combine(const CombineArgs& a, int D, cudaStream_t stream) {
-  const unsigned blocks = static_cast<unsigned>((a.rows + 7) / 8);
-  if (D == 128)
-    fa_combine_kernel<128><<<blocks, 256, 0, stream>>>(a);
-  else
-    fa_combine_kernel<64><<<blocks, 256, 0, stream>>>(a);
-  return cudaGetLastError();
+  // Programmatic dependent launch: the CTAs may be scheduled while the
+  // preceding kernel on the stream is still finishing (the split-KV pass
+  // allows it once all of its CTAs have started) and wait for its results in
+  // griddepcontrol.wait, so the launch latency overlaps that kernel's tail.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((a.rows + 7) / 8));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (D == 128) return cudaLaunchKernelEx(&cfg, fa_combine_kernel<128>, a);
+  return cudaLaunchKernelEx(&cfg, fa_combine_kernel<64>, a);
 }
 
 }  // namespace fa

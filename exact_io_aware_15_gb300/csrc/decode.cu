@@ -241,6 +241,9 @@ __device__ __forceinline__ void chunk_range(int L, int S, int c, int& k0, int& k
 // 256-byte rows (2 KB contiguous at D = 128).
 template <int D>
 __global__ void __launch_bounds__(256) fa_decode_splitkv_kernel(const DecodeArgs a) {
+  // The combine that follows may be scheduled once every CTA of this grid
+  // has started (it waits for this grid's results before reading them).
+  asm volatile("griddepcontrol.launch_dependents;");
   const int warp = threadIdx.x >> 5;
   const int c = blockIdx.x;
   const int h = blockIdx.y * 8 + warp;

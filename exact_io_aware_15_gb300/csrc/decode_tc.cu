@@ -12,8 +12,8 @@
 //
 // fa_decode_paged_tc_kernel: one CTA per (sequence b, KV head hk, chunk c),
 // 192 threads: warp 0 TMA producer, warp 1 MMA issuer, warps 2..5 softmax.
-// Per tile of 128 keys (tiles aligned to multiples of 128 in the sequence;
-// keys outside the chunk are masked):
+// Per tile of 128 keys (tiles aligned to multiples of 128 in the sequence,
+// chunks made of whole tiles, keys past the sequence end masked):
 //   S^T[key, head] = K_tile . Q_g^T      M = 128 keys, N = 16 (the G heads,
 //                                         padded), A = K (smem), B = Q (smem)
 //   softmax, thread = key: per-head maximum over the tile through one
@@ -128,7 +128,9 @@ __global__ void __launch_bounds__(192, 1)
     if (threadIdx.x == 0) atomicOr(a.status, kStatusBounds);
     L = 0;
   }
-  const int size = (L + S - 1) / S;
+  // Chunks are whole 128-key tiles (ceil(L / S) rounded up), so no tile is
+  // read by two chunks.
+  const int size = ((L + S - 1) / S + kKeys - 1) / kKeys * kKeys;
   const int k0 = min(L, c * size), k1 = min(L, (c + 1) * size);
   if (k0 >= k1) {  // empty chunk: the identity (-inf, 0, 0) for every head of the group
     for (int i = threadIdx.x; i < G * 128; i += blockDim.x) {

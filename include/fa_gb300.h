@@ -308,8 +308,8 @@ int fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
 
 /*
  * Split-KV decode, first pass, over a paged KV cache with grouped query
- * heads.  Same chunking and outputs as fa_decode_splitkv (part_m, part_d,
- * part_o for B*H rows; finish with fa_combine_states).
+ * heads.  Same outputs as fa_decode_splitkv (part_m, part_d, part_o for B*H
+ * rows; finish with fa_combine_states); the chunking is described below.
  *   q           : bf16 [B, H, D]
  *   k_pages     : bf16 [num_pages, page_size, H_kv, D], v_pages likewise
  *   block_table : int32 [B, max_blocks] DEVICE array: key t of sequence b is
@@ -324,10 +324,13 @@ int fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
  * out of the fold.
  * With D = 128, 2 <= H / H_kv <= 16 and page_size >= 8 the query heads of a
  * group share one tensor-core product per 128-key tile (keys in M, the
- * group's heads in N): each KV row is read once for the whole group.  Chunk
- * boundaries that fall inside a 128-key tile make both neighbouring chunks
- * read that tile, so fewer chunks mean less traffic.  Other shapes fold on
- * the CUDA cores, one query head per warp.
+ * group's heads in N): each KV row is read once for the whole group.  On
+ * that path a chunk is made of whole tiles: its length ceil(L/S) is rounded
+ * up to a multiple of 128 keys (trailing chunks may then be empty), so no
+ * tile is read twice.  Other shapes fold on the CUDA cores, one query head
+ * per warp, with the chunks of fa_decode_splitkv.  Either way the combined
+ * output is the same attention; only the chunk boundaries of the partial
+ * states differ.
  */
 int fa_decode_paged_splitkv(const void* q, const void* k_pages, const void* v_pages,
                             const int* block_table, const int* seqlens, int num_pages,

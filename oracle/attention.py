@@ -111,7 +111,7 @@ def attention_ref(q, k, v, scale, causal, rows=None, window=None):
     return O, L
 
 
-def attention_bwd_head_ref(q, k, v, do, scale, causal, window=None):
+def attention_bwd_head_ref(q, k, v, do, scale, causal, window=None, o=None):
     """Gradients of one head's attention with respect to q, k, v, given the
     output gradient do (all [N, D] float64).  Recomputation, as the tiled
     backward does it: P is rebuilt from the scores and the row log-sum-exp
@@ -119,10 +119,14 @@ def attention_bwd_head_ref(q, k, v, do, scale, causal, window=None):
         dV = P^T dO,  dP = dO V^T,  Delta_i = sum_j P_ij dP_ij = dO_i . O_i,
         dS = P * (dP - Delta),  dQ = scale dS K,  dK = scale dS^T Q.
     ``window`` (with causal): the sliding window of attention_head_ref.
+    ``o``: the forward output a backward call is handed ([N, D]); Delta is
+    then formed as dO_i . o_i from it, as such a call defines it.  None (the
+    default) uses this oracle's own exact O, which gives the exact gradient.
     Returns dq, dk, dv and Delta."""
     q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
     n = q.shape[0]
-    o, lse = attention_head_ref(q, k, v, scale, causal, window=window)
+    o_own, lse = attention_head_ref(q, k, v, scale, causal, window=window)
+    o = o_own if o is None else to_f64(o)
     s = scores(q, k, scale)
     if causal:
         s = causal_mask(s, np.arange(n), np.arange(k.shape[0]))
@@ -139,13 +143,15 @@ def attention_bwd_head_ref(q, k, v, do, scale, causal, window=None):
 
 
 def attention_bwd_sampled_ref(q, k, v, do, scale, causal, rows, cols, chunk=1024,
-                              window=None):
+                              window=None, o_given=None):
     """Selected gradient rows of one head, for heads too long for the full
     matrices: dq at the query rows `rows`, dk and dv at the key rows `cols`.
     O and LSE of every query row come from attention_head_ref over row
     chunks; then, per query row i, the row of P and dP; per key row j, the
     column of P and dP (P_ij = e^{s_ij - LSE_i}, hidden keys 0).  The same
     formulas as attention_bwd_head_ref, evaluated one row or column at a time.
+    ``o_given``: as ``o`` of attention_bwd_head_ref (Delta from the forward
+    output the call is handed; None: this oracle's own O).
     Returns dq[len(rows), D], dk[len(cols), D], dv[len(cols), D]."""
     q, k, v, do = to_f64(q), to_f64(k), to_f64(v), to_f64(do)
     n = q.shape[0]
@@ -154,6 +160,8 @@ def attention_bwd_sampled_ref(q, k, v, do, scale, causal, rows, cols, chunk=1024
     for r0 in range(0, n, chunk):
         r = np.arange(r0, min(n, r0 + chunk))
         o[r], lse[r] = attention_head_ref(q, k, v, scale, causal, rows=r, window=window)
+    if o_given is not None:
+        o = to_f64(o_given)
     delta = (do * o).sum(axis=1)
     pos = np.arange(n)
     dq = np.zeros((len(rows), q.shape[1]))
@@ -179,17 +187,20 @@ def attention_bwd_sampled_ref(q, k, v, do, scale, causal, rows, cols, chunk=1024
     return dq, dk, dv
 
 
-def attention_bwd_ref(q, k, v, do, scale, causal, window=None):
+def attention_bwd_ref(q, k, v, do, scale, causal, window=None, o=None):
     """[B, H, N, D] inputs (any dtype, converted exactly to float64); returns
-    dq, dk, dv [B, H, N, D] and Delta [B, H, N] in float64."""
+    dq, dk, dv [B, H, N, D] and Delta [B, H, N] in float64.  ``o``
+    ([B, H, N, D] or None): as in attention_bwd_head_ref."""
     q, k, v, do = to_f64(q), to_f64(k), to_f64(v), to_f64(do)
+    o = None if o is None else to_f64(o)
     B, H, N, D = q.shape
     dq, dk, dv = (np.zeros((B, H, N, D)) for _ in range(3))
     delta = np.zeros((B, H, N))
     for b in range(B):
         for h in range(H):
             dq[b, h], dk[b, h], dv[b, h], delta[b, h] = attention_bwd_head_ref(
-                q[b, h], k[b, h], v[b, h], do[b, h], scale, causal, window=window)
+                q[b, h], k[b, h], v[b, h], do[b, h], scale, causal, window=window,
+                o=None if o is None else o[b, h])
     return dq, dk, dv, delta
 
 
@@ -270,9 +281,10 @@ def decode_paged_ref(q, k_pages, v_pages, block_table, seqlens, scale,
 
 
 def chunk_states_paged_ref(q, k_pages, v_pages, block_table, seqlens, num_splits,
-                           scale, batch=None, heads=None):
+                           scale, batch=None, heads=None, align=1):
     """Base-2 chunk states of split-KV decode over a paged cache with grouped
-    query heads (chunking as chunk_bounds).  Shapes as chunk_states_ref."""
+    query heads (chunking as chunk_bounds, chunk length rounded up to a
+    multiple of ``align`` keys).  Shapes as chunk_states_ref."""
     q, kp, vp = to_f64(q), to_f64(k_pages), to_f64(v_pages)
     B, H, D = q.shape
     group = H // kp.shape[2]
@@ -284,7 +296,7 @@ def chunk_states_paged_ref(q, k_pages, v_pages, block_table, seqlens, num_splits
         L = int(seqlens[b])
         kc, vc = paged_kv_gather(kp, vp, block_table, L, b)
         for h in (range(H) if heads is None else heads):
-            for c, (a, e) in enumerate(chunk_bounds(L, S)):
+            for c, (a, e) in enumerate(chunk_bounds(L, S, align)):
                 sig = (kc[a:e, h // group] @ q[b, h]) * (float(scale) * LOG2E)
                 M[b, h, c], Dn[b, h, c], Ot[b, h, c] = row_state(
                     sig, vc[a:e, h // group], base=2.0)
@@ -376,8 +388,11 @@ def row_state(s: np.ndarray, v: np.ndarray, base: float = math.e):
 # (sigma = s * log2(e)).
 # ---------------------------------------------------------------------------
 
-def chunk_bounds(L: int, num_splits: int):
+def chunk_bounds(L: int, num_splits: int, align: int = 1):
+    """Chunk c covers keys [c*C, min(L, (c+1)*C)), C = ceil(L / num_splits)
+    rounded up to a multiple of ``align`` (1: no rounding)."""
     size = -(-L // num_splits) if L > 0 else 0
+    size = -(-size // align) * align
     out = []
     for c in range(num_splits):
         a = min(L, c * size)
@@ -526,12 +541,14 @@ def prefix_attention_ref(q, k_cache, v_cache, cu_seqlens_k, scale, batch=None, h
     return O, LSE
 
 
-def attention_bwd_varlen_ref(q, k, v, do, cu_seqlens, scale, causal):
+def attention_bwd_varlen_ref(q, k, v, do, cu_seqlens, scale, causal, o=None):
     """Backward over packed sequences: q, k, v, do [T, H, D]; sequence s owns
     tokens [cu[s], cu[s+1]).  Every (sequence, head) is an independent head
-    of attention_bwd_head_ref.  Returns dq, dk, dv [T, H, D] and Delta [H, T]
+    of attention_bwd_head_ref.  ``o`` ([T, H, D] or None): as in
+    attention_bwd_head_ref.  Returns dq, dk, dv [T, H, D] and Delta [H, T]
     in float64."""
     q, k, v, do = to_f64(q), to_f64(k), to_f64(v), to_f64(do)
+    o = None if o is None else to_f64(o)
     cu = [int(x) for x in np.asarray(cu_seqlens).tolist()]
     T, H, D = q.shape
     dq, dk, dv = (np.zeros((T, H, D)) for _ in range(3))
@@ -541,6 +558,7 @@ def attention_bwd_varlen_ref(q, k, v, do, cu_seqlens, scale, causal):
         if e == a:
             continue
         for h in range(H):
-            g = attention_bwd_head_ref(q[a:e, h], k[a:e, h], v[a:e, h], do[a:e, h], scale, causal)
+            g = attention_bwd_head_ref(q[a:e, h], k[a:e, h], v[a:e, h], do[a:e, h], scale, causal,
+                                       o=None if o is None else o[a:e, h])
             dq[a:e, h], dk[a:e, h], dv[a:e, h], delta[h, a:e] = g
     return dq, dk, dv, delta

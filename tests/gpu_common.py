@@ -66,8 +66,9 @@ def check_lse(lse, ref, tol=TOL_LSE, what=""):
 # zero (sum_j P_ij (dP_ij - Delta_i) = 0), so dQ = scale dS K is a small
 # residual of up to N rounded terms and its relative error grows with N
 # (measured: about 2.5e-3 at N <= 1024, 6.3e-3 at N = 16384).  Per gradient
-# tensor g with oracle value ref, and per row r of it (one query or key
-# position, D values):
+# tensor g with oracle value ref (the gradient formed with the bf16 O the
+# backward call is handed, Delta_i = dO_i . O_i as the call defines it), and
+# per row r of it (one query or key position, D values):
 #   rel-L2(g, ref) <= 1e-2,
 #   max_j(|g_rj - ref_rj| - 2^-8 |ref_rj|) <= 2e-2 max_j|ref_rj| + 1e-3 max|ref|.
 # The bound of a row follows that row's own magnitude; the second term is an
@@ -99,6 +100,25 @@ def check_grad(g, ref, what=""):
                                  f"bound {bound[worst]:.3e} (row max |ref| "
                                  f"{np.abs(r2[worst]).max():.3e})")
     return float(ratio[worst]), r
+
+
+def check_grad_exact(g, ref, what=""):
+    """A gradient tensor against the exact gradient (Delta from the exact O):
+    rel-L2 <= 1e-2 and max(|g - ref| - 2^-8 |ref|) <= 2e-2 max|ref| over the
+    tensor.  The rows of a bf16 forward output differ from the exact O by one
+    rounding, which moves Delta and so each dQ and dK row by an amount that
+    does not follow that row's size; the row-by-row bound applies against
+    the gradient formed from the O a call is handed (check_grad)."""
+    g = np.asarray(g, np.float64)
+    assert np.isfinite(g).all(), f"{what}: non-finite gradient"
+    if g.size == 0:
+        return 0.0, 0.0
+    scale = float(np.abs(ref).max()) or 1.0
+    excess = float((np.abs(g - ref) - BF16_U * np.abs(ref)).max()) / scale
+    r = rel_l2(g, ref)
+    assert r <= TOL_BWD_REL_L2, f"{what}: rel-L2 {r:.3e} > {TOL_BWD_REL_L2}"
+    assert excess <= TOL_BWD_MAX, f"{what}: max excess {excess:.3e} x max|ref| > {TOL_BWD_MAX}"
+    return excess, r
 
 
 def report(name: str, **values) -> None:

@@ -1,7 +1,14 @@
 """GPU parity of the backward by recomputation (fa_bwd through the binding)
 against the float64 oracle on the same seeded inputs: small shapes element by
 element, the full-size causal head on sampled rows and columns, the
-degenerate scale 0, determinism and argument checks."""
+degenerate scale 0, determinism and argument checks.
+
+The backward is handed the forward's O and LSE.  In the parity tests these
+come from the oracle's forward, rounded as a bf16 forward returns them (O to
+bf16, LSE to fp32), so no oracle input comes from the GPU.  Each gradient is
+checked row by row against the oracle's gradient formed with that same bf16
+O (Delta_i = dO_i . O_i, as the call defines it), and as a tensor against
+the exact gradient (Delta from the exact O)."""
 import ctypes
 
 import numpy as np
@@ -10,7 +17,7 @@ import torch
 
 import fa_inputs as inp
 from oracle import attention as ora
-from tests.gpu_common import check_grad, np64
+from tests.gpu_common import check_grad, check_grad_exact, np64
 
 pytestmark = pytest.mark.gpu
 
@@ -31,6 +38,35 @@ def _run(fa, case, do):
     return dq, dk, dv
 
 
+def _oracle_fwd(q, k, v, scale, causal, window=None):
+    """The oracle's O and LSE, rounded as a bf16 forward returns them."""
+    O, L = ora.attention_ref(q, k, v, scale, causal, window=window)
+    return torch.from_numpy(O).to(torch.bfloat16), torch.from_numpy(L).to(torch.float32)
+
+
+def _check_both(grads, ref_given, ref_exact, tag):
+    for name, g, rg, re in zip(("dq", "dk", "dv"), grads, ref_given, ref_exact):
+        check_grad(np64(g), rg, f"{name} {tag}")
+        check_grad_exact(np64(g), re, f"{name} {tag} (exact gradient)")
+
+
+def _bwd_dense_checked(fa, case, do, causal, tag, window=None):
+    o_in, lse_in = _oracle_fwd(case.q, case.k, case.v, case.scale, causal, window)
+    q, k, v = case.q.cuda(), case.k.cuda(), case.v.cuda()
+    if window is None:
+        g = fa.fa_bwd(q, k, v, o_in.cuda(), do.cuda(), lse_in.cuda(), case.scale, causal)
+    else:
+        g = fa.fa_bwd_window(q, k, v, o_in.cuda(), do.cuda(), lse_in.cuda(), window, case.scale)
+    torch.cuda.synchronize()
+    assert fa.fa_check_device_status() == fa.FA_OK
+    rg = ora.attention_bwd_ref(case.q, case.k, case.v, do, case.scale, causal, window=window,
+                               o=o_in)[:3]
+    re = ora.attention_bwd_ref(case.q, case.k, case.v, do, case.scale, causal,
+                               window=window)[:3]
+    _check_both(g, rg, re, tag)
+    return g
+
+
 SHAPES = [
     # (B, H, N, D, causal): one row, exact tiles, ragged tails, both head dims
     (1, 1, 1, 64, False),
@@ -48,23 +84,14 @@ SHAPES = [
 def test_bwd_small(fa, B, H, N, D, causal):
     case = inp.dense(B, H, N, D, seed=900 + N + D, causal=causal)
     do = inp.output_grad((B, H, N, D), seed=901 + N)
-    dq, dk, dv = _run(fa, case, do)
-    rq, rk, rv, _ = ora.attention_bwd_ref(case.q, case.k, case.v, do, case.scale, causal)
-    tag = (B, H, N, D, causal)
-    check_grad(np64(dq), rq, f"dq {tag}")
-    check_grad(np64(dk), rk, f"dk {tag}")
-    check_grad(np64(dv), rv, f"dv {tag}")
+    _bwd_dense_checked(fa, case, do, causal, (B, H, N, D, causal))
 
 
 def test_bwd_large_scores(fa):
     """q, k with std 2 (peaked softmax rows, large LSE)."""
     case = inp.dense(1, 2, 384, 128, seed=930, causal=True, qk_std=2.0)
     do = inp.output_grad((1, 2, 384, 128), seed=931)
-    dq, dk, dv = _run(fa, case, do)
-    rq, rk, rv, _ = ora.attention_bwd_ref(case.q, case.k, case.v, do, case.scale, True)
-    check_grad(np64(dq), rq, "dq std2")
-    check_grad(np64(dk), rk, "dk std2")
-    check_grad(np64(dv), rv, "dv std2")
+    _bwd_dense_checked(fa, case, do, True, "std2")
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -75,7 +102,8 @@ def test_bwd_scale_zero(fa, causal):
     dq, dk, dv = _run(fa, case, do)
     assert not dq.any() and not dk.any()
     _, _, rv, _ = ora.attention_bwd_ref(case.q, case.k, case.v, do, 0.0, causal)
-    check_grad(np64(dv), rv, "dv scale0")
+    check_grad_exact(np64(dv), rv, "dv scale0")
+    check_grad(np64(dv), rv, "dv scale0")  # dV does not depend on Delta
 
 
 def test_bwd_deterministic(fa):
@@ -94,16 +122,48 @@ def test_bwd_full_size_sampled(fa):
     B, H, N, D = 1, 32, 16384, 128
     case = inp.dense(B, H, N, D, seed=960, causal=True)
     do = inp.output_grad((B, H, N, D), seed=961)
-    dq, dk, dv = _run(fa, case, do)
     rng = np.random.default_rng(962)
     picks = sorted(set([0, 1, 127, 128, 8191, 8192, N - 129, N - 128, N - 1]) |
                    set(rng.integers(0, N, 23).tolist()))
-    for h in (0, H - 1):
-        rq, rk, rv = ora.attention_bwd_sampled_ref(case.q[0, h], case.k[0, h], case.v[0, h],
-                                                   do[0, h], case.scale, True, picks, picks)
-        check_grad(np64(dq[0, h, picks]), rq, f"dq head {h}")
-        check_grad(np64(dk[0, h, picks]), rk, f"dk head {h}")
-        check_grad(np64(dv[0, h, picks]), rv, f"dv head {h}")
+    _full_size_sampled(fa, case, do, picks, "")
+
+
+def _full_size_sampled(fa, case, do, picks, tag, window=None):
+    """Heads 0 and H-1 of a [1, H, N, D] problem: their O and LSE from the
+    oracle (rounded as the bf16 forward returns them), the other heads' from
+    the GPU forward (not checked); sampled rows of dq, dk, dv against both
+    oracle gradients."""
+    B, H, N, D = case.q.shape
+    q, k, v = case.q.cuda(), case.k.cuda(), case.v.cuda()
+    if window is None:
+        o, lse = fa.fa_fwd(q, k, v, case.scale, True)
+    else:
+        o, lse = fa.fa_fwd_window(q, k, v, window, case.scale)
+    heads = (0, H - 1)
+    o_in = {}
+    for h in heads:
+        O = np.zeros((N, D))
+        L = np.zeros(N)
+        for r0 in range(0, N, 2048):
+            r = np.arange(r0, min(N, r0 + 2048))
+            O[r], L[r] = ora.attention_head_ref(ora.to_f64(case.q[0, h]), ora.to_f64(case.k[0, h]),
+                                                ora.to_f64(case.v[0, h]), case.scale, True,
+                                                rows=r, window=window)
+        o_in[h] = torch.from_numpy(O).to(torch.bfloat16)
+        o[0, h] = o_in[h].cuda()
+        lse[0, h] = torch.from_numpy(L).to(torch.float32).cuda()
+    if window is None:
+        dq, dk, dv = fa.fa_bwd(q, k, v, o, do.cuda(), lse, case.scale, True)
+    else:
+        dq, dk, dv = fa.fa_bwd_window(q, k, v, o, do.cuda(), lse, window, case.scale)
+    torch.cuda.synchronize()
+    assert fa.fa_check_device_status() == fa.FA_OK
+    for h in heads:
+        args = (case.q[0, h], case.k[0, h], case.v[0, h], do[0, h], case.scale, True, picks, picks)
+        rg = ora.attention_bwd_sampled_ref(*args, window=window, o_given=o_in[h])
+        re = ora.attention_bwd_sampled_ref(*args, window=window)
+        got = (dq[0, h, picks], dk[0, h, picks], dv[0, h, picks])
+        _check_both(got, rg, re, f"{tag}head {h}")
 
 
 def test_bwd_invalid_args(fa):
@@ -133,6 +193,31 @@ def test_bwd_invalid_args(fa):
 
 # --- packed sequences -------------------------------------------------------------
 
+def _varlen_checked(fa, case, do, causal, tag):
+    """Packed backward on the oracle's O and LSE (rounded as the bf16
+    forward returns them), checked against both oracle gradients."""
+    T, H, D = case.q.shape
+    ref = ora.varlen_ref(case.q, case.k, case.v, case.cu_seqlens, case.scale, causal)
+    cuh = case.cu_seqlens.tolist()
+    O = np.zeros((T, H, D))
+    L = np.zeros((H, T))
+    for s_, (Os, Ls) in ref.items():
+        O[cuh[s_]:cuh[s_ + 1]] = Os
+        L[:, cuh[s_]:cuh[s_ + 1]] = Ls
+    o_in = torch.from_numpy(O).to(torch.bfloat16)
+    lse_in = torch.from_numpy(L).to(torch.float32)
+    cu = case.cu_seqlens.cuda()
+    g = fa.fa_bwd_varlen(case.q.cuda(), case.k.cuda(), case.v.cuda(), o_in.cuda(), do.cuda(),
+                         lse_in.cuda(), cu, case.max_seqlen, case.scale, causal)
+    torch.cuda.synchronize()
+    assert fa.fa_check_device_status() == fa.FA_OK
+    rg = ora.attention_bwd_varlen_ref(case.q, case.k, case.v, do, case.cu_seqlens, case.scale,
+                                      causal, o=o_in)[:3]
+    re = ora.attention_bwd_varlen_ref(case.q, case.k, case.v, do, case.cu_seqlens, case.scale,
+                                      causal)[:3]
+    _check_both(g, rg, re, tag)
+
+
 def _varlen_run(fa, case, do, causal):
     cu = case.cu_seqlens.cuda()
     q, k, v = case.q.cuda(), case.k.cuda(), case.v.cuda()
@@ -150,12 +235,7 @@ def test_bwd_varlen(fa, D, causal):
     lens = [1, 100, 128, 129, 300]
     case = inp.varlen(lens, H=2, D=D, seed=970 + D, causal=causal)
     do = inp.output_grad(tuple(case.q.shape), seed=971)
-    dq, dk, dv = _varlen_run(fa, case, do, causal)
-    rq, rk, rv, _ = ora.attention_bwd_varlen_ref(case.q, case.k, case.v, do, case.cu_seqlens,
-                                                 case.scale, causal)
-    check_grad(np64(dq), rq, f"varlen dq D={D}")
-    check_grad(np64(dk), rk, f"varlen dk D={D}")
-    check_grad(np64(dv), rv, f"varlen dv D={D}")
+    _varlen_checked(fa, case, do, causal, f"varlen D={D}")
 
 
 def test_bwd_varlen_one_sequence_equals_dense(fa):
@@ -192,14 +272,7 @@ def test_bwd_window(fa, D, w):
     N = 517
     case = inp.dense(1, 2, N, D, seed=980 + w, causal=True)
     do = inp.output_grad((1, 2, N, D), seed=981 + w)
-    q, k, v = case.q.cuda(), case.k.cuda(), case.v.cuda()
-    o, lse = fa.fa_fwd_window(q, k, v, w, case.scale)
-    g = fa.fa_bwd_window(q, k, v, o, do.cuda(), lse, w, case.scale)
-    torch.cuda.synchronize()
-    assert fa.fa_check_device_status() == fa.FA_OK
-    refs = ora.attention_bwd_ref(case.q, case.k, case.v, do, case.scale, True, window=w)[:3]
-    for name, x, ref in zip(("dq", "dk", "dv"), g, refs):
-        check_grad(np64(x), ref, f"window {w} D={D} {name}")
+    _bwd_dense_checked(fa, case, do, True, f"window {w} D={D}", window=w)
 
 
 def test_bwd_window_at_least_n_equals_causal(fa):
@@ -221,17 +294,6 @@ def test_bwd_window_full_size_sampled(fa):
     B, H, N, D, w = 1, 32, 16384, 128, 4096
     case = inp.dense(B, H, N, D, seed=987, causal=True)
     do = inp.output_grad((B, H, N, D), seed=988)
-    q, k, v = case.q.cuda(), case.k.cuda(), case.v.cuda()
-    o, lse = fa.fa_fwd_window(q, k, v, w, case.scale)
-    dq, dk, dv = fa.fa_bwd_window(q, k, v, o, do.cuda(), lse, w, case.scale)
-    torch.cuda.synchronize()
-    assert fa.fa_check_device_status() == fa.FA_OK
     rng = np.random.default_rng(989)
     picks = sorted(set([0, 127, 128, w - 1, w, 8191, N - 1]) | set(rng.integers(0, N, 13).tolist()))
-    for h in (0, H - 1):
-        rq, rk, rv = ora.attention_bwd_sampled_ref(case.q[0, h], case.k[0, h], case.v[0, h],
-                                                   do[0, h], case.scale, True, picks, picks,
-                                                   window=w)
-        check_grad(np64(dq[0, h, picks]), rq, f"window dq head {h}")
-        check_grad(np64(dk[0, h, picks]), rk, f"window dk head {h}")
-        check_grad(np64(dv[0, h, picks]), rv, f"window dv head {h}")
+    _full_size_sampled(fa, case, do, picks, "window ", window=w)

@@ -60,8 +60,8 @@ def test_decode_graph_replay(fa):
     q = d.q.clone()
     pm, pd, po = (torch.empty(s, dtype=torch.float32, device="cuda")
                   for s in ((8, 8, S), (8, 8, S), (8, 8, S, 128)))
-    out = torch.empty((8 * 8, 128), dtype=torch.bfloat16, device="cuda")
-    lse = torch.empty(8 * 8, dtype=torch.float32, device="cuda")
+    out = torch.empty((8, 8, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((8, 8), dtype=torch.float32, device="cuda")
 
     def step():
         fa.fa_decode_splitkv(q, d.k_cache, d.v_cache, cu, S, d.scale, pm, pd, po)

@@ -61,6 +61,12 @@ def test_window_invalid(fa):
 
 # --- paged KV cache, grouped query heads -------------------------------------------
 
+def _paged_align(H, Hkv, page, D):
+    """Chunk length granularity of fa_decode_paged_splitkv: whole 128-key
+    tiles on the grouped-head tensor-core path, single keys otherwise."""
+    return 128 if D == 128 and 2 <= H // Hkv <= 16 and page >= 8 else 1
+
+
 def _paged_gpu(case):
     return (case.q.cuda(), case.k_pages.cuda(), case.v_pages.cuda(),
             case.block_table.cuda(), case.seqlens.cuda())
@@ -75,7 +81,8 @@ def test_paged_decode(fa, H, Hkv, page, S, D):
     args = _paged_gpu(case)
     pm, pd, po = fa.fa_decode_paged_splitkv(*args, S, case.scale)
     M, Dn, Oc = ora.chunk_states_paged_ref(case.q, case.k_pages, case.v_pages,
-                                           case.block_table, case.seqlens, S, case.scale)
+                                           case.block_table, case.seqlens, S, case.scale,
+                                           align=_paged_align(H, Hkv, page, D))
     full = np.isfinite(M)
     assert (np64(pm)[~full] == -np.inf).all() and (np64(pd)[~full] == 0).all()
     assert np.abs(np64(pm)[full] - M[full]).max() <= 1e-4 * max(1.0, np.abs(M[full]).max())
@@ -102,7 +109,8 @@ def test_paged_decode_tensor_core_groups(fa, H, Hkv, page, S):
     torch.cuda.synchronize()
     assert fa.fa_check_device_status() == fa.FA_OK
     M, Dn, Oc = ora.chunk_states_paged_ref(case.q, case.k_pages, case.v_pages,
-                                           case.block_table, case.seqlens, S, case.scale)
+                                           case.block_table, case.seqlens, S, case.scale,
+                                           align=128)
     full = np.isfinite(M)
     assert (np64(pm)[~full] == -np.inf).all() and (np64(pd)[~full] == 0).all()
     assert np.abs(np64(pm)[full] - M[full]).max() <= 1e-4 * max(1.0, np.abs(M[full]).max())

@@ -332,6 +332,21 @@ def test_chunk_bounds_cover(L, S):
     assert all(e - a <= size for a, e in b)
 
 
+@pytest.mark.parametrize("L,S,align", [(1, 16, 128), (127, 2, 128), (1024, 16, 128),
+                                       (1025, 16, 128), (3001, 5, 128), (700, 7, 64)])
+def test_chunk_bounds_aligned(L, S, align):
+    """Aligned chunking: the chunks still tile [0, L) in order, every
+    boundary but the end is a multiple of align, and the chunk length is
+    ceil(L / S) rounded up to such a multiple (trailing chunks may be empty)."""
+    b = ora.chunk_bounds(L, S, align)
+    assert len(b) == S and b[0][0] == 0 and b[-1][1] == L
+    for (a0, a1), (b0, _) in zip(b, b[1:]):
+        assert a1 == b0 and a0 <= a1
+    assert all(a % align == 0 for a, _ in b if a < L)
+    size = -(-(-(-L // S)) // align) * align
+    assert all(e - a == min(size, max(0, L - a)) for a, e in b)
+
+
 def _decode_case(B=3, H=2, D=8, lens=(1, 9, 40), seed=0, std=2.0):
     rng = np.random.default_rng(seed)
     T = sum(lens)

@@ -152,3 +152,39 @@ def test_window_at_least_n_and_sampled():
     np.testing.assert_allclose(sq, full[0][pick], rtol=1e-11, atol=1e-13)
     np.testing.assert_allclose(sk, full[1][pick], rtol=1e-11, atol=1e-13)
     np.testing.assert_allclose(sv, full[2][pick], rtol=1e-11, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_given_output_shifts_delta_only(causal):
+    """A backward call is handed the forward output o and forms Delta_i =
+    dO_i . o_i from it.  With o = O + E (E a perturbation, e.g. the rounding
+    of O to bf16) only Delta moves, by -dO_i . E_i, so in closed form
+        dV' = dV,
+        dQ'_i = dQ_i + scale (Delta_i - Delta'_i) sum_j P_ij k_j,
+        dK'_j = dK_j + scale sum_i P_ij (Delta_i - Delta'_i) q_i,
+    with P the softmax of the scores, here from torch in float64; the
+    unperturbed gradients are pinned by finite differences above.  The
+    sampled form with o_given agrees with the full form."""
+    N, D, scale = 40, 8, 0.45
+    q, k, v, do = _case(N, D, 21 + causal, std=1.3)
+    rng = np.random.default_rng(5)
+    o_exact, _ = ora.attention_head_ref(q, k, v, scale, causal)
+    o_given = o_exact + 1e-3 * rng.standard_normal(o_exact.shape)
+    dq, dk, dv, delta = ora.attention_bwd_head_ref(q, k, v, do, scale, causal)
+    dq2, dk2, dv2, delta2 = ora.attention_bwd_head_ref(q, k, v, do, scale, causal, o=o_given)
+    s = torch.from_numpy(q @ k.T * scale)
+    if causal:
+        s = s.masked_fill(torch.ones(N, N, dtype=torch.bool).triu(1), float("-inf"))
+    p = torch.softmax(s, dim=-1).numpy()
+    shift = delta - delta2
+    np.testing.assert_allclose(delta2, (do * o_given).sum(1), rtol=1e-13, atol=1e-13)
+    np.testing.assert_array_equal(dv2, dv)
+    np.testing.assert_allclose(dq2, dq + scale * shift[:, None] * (p @ k), rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(dk2, dk + scale * (p * shift[:, None]).T @ q, rtol=1e-9,
+                               atol=1e-12)
+    picks = [0, 1, 17, N - 1]
+    sq, sk, sv = ora.attention_bwd_sampled_ref(q, k, v, do, scale, causal, picks, picks,
+                                               chunk=16, o_given=o_given)
+    np.testing.assert_allclose(sq, dq2[picks], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(sk, dk2[picks], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(sv, dv2[picks], rtol=1e-10, atol=1e-12)
