@@ -7,9 +7,10 @@
 // row is read off as o / d ("The State").
 //
 // One warp per row; lane l owns D/32 consecutive columns, so each chunk's
-// partial o row is one coalesced 512-byte (D = 128) read.  A lane loads the
+// partial o row is one coalesced 512-byte (D = 128) read.  A warp loads the
 // states of 16 chunks at a time before folding them, so a row waits for
-// memory once per 16 chunks rather than once per chunk.  Chunks are folded
+// memory once per 16 chunks rather than once per chunk, and the 16 merge
+// factors of a batch are computed at once, one per lane.  Chunks are folded
 // in index order 0, 1, ..., S-1 starting from the identity, with no atomics,
 // so the result does not depend on the launch.  Every arithmetic step is a
 // single IEEE binary32 operation with round-to-nearest (the __f*_rn
@@ -118,48 +119,69 @@ __global__ void __launch_bounds__(256) fa_combine_kernel(const CombineArgs a) {
   for (int i = 0; i < VPL; ++i) o[i] = 0.0f;
 
   for (int c0 = 0; c0 < S; c0 += kBatch) {
-    // All loads of the batch first (one memory latency per batch), then the
-    // fold in chunk order.
-    float mb[kBatch], db[kBatch], ob[kBatch][VPL];
+    // All loads of the batch first (one memory latency per batch): every
+    // lane its columns of the 16 partial o rows, lane i < 16 the m and d of
+    // chunk c0 + i.
+    float ob[kBatch][VPL];
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
+#pragma unroll
+      for (int k = 0; k < VPL; ++k) ob[i][k] = 0.0f;
       if (c0 + i < S) {
-        const int c = c0 + i;
-        mb[i] = __ldg(pm + c);
-        db[i] = __ldg(pd + c);
+        const size_t c = static_cast<size_t>(c0 + i);
         if constexpr (VPL == 4) {
-          const float4 x =
-              __ldg(reinterpret_cast<const float4*>(po + static_cast<size_t>(c) * D));
+          const float4 x = __ldg(reinterpret_cast<const float4*>(po + c * D));
           ob[i][0] = x.x; ob[i][1] = x.y; ob[i][2] = x.z; ob[i][3] = x.w;
         } else {
-          const float2 x =
-              __ldg(reinterpret_cast<const float2*>(po + static_cast<size_t>(c) * D));
+          const float2 x = __ldg(reinterpret_cast<const float2*>(po + c * D));
           ob[i][0] = x.x; ob[i][1] = x.y;
         }
       }
     }
+    float my_m = -INFINITY, my_d = 0.0f;  // past the last chunk: the identity
+    if (lane < kBatch && c0 + lane < S) {
+      my_m = __ldg(pm + c0 + lane);
+      my_d = __ldg(pd + c0 + lane);
+    }
+    // The running maximum before each chunk follows from the chunks' m alone
+    // (the merge keeps the larger one), so lane i can compute chunk c0 + i's
+    // merge factor while the other lanes compute theirs; the fold below then
+    // applies them in chunk order.  Each factor is the same operation on the
+    // same operands as in a serial fold.
+    float my_mprev = m;
+    {
+      float mr = m;
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const float mbi = __shfl_sync(0xffffffffu, my_m, i);
+        if (lane == i) my_mprev = mr;
+        if (mbi != -INFINITY && (mr == -INFINITY || !(mr >= mbi))) mr = mbi;
+      }
+    }
+    const float my_f = sw_exp2(my_mprev >= my_m ? __fsub_rn(my_m, my_mprev)
+                                                : __fsub_rn(my_mprev, my_m));
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
-      if (c0 + i >= S) break;
-      if (mb[i] == -INFINITY) continue;  // chunk c0 + i is the identity
-      if (m == -INFINITY) {              // the running state is the identity
-        m = mb[i];
-        d = db[i];
+      const float mbi = __shfl_sync(0xffffffffu, my_m, i);
+      const float dbi = __shfl_sync(0xffffffffu, my_d, i);
+      const float fi = __shfl_sync(0xffffffffu, my_f, i);
+      if (mbi == -INFINITY) continue;  // chunk c0 + i is the identity
+      if (m == -INFINITY) {            // the running state is the identity
+        m = mbi;
+        d = dbi;
 #pragma unroll
         for (int k = 0; k < VPL; ++k) o[k] = ob[i][k];
         continue;
       }
-      if (m >= mb[i]) {
-        const float f = sw_exp2(__fsub_rn(mb[i], m));
-        d = __fmaf_rn(db[i], f, d);
+      if (m >= mbi) {
+        d = __fmaf_rn(dbi, fi, d);
 #pragma unroll
-        for (int k = 0; k < VPL; ++k) o[k] = __fmaf_rn(ob[i][k], f, o[k]);
+        for (int k = 0; k < VPL; ++k) o[k] = __fmaf_rn(ob[i][k], fi, o[k]);
       } else {
-        const float f = sw_exp2(__fsub_rn(m, mb[i]));
-        d = __fmaf_rn(d, f, db[i]);
+        d = __fmaf_rn(d, fi, dbi);
 #pragma unroll
-        for (int k = 0; k < VPL; ++k) o[k] = __fmaf_rn(o[k], f, ob[i][k]);
-        m = mb[i];
+        for (int k = 0; k < VPL; ++k) o[k] = __fmaf_rn(o[k], fi, ob[i][k]);
+        m = mbi;
       }
     }
   }

@@ -31,33 +31,33 @@
 //
 // Roles (224 threads):
 //   warp 0      TMA producer: Q once, then K and V tiles into two rings of
-//               stages, in the order the MMA issuer consumes them
-//               (K_0, K_1, then V_j, K_{j+2} for each j).
-//   warp 1      QK issuer (one thread): S = Q K_j^T into the one TMEM S
-//               buffer (SS form), once K_j has landed, the softmax warps have
-//               loaded S_{j-1} into registers, and P_{j-4} V_{j-4} has
-//               finished with P buffer j % 4.  QK_{j+1} runs during the
-//               softmax of tile j.
+//               stages, in the order the MMA issuers consume them
+//               (K_0 .. K_{KS-1}, then V_j, K_{j+KS} for each j).
+//   warp 1      QK issuer (one thread): S_j = Q K_j^T into TMEM S buffer
+//               j % 3 (SS form), once K_j has landed and P_{j-3} V_{j-3} has
+//               finished with that buffer.  With three S buffers the
+//               products run up to two tiles ahead of the softmax, so the
+//               softmax warps never wait for S.
 //   warp 6      PV issuer (one thread): O += P_j V_j with P_j read from TMEM
-//               (TS form, P_j in TMEM buffer j % 4) once the softmax has
-//               written P_j (and, on the rare tiles that need it, rescaled O).
-//               Two issuing threads keep the tensor pipe fed: one thread
-//               issues an M=128 K=16 product about every 80-90 cycles at best,
-//               while two threads together reach one per ~65 cycles at
-//               N = 128, the pipe's own rate.
+//               (TS form, P_j over the second half of S buffer j % 3) once
+//               the softmax has written P_j (and, on the rare tiles that
+//               need it, rescaled O).  Two issuing threads keep the tensor
+//               pipe fed: one thread issues an M=128 K=16 product about
+//               every 80-90 cycles at best, while two threads together reach
+//               one per ~65 cycles at N = 128, the pipe's own rate.
 //   warps 2..5  softmax: thread t owns row 32*(warp%4) + lane; per tile it
-//               loads its raw S row (then releases the S buffer), masks,
-//               takes the row max (3-input max instructions, sixteen
-//               independent chains), moves its reference maximum if the
-//               tile's exceeds it by more than kRescaleLog2, computes p =
-//               2^(s c - m) with one packed fused multiply-add per pair of
-//               columns, rounds P to bf16 into TMEM buffer j % 4 (free: S_j
-//               was issued after the product that last read it had
-//               finished), sums p with packed adds, and, on the rare tiles
-//               where a row of the warp moved its reference, waits for
-//               P_{j-1} V_{j-1} and rescales its O row in TMEM by alpha_j =
-//               2^(m_old - m_new) (the rescale half of the merge); then it
-//               signals P_j.
+//               loads its raw S row, masks, takes the row max (3-input max
+//               instructions, sixteen independent chains), moves its
+//               reference maximum if the tile's exceeds it by more than
+//               kRescaleLog2, computes p = 2^(s c - m) with one packed fused
+//               multiply-add per pair of columns, rounds P to bf16 over the
+//               second half of the tile's S buffer (those scores are in
+//               registers by then), sums p with packed adds (four chains),
+//               and, on the
+//               rare tiles where a row of the warp moved its reference,
+//               waits for P_{j-1} V_{j-1} and rescales its O row in TMEM by
+//               alpha_j = 2^(m_old - m_new) (the rescale half of the merge);
+//               then it signals P_j.
 //               Epilogue: O / d' in fp32 (d' = d less the largest weights'
 //               rounding), LSE = ln2 (m + log2 d), stores (bf16 O at
 //               D = 128: staged in Q's buffer, one TMA store per warp and
@@ -67,8 +67,9 @@
 // mbarriers.  A 128 x D bf16 tile is stored as D/64 column halves of
 // 128 rows x 128 bytes, 128-byte swizzled (the TMA box layout and the
 // canonical K-major / MN-major tcgen05 operand layouts).
-// Tensor memory (512 columns): S [0,128), O [128, 128 + D), P_0..P_3 at
-// [256 + 64 i, 320 + 64 i) (bf16 pairs, 64 columns per 128 keys).
+// Tensor memory (512 columns): S buffers at [128 b, 128 b + 128) for b < 3
+// (P_j, bf16 pairs, over columns [64, 128) of its buffer) and O at
+// [384, 384 + D).
 
 #include <cuda.h>
 #include <atomic>
@@ -93,31 +94,31 @@ struct TcCfg {
   static constexpr uint32_t TILE_BYTES = HALVES * HALF_BYTES;
   static constexpr int KS = 2;  // K ring stages
   static constexpr int VS = 3;  // V ring stages
-  static constexpr int NP = 4;  // P buffers in TMEM
+  static constexpr int NS = 3;  // S buffers in TMEM (P_j is written over S_j)
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + KS * TILE_BYTES;
   static constexpr uint32_t OFF_BAR = OFF_V + VS * TILE_BYTES;
-  // barrier indices.  V_EMPTY(s) completes when the P V product that read V
-  // stage s has finished; PV_DONE(i) when the one that read P buffer i has
-  // (P_j V_j has finished: O holds it and P buffer j % NP is free).
+  // barrier indices, one per stage or buffer.  V_EMPTY(s) completes when the
+  // P V product that read V stage s has finished; S_FULL(b) when Q K_j^T is
+  // in S buffer b = j % NS, P_FULL(b) when the softmax warps have written
+  // P_j over it, PV_DONE(b) when P_j V_j has finished (O holds it and S
+  // buffer b is free for Q K_{j+NS}^T).
   static constexpr int B_Q_FULL = 0;
   static constexpr int B_K_FULL = 1;
   static constexpr int B_V_FULL = B_K_FULL + KS;
   static constexpr int B_K_EMPTY = B_V_FULL + VS;
   static constexpr int B_V_EMPTY = B_K_EMPTY + KS;
   static constexpr int B_S_FULL = B_V_EMPTY + VS;
-  static constexpr int B_S_FREE = B_S_FULL + 1;  // S loaded by the softmax warps
-  static constexpr int B_P_FULL = B_S_FREE + 1;  // one per P buffer
-  static constexpr int B_PV_DONE = B_P_FULL + NP;
-  static constexpr int B_DRAIN = B_PV_DONE + NP;  // one per issuing thread
+  static constexpr int B_P_FULL = B_S_FULL + NS;
+  static constexpr int B_PV_DONE = B_P_FULL + NS;
+  static constexpr int B_DRAIN = B_PV_DONE + NS;  // one per issuing thread
   static constexpr int NUM_BARS = B_DRAIN + 2;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t TMEM_S = 0;
-  static constexpr uint32_t TMEM_O = 128;
-  static constexpr uint32_t TMEM_P = 256;  // buffer i at TMEM_P + 64 i
+  static constexpr uint32_t TMEM_S = 0;    // buffer b at TMEM_S + 128 b
+  static constexpr uint32_t TMEM_O = 384;
   static constexpr int THREADS = 224;
   static constexpr int WARP_PV = 6;
   static constexpr int SOFTMAX_THREADS = 128;
@@ -253,9 +254,8 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
       mbar_init(bar(C::B_V_FULL + s), 1);
       mbar_init(bar(C::B_V_EMPTY + s), 1);
     }
-    mbar_init(bar(C::B_S_FULL), 1);
-    mbar_init(bar(C::B_S_FREE), C::SOFTMAX_THREADS);
-    for (int b = 0; b < C::NP; ++b) {
+    for (int b = 0; b < C::NS; ++b) {
+      mbar_init(bar(C::B_S_FULL + b), 1);
       mbar_init(bar(C::B_P_FULL + b), C::SOFTMAX_THREADS);
       mbar_init(bar(C::B_PV_DONE + b), 1);
     }
@@ -273,8 +273,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
       tile_coords(c, mb * C::BM, c0, c1, c2);
       tma_load_3d(sbase + C::OFF_Q + c * C::HALF_BYTES, &tm_q, qb, c0, c1, c2);
     }
-    load(false, 0);
-    if (n_kv >= 2) load(false, 1);
+    for (int jk = 0; jk < C::KS && jk < n_kv; ++jk) load(false, jk);
     load(true, 0);
   }
   if (warp == 1) {
@@ -289,16 +288,16 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
   if (warp == 0) {
     // ======================= TMA producer =======================
     if (lane == 0) {
-      // Q, K_0, K_1 and V_0 were issued before the CTA barrier.
-      int k_issued = min(n_kv, 2), v_issued = 1;
+      // Q, K_0 .. K_{KS-1} and V_0 were issued before the CTA barrier.
+      int k_issued = min(n_kv, C::KS), v_issued = 1;
       for (int j = 0; j < n_kv; ++j) {
         if (j > 0) {
           if (!load(true, j)) break;
           v_issued = j + 1;
         }
-        if (j + 2 < n_kv) {
-          if (!load(false, j + 2)) break;
-          k_issued = j + 3;
+        if (j + C::KS < n_kv) {
+          if (!load(false, j + C::KS)) break;
+          k_issued = j + C::KS + 1;
         }
       }
       if (*abort_flag) {
@@ -320,20 +319,19 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
       const uint32_t q_s = sbase + C::OFF_Q;
       bool ok = mbar_wait(bar(C::B_Q_FULL), 0, abort_flag, args.status, wlim);
       for (int j = 0; ok && j < n_kv; ++j) {
-        // The S buffer is free once the softmax warps have loaded S_{j-1};
-        // P buffer j % 4, which the softmax of tile j writes, once
-        // P_{j-4} V_{j-4} has finished.
+        // S buffer j % NS is free once P_{j-NS} V_{j-NS}, which read the P
+        // written over it, has finished (the softmax warps loaded S_{j-NS}
+        // before writing that P).
         if (!mbar_wait(bar(C::B_K_FULL + j % C::KS), (j / C::KS) & 1, abort_flag,
-                       args.status) ||
-            (j >= 1 && !mbar_wait(bar(C::B_S_FREE), (j - 1) & 1, abort_flag, args.status, wlim)) ||
-            (j >= C::NP && !mbar_wait(bar(C::B_PV_DONE + j % C::NP), ((j - C::NP) / C::NP) & 1,
+                       args.status, wlim) ||
+            (j >= C::NS && !mbar_wait(bar(C::B_PV_DONE + j % C::NS), ((j - C::NS) / C::NS) & 1,
                                       abort_flag, args.status, wlim))) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t k_s = sbase + C::OFF_K + (j % C::KS) * C::TILE_BYTES;
-        const uint32_t s_t = tmem + C::TMEM_S;
+        const uint32_t s_t = tmem + C::TMEM_S + 128u * (j % C::NS);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           // 16-column slice kk of the head dimension: half kk/4, 32 bytes
@@ -342,7 +340,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
           tc_mma_ss(s_t, sdesc_sw128(q_s + off, 16u, 1024u), sdesc_sw128(k_s + off, 16u, 1024u),
                     idesc_qk, kk > 0 ? 1u : 0u);
         }
-        tc_commit(bar(C::B_S_FULL));
+        tc_commit(bar(C::B_S_FULL + j % C::NS));
         tc_commit(bar(C::B_K_EMPTY + j % C::KS));
       }
       // Every MMA this thread issued completes before TMEM is released.
@@ -355,12 +353,13 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
       for (int j = 0; j < n_kv; ++j) {
         const int sv = j % C::VS;
-        if (!mbar_wait(bar(C::B_P_FULL + j % C::NP), (j / C::NP) & 1, abort_flag, args.status, wlim) ||
+        if (!mbar_wait(bar(C::B_P_FULL + j % C::NS), (j / C::NS) & 1, abort_flag, args.status, wlim) ||
             !mbar_wait(bar(C::B_V_FULL + sv), (j / C::VS) & 1, abort_flag, args.status, wlim))
           break;
         tc_fence_after();
         const uint32_t v_s = sbase + C::OFF_V + sv * C::TILE_BYTES;
-        const uint32_t p_t = tmem + C::TMEM_P + 64u * (j % C::NP);
+        // P_j lies over the second half of S_j's buffer
+        const uint32_t p_t = tmem + C::TMEM_S + 128u * (j % C::NS) + 64u;
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk) {
           // B = V_j as an MN-major operand: N = D (64-column halves
@@ -370,7 +369,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
                     (j > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(bar(C::B_V_EMPTY + sv));
-        tc_commit(bar(C::B_PV_DONE + j % C::NP));
+        tc_commit(bar(C::B_PV_DONE + j % C::NS));
       }
       tc_commit(bar(C::B_DRAIN + 1));
       mbar_wait_unwind(bar(C::B_DRAIN + 1), 0);
@@ -391,8 +390,10 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
     bool ok = true;
 
     for (int j = 0; j < n_kv; ++j) {
-      const uint32_t s_t = tmem + lane_off + C::TMEM_S;
-      const bool w = mbar_wait(bar(C::B_S_FULL), j & 1, abort_flag, args.status, wlim);
+      const int sb = j % C::NS;
+      const uint32_t s_t = tmem + lane_off + C::TMEM_S + 128u * sb;
+      const bool w = mbar_wait(bar(C::B_S_FULL + sb), (j / C::NS) & 1, abort_flag, args.status,
+                               wlim);
       if (__any_sync(0xffffffffu, !w)) {
         ok = false;
         break;
@@ -409,12 +410,10 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 64; ++i) t[64 + i] = __uint_as_float(raw[i]);
       }
-      // S_j is in registers: QK_{j+1} may overwrite the buffer.
-      tc_fence_before();
-      mbar_arrive(bar(C::B_S_FREE));
       const int kbase = (j0 + j) * C::BN;
       const bool win_edge = args.window > 0 && kbase < mb * C::BM + C::BM - args.window;
-      if ((args.causal && j0 + j == mb) || kbase + C::BN > L || win_edge) {
+      const bool masked = (args.causal && j0 + j == mb) || kbase + C::BN > L || win_edge;
+      if (masked) {
         int lim = L - kbase;  // keys [lo, lim) of the tile are visible
         if (args.causal) lim = min(lim, qpos - kbase + 1);
         if (args.window > 0) {
@@ -449,10 +448,14 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
       const float mx = tmax * c;
       const float m_new = (mx > m + kRescaleLog2) ? mx : m;  // also moves off -inf
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = (m_new == m) ? 1.f : ex2_approx(m - m_use);
-      const uint32_t p_t = tmem + lane_off + C::TMEM_P + 64u * (j % C::NP);
+      // p = 2^(sigma - m_use), rounded to bf16 over the second half of S's
+      // buffer (its scores are in registers), from where P_j V_j reads it.
+      const uint32_t p_t = s_t + 64u;
       const float2 cc = make_float2(c, c), nm = make_float2(-m_use, -m_use);
-      float2 a0 = make_float2(0.f, 0.f), a1 = a0;
+      // Four packed sum chains keep the additions off each other's latency.
+      float2 a[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) a[k] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t pk[32];
@@ -460,12 +463,13 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
         for (int i = 0; i < 32; ++i) {
           const float2 x = __ffma2_rn(make_float2(t[64 * h + 2 * i], t[64 * h + 2 * i + 1]), cc, nm);
           const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-          if (i & 1) a1 = __fadd2_rn(a1, p); else a0 = __fadd2_rn(a0, p);
+          a[i & 3] = __fadd2_rn(a[i & 3], p);
           pk[i] = pack_bf16x2(p.x, p.y);
         }
         tmem_st32(p_t + 32u * h, pk);
       }
-      const float2 aa = __fadd2_rn(a0, a1);
+      const float alpha = (m_new == m) ? 1.f : ex2_approx(m - m_use);
+      const float2 aa = __fadd2_rn(__fadd2_rn(a[0], a[1]), __fadd2_rn(a[2], a[3]));
       // The tile's largest weight as the loop computed it (same fused
       // multiply-add, same ex2) and what bf16 rounding took from it.
       const float pm = ex2_approx(fmaf(tmax, c, -m_use));
@@ -477,7 +481,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         // o <- alpha * o between P_{j-1} V_{j-1} and P_j V_j (rare: only
         // when a row of this warp moved its reference maximum).
-        const bool w2 = mbar_wait(bar(C::B_PV_DONE + (j - 1) % C::NP), ((j - 1) / C::NP) & 1,
+        const bool w2 = mbar_wait(bar(C::B_PV_DONE + (j - 1) % C::NS), ((j - 1) / C::NS) & 1,
                                   abort_flag, args.status, wlim);
         if (__any_sync(0xffffffffu, !w2)) {
           ok = false;
@@ -496,12 +500,12 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(C::B_P_FULL + j % C::NP));
+      mbar_arrive(bar(C::B_P_FULL + sb));
     }
 
     if (ok) {
-      const bool w = mbar_wait(bar(C::B_PV_DONE + (n_kv - 1) % C::NP),
-                               ((n_kv - 1) / C::NP) & 1, abort_flag, args.status, wlim);
+      const bool w = mbar_wait(bar(C::B_PV_DONE + (n_kv - 1) % C::NS),
+                               ((n_kv - 1) / C::NS) & 1, abort_flag, args.status, wlim);
       if (!__any_sync(0xffffffffu, !w)) {
         tc_fence_after();
         const float inv = dnorm > 0.f ? 1.f / dnorm : 0.f;
