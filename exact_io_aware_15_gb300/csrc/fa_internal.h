@@ -29,6 +29,10 @@ struct TcFwdArgs {
   // unloaded, so the wait for it runs out and every role unwinds.
   unsigned long long wait_limit_ns;
   int skip_k_tile;
+  // Set by launch_fwd_tc: the number of work items (query tiles x
+  // (sequence, head) pairs) and whether CTAs loop over them persistently.
+  int num_items;
+  int persistent;
 };
 
 // Tensor maps of Q, K, V (128-row boxes) and of O (32-row boxes, used when

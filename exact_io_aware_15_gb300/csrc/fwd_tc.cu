@@ -85,6 +85,9 @@ namespace fa {
 // more than this (base-2 units).
 constexpr float kRescaleLog2 = 32.f;
 
+// Sequences of at most this many 128-row query tiles run on persistent CTAs.
+constexpr int kPersistentMaxTiles = 32;
+
 template <int D>
 struct TcCfg {
   static constexpr int BM = 128;
@@ -95,8 +98,8 @@ struct TcCfg {
   static constexpr int KS = 2;  // K ring stages
   static constexpr int VS = 3;  // V ring stages
   static constexpr int NS = 3;  // S buffers in TMEM (P_j is written over S_j)
-  static constexpr uint32_t OFF_Q = 0;
-  static constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;
+  static constexpr uint32_t OFF_Q = 0;  // two Q buffers (consecutive items)
+  static constexpr uint32_t OFF_K = OFF_Q + 2 * TILE_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + KS * TILE_BYTES;
   static constexpr uint32_t OFF_BAR = OFF_V + VS * TILE_BYTES;
   // barrier indices, one per stage or buffer.  V_EMPTY(s) completes when the
@@ -104,8 +107,9 @@ struct TcCfg {
   // in S buffer b = j % NS, P_FULL(b) when the softmax warps have written
   // P_j over it, PV_DONE(b) when P_j V_j has finished (O holds it and S
   // buffer b is free for Q K_{j+NS}^T).
-  static constexpr int B_Q_FULL = 0;
-  static constexpr int B_K_FULL = 1;
+  static constexpr int B_Q_FULL = 0;   // two: one per Q buffer
+  static constexpr int B_Q_EMPTY = 2;  // two: the item's epilogue is done with it
+  static constexpr int B_K_FULL = 4;
   static constexpr int B_V_FULL = B_K_FULL + KS;
   static constexpr int B_K_EMPTY = B_V_FULL + VS;
   static constexpr int B_V_EMPTY = B_K_EMPTY + KS;
@@ -141,7 +145,7 @@ __device__ __forceinline__ void mbar_wait_unwind(uint32_t bar, uint32_t parity) 
   }
 }
 
-template <int D>
+template <int D, bool PERSIST>
 __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
@@ -150,49 +154,95 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
   using C = TcCfg<D>;
   extern __shared__ uint8_t smem_raw[];
 
-  // ---- which tile ----
-  // A 1-D grid of (heads x query tiles).  Heads are taken in groups of four;
-  // inside a group the heaviest query tiles (the longest causal KV ranges)
-  // come first.  A group's K/V (4 heads x 8 MB at N = 16384, D = 128) stays
-  // in L2 while its tiles run, and the light tiles fill the tail.
   const int nmb = args.num_mblocks;
-  const int BHt = static_cast<int>(gridDim.x) / nmb;
-  const long long lin = blockIdx.x;
-  const long long per_group = 4LL * nmb;
-  const int g = static_cast<int>(lin / per_group);
-  const int gsize = min(4, BHt - g * 4);
-  const int rr = static_cast<int>(lin - g * per_group);
-  const int mb = nmb - 1 - rr / gsize;
-  const int bh = g * 4 + rr % gsize;
-  const int h = bh % args.H;
-  const int seq = bh / args.H;
+  const int BHt = args.num_items / nmb;  // (sequence, head) pairs
   const bool varlen = args.cu_seqlens != nullptr;
-  int L, tok0;
-  if (varlen) {
-    const int a = __ldg(args.cu_seqlens + seq);
-    const int e = __ldg(args.cu_seqlens + seq + 1);
-    if (a < 0 || e < a || e > args.total_tokens || e - a > args.max_seqlen) {
-      if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(args.status, kStatusBounds);
-      return;
+
+  // ---- work items ----
+  // An item is one 128-row query tile of one (sequence, head).  With one CTA
+  // per item, CTA i takes item i of a head-grouped order: heads in groups of
+  // four, inside a group the heaviest query tiles (the longest causal KV
+  // ranges) first, so a group's K/V (4 heads x 8 MB at N = 16384, D = 128)
+  // stays in L2 while its tiles run and the light tiles fill the tail.
+  // Launched persistently (one CTA per SM, for short sequences), CTA c of P
+  // takes the items at positions c, 2P-1-c, 2P+c, 4P-1-c, ... of a
+  // heavy-first list (every head's last query tile first; the direction of
+  // each round alternates, which evens out the causal loads), and the next
+  // item's loads and first products overlap the current item's last tiles
+  // and epilogue.
+  struct Item {
+    int mb, bh, h, L, tok0, n_kv, j0;
+  };
+  // The k-th item of this CTA; false when there is none.  An item whose
+  // query tile holds no row of its sequence, or whose sequence offsets fail
+  // the bounds check (reported once, by thread 0), gets n_kv = 0 and is
+  // skipped by every role.
+  auto item_at = [&](int k, Item& it) -> bool {
+    int mb, bh;
+    if constexpr (PERSIST) {
+      const int P = static_cast<int>(gridDim.x);
+      const int c = static_cast<int>(blockIdx.x);
+      const long long idx = static_cast<long long>(k) * P + ((k & 1) ? P - 1 - c : c);
+      if (idx >= args.num_items) return false;
+      mb = nmb - 1 - static_cast<int>(idx / BHt);
+      bh = static_cast<int>(idx % BHt);
+    } else {
+      if (k > 0) return false;
+      const long long lin = blockIdx.x;
+      const long long per_group = 4LL * nmb;
+      const int g = static_cast<int>(lin / per_group);
+      const int gsize = min(4, BHt - g * 4);
+      const int rr = static_cast<int>(lin - g * per_group);
+      mb = nmb - 1 - rr / gsize;
+      bh = g * 4 + rr % gsize;
     }
-    L = e - a;
-    tok0 = a;
-  } else {
-    L = args.N;
-    tok0 = 0;
-  }
-  if (mb * C::BM >= L) return;  // no query row of this sequence in the tile
-  int n_kv = (L + C::BN - 1) / C::BN;
-  if (args.causal) n_kv = min(n_kv, mb + 1);
-  // With a sliding window the tile's rows see no key below
-  // mb*BM - window + 1, so the KV tiles start at j0 (all later tile indices
-  // j run from 0 and stand for KV tile j0 + j).
-  int j0 = 0;
-  if (args.window > 0) {
-    const int lo = mb * C::BM - args.window + 1;
-    j0 = lo > 0 ? lo / C::BN : 0;
-  }
-  n_kv -= j0;
+    it.mb = mb;
+    it.bh = bh;
+    it.h = bh % args.H;
+    it.n_kv = 0;
+    it.j0 = 0;
+    if (varlen) {
+      const int seq = bh / args.H;
+      const int a = __ldg(args.cu_seqlens + seq);
+      const int e = __ldg(args.cu_seqlens + seq + 1);
+      if (a < 0 || e < a || e > args.total_tokens || e - a > args.max_seqlen) {
+        if (threadIdx.x == 0) atomicOr(args.status, kStatusBounds);
+        return true;
+      }
+      it.L = e - a;
+      it.tok0 = a;
+    } else {
+      it.L = args.N;
+      it.tok0 = 0;
+    }
+    if (mb * C::BM >= it.L) return true;  // no query row of this sequence in the tile
+    int n_kv = (it.L + C::BN - 1) / C::BN;
+    if (args.causal) n_kv = min(n_kv, mb + 1);
+    // With a sliding window the tile's rows see no key below
+    // mb*BM - window + 1, so the KV tiles start at j0 (all later tile indices
+    // j run from 0 and stand for KV tile j0 + j).
+    if (args.window > 0) {
+      const int lo = mb * C::BM - args.window + 1;
+      it.j0 = lo > 0 ? lo / C::BN : 0;
+    }
+    it.n_kv = n_kv - it.j0;
+    return true;
+  };
+  // Advances k to this CTA's next item with work; false when none is left.
+  // (A CTA of the one-item launch has exactly one item: the loops below then
+  // run once, with their counters known at compile time.)
+  auto next_item = [&](int& k, Item& it) -> bool {
+    if constexpr (!PERSIST) {
+      if (k >= 0) return false;
+    }
+    while (item_at(++k, it))
+      if (it.n_kv > 0) return true;
+    return false;
+  };
+  // A CTA without any item leaves at once.
+  int first_k = -1;
+  Item first{};
+  if (!next_item(first_k, first)) return;
 
   // ---- shared memory carve-up ----
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -206,46 +256,91 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
   const int lane = threadIdx.x & 31;
   const unsigned long long wlim = args.wait_limit_ns ? args.wait_limit_ns : kWaitLimitNs;
 
-  // TMA box origin of a 128-row tile starting at sequence position `row0`,
-  // column half `c`.  Dense maps are (D, N, B*H); varlen maps are (D, H, T).
-  auto tile_coords = [&](int c, int row0, int& c0, int& c1, int& c2) {
+  // TMA box origin of a 128-row tile of item `it` starting at sequence
+  // position `row0`, column half `c`.  Dense maps are (D, N, B*H); varlen
+  // maps are (D, H, T).
+  auto tile_coords = [&](const Item& it, int c, int row0, int& c0, int& c1, int& c2) {
     c0 = c * 64;
     if (varlen) {
-      c1 = h;
-      c2 = tok0 + row0;
+      c1 = it.h;
+      c2 = it.tok0 + row0;
     } else {
       c1 = row0;
-      c2 = bh;
+      c2 = it.bh;
     }
   };
-  // One tile of K (is_v false) or V into its ring, after the product that
-  // read the stage's previous tile has finished (issued by thread 0 only).
-  auto load = [&](bool is_v, int j) -> bool {
+
+  // ---- producer state (thread 0) ----
+  // Loads are numbered per CTA across items: the K and V tiles of the g-th
+  // KV step of the CTA go to ring stages g % KS and g % VS, the Q tile of the
+  // t-th item to buffer t % 2.
+  int k_issued = 0, v_issued = 0, q_issued = 0;
+  bool k_skipped[C::KS];  // the stage's last request was left out (fault injection)
+#pragma unroll
+  for (int s = 0; s < C::KS; ++s) k_skipped[s] = false;
+  // The tile of KV step j of item `it` (global step g) into its ring, once
+  // the product that read the stage's previous tile has finished.
+  auto load_kv = [&](bool is_v, const Item& it, int j, int g) -> bool {
     const int S = is_v ? C::VS : C::KS;
-    const int st = j % S;
-    if (j >= S && !mbar_wait(bar((is_v ? C::B_V_EMPTY : C::B_K_EMPTY) + st), ((j / S) - 1) & 1,
+    const int st = g % S;
+    if (g >= S && !mbar_wait(bar((is_v ? C::B_V_EMPTY : C::B_K_EMPTY) + st), ((g / S) - 1) & 1,
                              abort_flag, args.status, wlim))
       return false;
-    // Fault injection (tests of the timeout path only): this key tile is
-    // never requested, so its full barrier never completes.
-    if (!is_v && j == args.skip_k_tile) return true;
+    if (is_v) {
+      v_issued = g + 1;
+    } else {
+      k_issued = g + 1;
+      // Fault injection (tests of the timeout path only): this key tile is
+      // never requested, so its full barrier never completes.
+      k_skipped[st] = j == args.skip_k_tile;
+      if (k_skipped[st]) return true;
+    }
     const uint32_t fb = bar((is_v ? C::B_V_FULL : C::B_K_FULL) + st);
     const uint32_t dst = sbase + (is_v ? C::OFF_V : C::OFF_K) + st * C::TILE_BYTES;
     mbar_arrive_expect_tx(fb, C::TILE_BYTES);
 #pragma unroll
     for (int c = 0; c < C::HALVES; ++c) {
       int c0, c1, c2;
-      tile_coords(c, (j0 + j) * C::BN, c0, c1, c2);
+      tile_coords(it, c, (it.j0 + j) * C::BN, c0, c1, c2);
       tma_load_3d(dst + c * C::HALF_BYTES, is_v ? &tm_v : &tm_k, fb, c0, c1, c2);
     }
     return true;
+  };
+  // The Q tile of the t-th item, once the epilogue of item t-2 has released
+  // its buffer.
+  auto load_q = [&](const Item& it, int t) -> bool {
+    const int qb = t & 1;
+    if (t >= 2 && !mbar_wait(bar(C::B_Q_EMPTY + qb), ((t >> 1) - 1) & 1, abort_flag,
+                             args.status, wlim))
+      return false;
+    q_issued = t + 1;
+    const uint32_t fb = bar(C::B_Q_FULL + qb);
+    mbar_arrive_expect_tx(fb, C::TILE_BYTES);
+#pragma unroll
+    for (int c = 0; c < C::HALVES; ++c) {
+      int c0, c1, c2;
+      tile_coords(it, c, it.mb * C::BM, c0, c1, c2);
+      tma_load_3d(sbase + C::OFF_Q + qb * C::TILE_BYTES + c * C::HALF_BYTES, &tm_q, fb, c0, c1,
+                  c2);
+    }
+    return true;
+  };
+  // An item's first copies: Q, K_0 .. K_{KS-1}, V_0 (global step g0).
+  auto load_prologue = [&](const Item& it, int t, int g0) -> bool {
+    if (!load_q(it, t)) return false;
+    for (int jk = 0; jk < C::KS && jk < it.n_kv; ++jk)
+      if (!load_kv(false, it, jk, g0 + jk)) return false;
+    return load_kv(true, it, 0, g0);
   };
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
-    mbar_init(bar(C::B_Q_FULL), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(C::B_Q_FULL + b), 1);
+      mbar_init(bar(C::B_Q_EMPTY + b), C::SOFTMAX_THREADS);
+    }
     for (int s = 0; s < C::KS; ++s) {
       mbar_init(bar(C::B_K_FULL + s), 1);
       mbar_init(bar(C::B_K_EMPTY + s), 1);
@@ -263,18 +358,9 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
     mbar_init(bar(C::B_DRAIN + 1), 1);
     *abort_flag = 0;
     fence_mbar_init();
-    // The first copies need no free stage: start them before the CTA-wide
-    // setup (TMEM allocation, barrier), so their latency overlaps it.
-    const uint32_t qb = bar(C::B_Q_FULL);
-    mbar_arrive_expect_tx(qb, C::TILE_BYTES);
-#pragma unroll
-    for (int c = 0; c < C::HALVES; ++c) {
-      int c0, c1, c2;
-      tile_coords(c, mb * C::BM, c0, c1, c2);
-      tma_load_3d(sbase + C::OFF_Q + c * C::HALF_BYTES, &tm_q, qb, c0, c1, c2);
-    }
-    for (int jk = 0; jk < C::KS && jk < n_kv; ++jk) load(false, jk);
-    load(true, 0);
+    // The first item's copies need no free stage: start them before the
+    // CTA-wide setup (TMEM allocation, barrier), so their latency overlaps it.
+    load_prologue(first, 0, 0);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
@@ -288,61 +374,76 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
   if (warp == 0) {
     // ======================= TMA producer =======================
     if (lane == 0) {
-      // Q, K_0 .. K_{KS-1} and V_0 were issued before the CTA barrier.
-      int k_issued = min(n_kv, C::KS), v_issued = 1;
-      for (int j = 0; j < n_kv; ++j) {
-        if (j > 0) {
-          if (!load(true, j)) break;
-          v_issued = j + 1;
+      int g0 = 0, ti = 0, k = first_k;
+      bool ok = true;
+      Item it = first;
+      do {
+        if (ti > 0 && !load_prologue(it, ti, g0)) break;
+        for (int j = 0; j < it.n_kv; ++j) {
+          if ((j > 0 && !load_kv(true, it, j, g0 + j)) ||
+              (j + C::KS < it.n_kv && !load_kv(false, it, j + C::KS, g0 + j + C::KS))) {
+            ok = false;
+            break;
+          }
         }
-        if (j + C::KS < n_kv) {
-          if (!load(false, j + C::KS)) break;
-          k_issued = j + C::KS + 1;
-        }
-      }
+        g0 += it.n_kv;
+        ++ti;
+      } while (ok && next_item(k, it));
       if (*abort_flag) {
         // Let every copy this thread started land before the CTA exits.
-        // Tiles before the last KS (VS) were waited for by the products
-        // that freed their stages for the later tiles.
-        mbar_wait_unwind(bar(C::B_Q_FULL), 0);
-        for (int j = max(0, k_issued - C::KS); j < k_issued; ++j)
-          if (j != args.skip_k_tile)  // never requested: nothing in flight
-            mbar_wait_unwind(bar(C::B_K_FULL + j % C::KS), (j / C::KS) & 1);
-        for (int j = max(0, v_issued - C::VS); j < v_issued; ++j)
-          mbar_wait_unwind(bar(C::B_V_FULL + j % C::VS), (j / C::VS) & 1);
+        // Copies before the last two Q tiles and the last KS (VS) K (V)
+        // tiles were waited for by the products that freed their buffers
+        // for the later ones.
+        for (int i = max(0, q_issued - 2); i < q_issued; ++i)
+          mbar_wait_unwind(bar(C::B_Q_FULL + (i & 1)), (i >> 1) & 1);
+        for (int g = max(0, k_issued - C::KS); g < k_issued; ++g)
+          if (!k_skipped[g % C::KS])  // never requested: nothing in flight
+            mbar_wait_unwind(bar(C::B_K_FULL + g % C::KS), (g / C::KS) & 1);
+        for (int g = max(0, v_issued - C::VS); g < v_issued; ++g)
+          mbar_wait_unwind(bar(C::B_V_FULL + g % C::VS), (g / C::VS) & 1);
       }
     }
   } else if (warp == 1) {
     // ======================= QK issuer =======================
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
-      const uint32_t q_s = sbase + C::OFF_Q;
-      bool ok = mbar_wait(bar(C::B_Q_FULL), 0, abort_flag, args.status, wlim);
-      for (int j = 0; ok && j < n_kv; ++j) {
-        // S buffer j % NS is free once P_{j-NS} V_{j-NS}, which read the P
-        // written over it, has finished (the softmax warps loaded S_{j-NS}
-        // before writing that P).
-        if (!mbar_wait(bar(C::B_K_FULL + j % C::KS), (j / C::KS) & 1, abort_flag,
-                       args.status, wlim) ||
-            (j >= C::NS && !mbar_wait(bar(C::B_PV_DONE + j % C::NS), ((j - C::NS) / C::NS) & 1,
-                                      abort_flag, args.status, wlim))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t k_s = sbase + C::OFF_K + (j % C::KS) * C::TILE_BYTES;
-        const uint32_t s_t = tmem + C::TMEM_S + 128u * (j % C::NS);
+      int g0 = 0, ti = 0, k = first_k;
+      bool ok = true;
+      Item it = first;
+      do {
+        const int qb = ti & 1;
+        if (!mbar_wait(bar(C::B_Q_FULL + qb), (ti >> 1) & 1, abort_flag, args.status, wlim)) break;
+        const uint32_t q_s = sbase + C::OFF_Q + qb * C::TILE_BYTES;
+        for (int j = 0; j < it.n_kv; ++j) {
+          const int g = g0 + j;
+          // S buffer g % NS is free once P_{g-NS} V_{g-NS}, which read the P
+          // written over it, has finished (the softmax warps loaded S_{g-NS}
+          // before writing that P).
+          if (!mbar_wait(bar(C::B_K_FULL + g % C::KS), (g / C::KS) & 1, abort_flag,
+                         args.status, wlim) ||
+              (g >= C::NS && !mbar_wait(bar(C::B_PV_DONE + g % C::NS),
+                                        ((g - C::NS) / C::NS) & 1, abort_flag, args.status,
+                                        wlim))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t k_s = sbase + C::OFF_K + (g % C::KS) * C::TILE_BYTES;
+          const uint32_t s_t = tmem + C::TMEM_S + 128u * (g % C::NS);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          // 16-column slice kk of the head dimension: half kk/4, 32 bytes
-          // per slice inside the 128-byte swizzled row.
-          const uint32_t off = (kk >> 2) * C::HALF_BYTES + (kk & 3) * 32u;
-          tc_mma_ss(s_t, sdesc_sw128(q_s + off, 16u, 1024u), sdesc_sw128(k_s + off, 16u, 1024u),
-                    idesc_qk, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            // 16-column slice kk of the head dimension: half kk/4, 32 bytes
+            // per slice inside the 128-byte swizzled row.
+            const uint32_t off = (kk >> 2) * C::HALF_BYTES + (kk & 3) * 32u;
+            tc_mma_ss(s_t, sdesc_sw128(q_s + off, 16u, 1024u),
+                      sdesc_sw128(k_s + off, 16u, 1024u), idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(bar(C::B_S_FULL + g % C::NS));
+          tc_commit(bar(C::B_K_EMPTY + g % C::KS));
         }
-        tc_commit(bar(C::B_S_FULL + j % C::NS));
-        tc_commit(bar(C::B_K_EMPTY + j % C::KS));
-      }
+        g0 += it.n_kv;
+        ++ti;
+      } while (ok && next_item(k, it));
       // Every MMA this thread issued completes before TMEM is released.
       tc_commit(bar(C::B_DRAIN));
       mbar_wait_unwind(bar(C::B_DRAIN), 0);
@@ -351,26 +452,38 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
     // ======================= PV issuer =======================
     if (lane == 0) {
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
-      for (int j = 0; j < n_kv; ++j) {
-        const int sv = j % C::VS;
-        if (!mbar_wait(bar(C::B_P_FULL + j % C::NS), (j / C::NS) & 1, abort_flag, args.status, wlim) ||
-            !mbar_wait(bar(C::B_V_FULL + sv), (j / C::VS) & 1, abort_flag, args.status, wlim))
-          break;
-        tc_fence_after();
-        const uint32_t v_s = sbase + C::OFF_V + sv * C::TILE_BYTES;
-        // P_j lies over the second half of S_j's buffer
-        const uint32_t p_t = tmem + C::TMEM_S + 128u * (j % C::NS) + 64u;
+      int g0 = 0, k = first_k;
+      bool ok = true;
+      Item it = first;
+      do {
+        for (int j = 0; j < it.n_kv; ++j) {
+          const int g = g0 + j;
+          const int sv = g % C::VS;
+          if (!mbar_wait(bar(C::B_P_FULL + g % C::NS), (g / C::NS) & 1, abort_flag, args.status,
+                         wlim) ||
+              !mbar_wait(bar(C::B_V_FULL + sv), (g / C::VS) & 1, abort_flag, args.status, wlim)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t v_s = sbase + C::OFF_V + sv * C::TILE_BYTES;
+          // P_j lies over the second half of S_j's buffer
+          const uint32_t p_t = tmem + C::TMEM_S + 128u * (g % C::NS) + 64u;
 #pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk) {
-          // B = V_j as an MN-major operand: N = D (64-column halves
-          // HALF_BYTES apart), K = 16 keys starting at key 16*kk.
-          const uint64_t bdesc = sdesc_sw128(v_s + kk * 16u * 128u, C::HALF_BYTES, 1024u);
-          tc_mma_ts(tmem + C::TMEM_O, p_t + kk * 8u, bdesc, idesc_pv,
-                    (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < C::BN / 16; ++kk) {
+            // B = V_j as an MN-major operand: N = D (64-column halves
+            // HALF_BYTES apart), K = 16 keys starting at key 16*kk.  The
+            // item's first product overwrites O (the previous item's
+            // epilogue has read it: its softmax warps wrote P_0 after).
+            const uint64_t bdesc = sdesc_sw128(v_s + kk * 16u * 128u, C::HALF_BYTES, 1024u);
+            tc_mma_ts(tmem + C::TMEM_O, p_t + kk * 8u, bdesc, idesc_pv,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(bar(C::B_V_EMPTY + sv));
+          tc_commit(bar(C::B_PV_DONE + g % C::NS));
         }
-        tc_commit(bar(C::B_V_EMPTY + sv));
-        tc_commit(bar(C::B_PV_DONE + j % C::NS));
-      }
+        g0 += it.n_kv;
+      } while (ok && next_item(k, it));
       tc_commit(bar(C::B_DRAIN + 1));
       mbar_wait_unwind(bar(C::B_DRAIN + 1), 0);
     }
@@ -378,230 +491,249 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
     // ======================= softmax / epilogue =======================
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
-    const int qpos = mb * C::BM + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     // sigma = s * c; with c = 0 every visible score is 0 and the masked ones
     // -inf, which c = 1 applied to (0 | -inf) reproduces without 0 * inf.
     const bool zero_scale = args.scale_log2 == 0.f;
     const float c = zero_scale ? 1.f : args.scale_log2;
-    float m = -INFINITY;  // reference maximum (base 2)
-    float dsum = 0.f;     // sum of the weights (for the log-sum-exp)
-    float dnorm = 0.f;    // the same less the largest weights' rounding (divides O)
     bool ok = true;
+    int g0 = 0, ti = 0, k = first_k;
+    Item it = first;
+    do {
+      const int mb = it.mb, L = it.L, j0 = it.j0, n_kv = it.n_kv;
+      const int qpos = mb * C::BM + r;
+      float m = -INFINITY;  // reference maximum (base 2)
+      float dsum = 0.f;     // sum of the weights (for the log-sum-exp)
+      float dnorm = 0.f;    // the same less the largest weights' rounding (divides O)
 
-    for (int j = 0; j < n_kv; ++j) {
-      const int sb = j % C::NS;
-      const uint32_t s_t = tmem + lane_off + C::TMEM_S + 128u * sb;
-      const bool w = mbar_wait(bar(C::B_S_FULL + sb), (j / C::NS) & 1, abort_flag, args.status,
-                               wlim);
+      for (int j = 0; j < n_kv; ++j) {
+        const int g = g0 + j;
+        const int sb = g % C::NS;
+        const uint32_t s_t = tmem + lane_off + C::TMEM_S + 128u * sb;
+        const bool w = mbar_wait(bar(C::B_S_FULL + sb), (g / C::NS) & 1, abort_flag,
+                                 args.status, wlim);
+        if (__any_sync(0xffffffffu, !w)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+
+        float t[128];
+        {
+          uint32_t raw[64];
+          tmem_ld64(s_t, raw);
+#pragma unroll
+          for (int i = 0; i < 64; ++i) t[i] = __uint_as_float(raw[i]);
+          tmem_ld64(s_t + 64, raw);
+#pragma unroll
+          for (int i = 0; i < 64; ++i) t[64 + i] = __uint_as_float(raw[i]);
+        }
+        const int kbase = (j0 + j) * C::BN;
+        const bool win_edge = args.window > 0 && kbase < mb * C::BM + C::BM - args.window;
+        const bool masked = (args.causal && j0 + j == mb) || kbase + C::BN > L || win_edge;
+        if (masked) {
+          int lim = L - kbase;  // keys [lo, lim) of the tile are visible
+          if (args.causal) lim = min(lim, qpos - kbase + 1);
+          if (args.window > 0) {
+            const int lo = qpos - args.window + 1 - kbase;
+#pragma unroll
+            for (int i = 0; i < 128; ++i)
+              if (i >= lim || i < lo) t[i] = -INFINITY;
+          } else {
+            // Without a window the visible keys are a prefix: one compare.
+#pragma unroll
+            for (int i = 0; i < 128; ++i) t[i] = i < lim ? t[i] : -INFINITY;
+          }
+        }
+        if (zero_scale) {
+#pragma unroll
+          for (int i = 0; i < 128; ++i) t[i] = (t[i] == -INFINITY) ? -INFINITY : 0.f;
+        }
+        // Row max over 128 values in 16 independent chains of 3-input maxima.
+        float q[16];
+#pragma unroll
+        for (int kq = 0; kq < 16; ++kq) q[kq] = fmax3(t[8 * kq], t[8 * kq + 1], t[8 * kq + 2]);
+#pragma unroll
+        for (int kq = 0; kq < 16; ++kq) q[kq] = fmax3(q[kq], t[8 * kq + 3], t[8 * kq + 4]);
+#pragma unroll
+        for (int kq = 0; kq < 16; ++kq) q[kq] = fmax3(q[kq], t[8 * kq + 5], t[8 * kq + 6]);
+#pragma unroll
+        for (int kq = 0; kq < 16; ++kq) q[kq] = fmaxf(q[kq], t[8 * kq + 7]);
+        const float r0 = fmax3(q[0], q[1], q[2]), r1 = fmax3(q[3], q[4], q[5]);
+        const float r2 = fmax3(q[6], q[7], q[8]), r3 = fmax3(q[9], q[10], q[11]);
+        const float r4 = fmax3(q[12], q[13], q[14]);
+        const float tmax = fmaxf(fmax3(r0, r1, r2), fmax3(r3, r4, q[15]));
+        const float mx = tmax * c;
+        const float m_new = (mx > m + kRescaleLog2) ? mx : m;  // also moves off -inf
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        // p = 2^(sigma - m_use), rounded to bf16 over the second half of S's
+        // buffer (its scores are in registers), from where P_j V_j reads it.
+        const uint32_t p_t = s_t + 64u;
+        const float2 cc = make_float2(c, c), nm = make_float2(-m_use, -m_use);
+        // Four packed sum chains keep the additions off each other's latency.
+        float2 a[4];
+#pragma unroll
+        for (int kq = 0; kq < 4; ++kq) a[kq] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float2 x =
+                __ffma2_rn(make_float2(t[64 * hh + 2 * i], t[64 * hh + 2 * i + 1]), cc, nm);
+            const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            a[i & 3] = __fadd2_rn(a[i & 3], p);
+            pk[i] = pack_bf16x2(p.x, p.y);
+          }
+          tmem_st32(p_t + 32u * hh, pk);
+        }
+        const float alpha = (m_new == m) ? 1.f : ex2_approx(m - m_use);
+        const float2 aa = __fadd2_rn(__fadd2_rn(a[0], a[1]), __fadd2_rn(a[2], a[3]));
+        // The tile's largest weight as the loop computed it (same fused
+        // multiply-add, same ex2) and what bf16 rounding took from it.
+        const float pm = ex2_approx(fmaf(tmax, c, -m_use));
+        const float pm_dropped = pm - __uint_as_float(pack_bf16x2(pm, 0.f) << 16);
+        dnorm = dnorm * alpha + ((aa.x + aa.y) - pm_dropped);
+        dsum = dsum * alpha + (aa.x + aa.y);
+        m = m_new;
+
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          // o <- alpha * o between P_{j-1} V_{j-1} and P_j V_j (rare: only
+          // when a row of this warp moved its reference maximum).
+          const bool w2 = mbar_wait(bar(C::B_PV_DONE + (g - 1) % C::NS), ((g - 1) / C::NS) & 1,
+                                    abort_flag, args.status, wlim);
+          if (__any_sync(0xffffffffu, !w2)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t o_t = tmem + lane_off + C::TMEM_O;
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t ov[32];
+            tmem_ld32(o_t + c0, ov);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tmem_st32(o_t + c0, ov);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(C::B_P_FULL + sb));
+      }
+      if (!ok) break;
+
+      // ---- epilogue of the item ----
+      const int gl = g0 + n_kv - 1;
+      const bool w = mbar_wait(bar(C::B_PV_DONE + gl % C::NS), (gl / C::NS) & 1, abort_flag,
+                               args.status, wlim);
       if (__any_sync(0xffffffffu, !w)) {
         ok = false;
         break;
       }
       tc_fence_after();
-
-      float t[128];
-      {
-        uint32_t raw[64];
-        tmem_ld64(s_t, raw);
-#pragma unroll
-        for (int i = 0; i < 64; ++i) t[i] = __uint_as_float(raw[i]);
-        tmem_ld64(s_t + 64, raw);
-#pragma unroll
-        for (int i = 0; i < 64; ++i) t[64 + i] = __uint_as_float(raw[i]);
+      const int qb = ti & 1;
+      const float inv = dnorm > 0.f ? 1.f / dnorm : 0.f;
+      const float lse = dsum > 0.f ? (m + log2f(dsum)) * 0.69314718055994530942f : -INFINITY;
+      const bool store = qpos < L;
+      size_t orow, lidx;
+      if (varlen) {
+        const size_t tk = static_cast<size_t>(it.tok0) + qpos;
+        orow = tk * args.H + it.h;
+        lidx = static_cast<size_t>(it.h) * args.total_tokens + tk;
+      } else {
+        orow = static_cast<size_t>(it.bh) * args.N + qpos;
+        lidx = orow;
       }
-      const int kbase = (j0 + j) * C::BN;
-      const bool win_edge = args.window > 0 && kbase < mb * C::BM + C::BM - args.window;
-      const bool masked = (args.causal && j0 + j == mb) || kbase + C::BN > L || win_edge;
-      if (masked) {
-        int lim = L - kbase;  // keys [lo, lim) of the tile are visible
-        if (args.causal) lim = min(lim, qpos - kbase + 1);
-        if (args.window > 0) {
-          const int lo = qpos - args.window + 1 - kbase;
+      const uint32_t o_t = tmem + lane_off + C::TMEM_O;
+      const int wrow0 = mb * C::BM + quarter * 32;  // this warp's first row
+      if (D == 128 && args.o_tma && (varlen ? wrow0 + 32 <= L : wrow0 < L)) {
+        // bf16 O through shared memory and one TMA store per 64-column half
+        // and warp: the rows are staged in the item's Q buffer (no product
+        // reads it any more) in the 128-byte-swizzled box layout, and the
+        // tensor map clips rows past the end of a dense sequence.  (A packed
+        // sequence's last rows are followed by the next sequence's, so a
+        // warp with rows past its end stores row by row below.)  At D = 64 a
+        // row is 128 bytes and the row-by-row stores are faster.
+        uint8_t* qbuf = smem + C::OFF_Q + qb * C::TILE_BYTES;
 #pragma unroll
-          for (int i = 0; i < 128; ++i)
-            if (i >= lim || i < lo) t[i] = -INFINITY;
-        } else {
-          // Without a window the visible keys are a prefix: one compare.
+        for (int c0 = 0; c0 < D; c0 += 64) {
+          uint32_t ov[64];
+          tmem_ld64(o_t + c0, ov);
+          uint8_t* row = qbuf + (c0 / 64) * C::HALF_BYTES + r * 128;
 #pragma unroll
-          for (int i = 0; i < 128; ++i) t[i] = i < lim ? t[i] : -INFINITY;
-        }
-      }
-      if (zero_scale) {
-#pragma unroll
-        for (int i = 0; i < 128; ++i) t[i] = (t[i] == -INFINITY) ? -INFINITY : 0.f;
-      }
-      // Row max over 128 values in 16 independent chains of 3-input maxima.
-      float q[16];
-#pragma unroll
-      for (int k = 0; k < 16; ++k) q[k] = fmax3(t[8 * k], t[8 * k + 1], t[8 * k + 2]);
-#pragma unroll
-      for (int k = 0; k < 16; ++k) q[k] = fmax3(q[k], t[8 * k + 3], t[8 * k + 4]);
-#pragma unroll
-      for (int k = 0; k < 16; ++k) q[k] = fmax3(q[k], t[8 * k + 5], t[8 * k + 6]);
-#pragma unroll
-      for (int k = 0; k < 16; ++k) q[k] = fmaxf(q[k], t[8 * k + 7]);
-      const float r0 = fmax3(q[0], q[1], q[2]), r1 = fmax3(q[3], q[4], q[5]);
-      const float r2 = fmax3(q[6], q[7], q[8]), r3 = fmax3(q[9], q[10], q[11]);
-      const float r4 = fmax3(q[12], q[13], q[14]);
-      const float tmax = fmaxf(fmax3(r0, r1, r2), fmax3(r3, r4, q[15]));
-      const float mx = tmax * c;
-      const float m_new = (mx > m + kRescaleLog2) ? mx : m;  // also moves off -inf
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      // p = 2^(sigma - m_use), rounded to bf16 over the second half of S's
-      // buffer (its scores are in registers), from where P_j V_j reads it.
-      const uint32_t p_t = s_t + 64u;
-      const float2 cc = make_float2(c, c), nm = make_float2(-m_use, -m_use);
-      // Four packed sum chains keep the additions off each other's latency.
-      float2 a[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) a[k] = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float2 x = __ffma2_rn(make_float2(t[64 * h + 2 * i], t[64 * h + 2 * i + 1]), cc, nm);
-          const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-          a[i & 3] = __fadd2_rn(a[i & 3], p);
-          pk[i] = pack_bf16x2(p.x, p.y);
-        }
-        tmem_st32(p_t + 32u * h, pk);
-      }
-      const float alpha = (m_new == m) ? 1.f : ex2_approx(m - m_use);
-      const float2 aa = __fadd2_rn(__fadd2_rn(a[0], a[1]), __fadd2_rn(a[2], a[3]));
-      // The tile's largest weight as the loop computed it (same fused
-      // multiply-add, same ex2) and what bf16 rounding took from it.
-      const float pm = ex2_approx(fmaf(tmax, c, -m_use));
-      const float pm_dropped = pm - __uint_as_float(pack_bf16x2(pm, 0.f) << 16);
-      dnorm = dnorm * alpha + ((aa.x + aa.y) - pm_dropped);
-      dsum = dsum * alpha + (aa.x + aa.y);
-      m = m_new;
-
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        // o <- alpha * o between P_{j-1} V_{j-1} and P_j V_j (rare: only
-        // when a row of this warp moved its reference maximum).
-        const bool w2 = mbar_wait(bar(C::B_PV_DONE + (j - 1) % C::NS), ((j - 1) / C::NS) & 1,
-                                  abort_flag, args.status, wlim);
-        if (__any_sync(0xffffffffu, !w2)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t o_t = tmem + lane_off + C::TMEM_O;
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t ov[32];
-          tmem_ld32(o_t + c0, ov);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-          tmem_st32(o_t + c0, ov);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(C::B_P_FULL + sb));
-    }
-
-    if (ok) {
-      const bool w = mbar_wait(bar(C::B_PV_DONE + (n_kv - 1) % C::NS),
-                               ((n_kv - 1) / C::NS) & 1, abort_flag, args.status, wlim);
-      if (!__any_sync(0xffffffffu, !w)) {
-        tc_fence_after();
-        const float inv = dnorm > 0.f ? 1.f / dnorm : 0.f;
-        const float lse = dsum > 0.f ? (m + log2f(dsum)) * 0.69314718055994530942f : -INFINITY;
-        const bool store = qpos < L;
-        size_t orow, lidx;
-        if (varlen) {
-          const size_t t = static_cast<size_t>(tok0) + qpos;
-          orow = t * args.H + h;
-          lidx = static_cast<size_t>(h) * args.total_tokens + t;
-        } else {
-          orow = static_cast<size_t>(bh) * args.N + qpos;
-          lidx = orow;
-        }
-        const uint32_t o_t = tmem + lane_off + C::TMEM_O;
-        const int wrow0 = mb * C::BM + quarter * 32;  // this warp's first row
-        if (D == 128 && args.o_tma && (varlen ? wrow0 + 32 <= L : wrow0 < L)) {
-          // bf16 O through shared memory and one TMA store per 64-column half
-          // and warp: the rows are staged in Q's buffer (no product reads Q
-          // any more) in the 128-byte-swizzled box layout, and the tensor
-          // map clips rows past the end of a dense sequence.  (A packed
-          // sequence's last rows are followed by the next sequence's, so a
-          // warp with rows past its end stores row by row below.)  At
-          // D = 64 a row is 128 bytes and the row-by-row stores are faster.
-#pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 64) {
-            uint32_t ov[64];
-            tmem_ld64(o_t + c0, ov);
-            uint8_t* row = smem + C::OFF_Q + (c0 / 64) * C::HALF_BYTES + r * 128;
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-              uint4 u;
-              u.x = pack_bf16x2(__uint_as_float(ov[8 * ch + 0]) * inv,
-                                __uint_as_float(ov[8 * ch + 1]) * inv);
-              u.y = pack_bf16x2(__uint_as_float(ov[8 * ch + 2]) * inv,
-                                __uint_as_float(ov[8 * ch + 3]) * inv);
-              u.z = pack_bf16x2(__uint_as_float(ov[8 * ch + 4]) * inv,
-                                __uint_as_float(ov[8 * ch + 5]) * inv);
-              u.w = pack_bf16x2(__uint_as_float(ov[8 * ch + 6]) * inv,
-                                __uint_as_float(ov[8 * ch + 7]) * inv);
-              *reinterpret_cast<uint4*>(row + ((ch ^ (r & 7)) << 4)) = u;
-            }
+          for (int ch = 0; ch < 8; ++ch) {
+            uint4 u;
+            u.x = pack_bf16x2(__uint_as_float(ov[8 * ch + 0]) * inv,
+                              __uint_as_float(ov[8 * ch + 1]) * inv);
+            u.y = pack_bf16x2(__uint_as_float(ov[8 * ch + 2]) * inv,
+                              __uint_as_float(ov[8 * ch + 3]) * inv);
+            u.z = pack_bf16x2(__uint_as_float(ov[8 * ch + 4]) * inv,
+                              __uint_as_float(ov[8 * ch + 5]) * inv);
+            u.w = pack_bf16x2(__uint_as_float(ov[8 * ch + 6]) * inv,
+                              __uint_as_float(ov[8 * ch + 7]) * inv);
+            *reinterpret_cast<uint4*>(row + ((ch ^ (r & 7)) << 4)) = u;
           }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
 #pragma unroll
-            for (int c = 0; c < C::HALVES; ++c) {
-              const uint32_t src = sbase + C::OFF_Q + c * C::HALF_BYTES + quarter * 32 * 128;
-              if (varlen)
-                tma_store_3d(&tm_o, src, c * 64, h, tok0 + wrow0);
-              else
-                tma_store_3d(&tm_o, src, c * 64, wrow0, bh);
-            }
-            tma_store_commit_and_wait_read();
+          for (int cc = 0; cc < C::HALVES; ++cc) {
+            const uint32_t src =
+                sbase + C::OFF_Q + qb * C::TILE_BYTES + cc * C::HALF_BYTES + quarter * 32 * 128;
+            if (varlen)
+              tma_store_3d(&tm_o, src, cc * 64, it.h, it.tok0 + wrow0);
+            else
+              tma_store_3d(&tm_o, src, cc * 64, wrow0, it.bh);
           }
-          __syncwarp();
-        } else {
-          // 64 columns per TMEM load (one wait each), then the stores.
+          tma_store_commit_and_wait_read();
+        }
+        __syncwarp();
+      } else {
+        // 64 columns per TMEM load (one wait each), then the stores.
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 64) {
-            uint32_t ov[64];
-            tmem_ld64(o_t + c0, ov);
-            if (store) {
-              if (args.o_f32) {
-                float4* dst =
-                    reinterpret_cast<float4*>(static_cast<float*>(args.o) + orow * D + c0);
+        for (int c0 = 0; c0 < D; c0 += 64) {
+          uint32_t ov[64];
+          tmem_ld64(o_t + c0, ov);
+          if (store) {
+            if (args.o_f32) {
+              float4* dst =
+                  reinterpret_cast<float4*>(static_cast<float*>(args.o) + orow * D + c0);
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                  dst[i] = make_float4(__uint_as_float(ov[4 * i]) * inv,
-                                       __uint_as_float(ov[4 * i + 1]) * inv,
-                                       __uint_as_float(ov[4 * i + 2]) * inv,
-                                       __uint_as_float(ov[4 * i + 3]) * inv);
-              } else {
-                uint4* dst =
-                    reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.o) + orow * D + c0);
+              for (int i = 0; i < 16; ++i)
+                dst[i] = make_float4(__uint_as_float(ov[4 * i]) * inv,
+                                     __uint_as_float(ov[4 * i + 1]) * inv,
+                                     __uint_as_float(ov[4 * i + 2]) * inv,
+                                     __uint_as_float(ov[4 * i + 3]) * inv);
+            } else {
+              uint4* dst =
+                  reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.o) + orow * D + c0);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  uint4 u;
-                  u.x = pack_bf16x2(__uint_as_float(ov[8 * i + 0]) * inv,
-                                    __uint_as_float(ov[8 * i + 1]) * inv);
-                  u.y = pack_bf16x2(__uint_as_float(ov[8 * i + 2]) * inv,
-                                    __uint_as_float(ov[8 * i + 3]) * inv);
-                  u.z = pack_bf16x2(__uint_as_float(ov[8 * i + 4]) * inv,
-                                    __uint_as_float(ov[8 * i + 5]) * inv);
-                  u.w = pack_bf16x2(__uint_as_float(ov[8 * i + 6]) * inv,
-                                    __uint_as_float(ov[8 * i + 7]) * inv);
-                  dst[i] = u;
-                }
+              for (int i = 0; i < 8; ++i) {
+                uint4 u;
+                u.x = pack_bf16x2(__uint_as_float(ov[8 * i + 0]) * inv,
+                                  __uint_as_float(ov[8 * i + 1]) * inv);
+                u.y = pack_bf16x2(__uint_as_float(ov[8 * i + 2]) * inv,
+                                  __uint_as_float(ov[8 * i + 3]) * inv);
+                u.z = pack_bf16x2(__uint_as_float(ov[8 * i + 4]) * inv,
+                                  __uint_as_float(ov[8 * i + 5]) * inv);
+                u.w = pack_bf16x2(__uint_as_float(ov[8 * i + 6]) * inv,
+                                  __uint_as_float(ov[8 * i + 7]) * inv);
+                dst[i] = u;
               }
             }
           }
         }
-        if (store) args.lse[lidx] = lse;
       }
-    }
+      if (store) args.lse[lidx] = lse;
+      // The item's Q buffer may take the Q tile of item ti + 2: its products
+      // have finished (P_last V_last has) and the staged O has been read.
+      tc_fence_before();
+      mbar_arrive(bar(C::B_Q_EMPTY + qb));
+      g0 += n_kv;
+      ++ti;
+    } while (ok && next_item(k, it));
     tc_fence_before();
   }
 
@@ -619,20 +751,46 @@ template <int D>
 static cudaError_t launch_tc_impl(const TcMaps& maps, const TcFwdArgs& a, int grid_x,
                                   cudaStream_t stream) {
   using C = TcCfg<D>;
-  // The shared-memory opt-in is a per-device attribute of the function.
-  static std::atomic<bool> attr_set[64];  // per device: attribute already set
+  // The shared-memory opt-in is a per-device attribute of each function.
+  static std::atomic<bool> attr_set[64];  // per device: attributes already set
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(C::SMEM_BYTES));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::SMEM_BYTES));
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_release);
   }
-  dim3 grid(static_cast<unsigned>(grid_x * a.num_mblocks));
-  fa_fwd_tc_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(maps.q, maps.k, maps.v, maps.o,
-                                                                   a);
+  static std::atomic<int> sm_count[64];  // per device: multiprocessors (0 = not read yet)
+  int nsm = (dev >= 0 && dev < 64) ? sm_count[dev].load(std::memory_order_acquire) : 0;
+  if (nsm == 0) {
+    e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) sm_count[dev].store(nsm, std::memory_order_release);
+  }
+  TcFwdArgs args = a;
+  args.num_items = grid_x * a.num_mblocks;
+  // Persistent CTAs (one per SM) for short dense sequences, where the fixed
+  // cost of a CTA (setup, first product, epilogue) is a large share of its
+  // work; one CTA per item otherwise (the hardware scheduler balances the
+  // long causal ranges, the head-grouped order keeps K/V in L2, and most
+  // items of a packed batch are empty, which a one-item CTA skips at once).
+  args.persistent = (a.cu_seqlens == nullptr && a.num_mblocks <= kPersistentMaxTiles &&
+                     args.num_items > nsm)
+                        ? 1
+                        : 0;
+  if (args.persistent)
+    fa_fwd_tc_kernel<D, true><<<dim3(static_cast<unsigned>(nsm)), C::THREADS, C::SMEM_BYTES,
+                                stream>>>(maps.q, maps.k, maps.v, maps.o, args);
+  else
+    fa_fwd_tc_kernel<D, false><<<dim3(static_cast<unsigned>(args.num_items)), C::THREADS,
+                                 C::SMEM_BYTES, stream>>>(maps.q, maps.k, maps.v, maps.o, args);
   return cudaGetLastError();
 }
 

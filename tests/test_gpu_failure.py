@@ -29,9 +29,13 @@ def fa():
     return fa
 
 
-@pytest.mark.parametrize("D,causal", [(128, False), (64, False), (128, True)])
-def test_wait_timeout_unwinds(fa, D, causal):
-    B, H, N = 1, 2, 512  # four query tiles, four key tiles
+@pytest.mark.parametrize("D,causal,H", [(128, False, 2), (64, False, 2), (128, True, 2),
+                                         (128, False, 80), (64, False, 80)])
+def test_wait_timeout_unwinds(fa, D, causal, H):
+    """H = 80 gives 320 query tiles, more than the GPU's SMs, so the short
+    sequence runs on persistent CTAs (a CTA that gives up leaves its later
+    items unwritten); H = 2 runs one CTA per query tile."""
+    B, N = 1, 512  # four query tiles, four key tiles per head
     case = inp.dense(B, H, N, D, seed=50 + D, causal=causal)
     q, k, v = case.q.cuda(), case.k.cuda(), case.v.cuda()
     assert fa.fa_check_device_status() == fa.FA_OK
