@@ -18,7 +18,11 @@ from typing import Optional
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_lib", "libfa_gb300.so")
+# The library the binding loads: the built one, or another build of the same
+# C ABI named by FA_GB300_LIBRARY (the bounds-checked debug build,
+# _lib/libfa_gb300_debug.so).
+LIB_PATH = os.environ.get("FA_GB300_LIBRARY") or os.path.join(_HERE, "_lib", "libfa_gb300.so")
+DEBUG_LIB_PATH = os.path.join(_HERE, "_lib", "libfa_gb300_debug.so")
 
 FA_OK = 0
 FA_ERR_INVALID_ARG = -1
@@ -616,5 +620,5 @@ __all__ = [
     "fa_decode_splitkv", "fa_combine_states", "fa_decode_splitkv_noalloc",
     "fa_decode_paged_splitkv",
     "fa_check_device_status", "fa_fwd_fault_inject",
-    "fa_status_string", "decode", "load_library", "FAError", "LIB_PATH",
+    "fa_status_string", "decode", "load_library", "FAError", "LIB_PATH", "DEBUG_LIB_PATH",
 ]

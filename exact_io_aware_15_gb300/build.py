@@ -5,6 +5,13 @@ objects are linked into one shared library (CUDA runtime linked statically,
 driver API reached through the runtime's entry-point query, so the library has
 no libcuda link dependency).  Outputs go under ``_lib/`` next to this file and
 are not committed.
+
+A second library, ``_lib/libfa_gb300_debug.so``, is linked from the same
+objects except the tensor-core forward, which is compiled with -DFA_DEBUG:
+its kernels then check every shared-memory, tensor-memory and output index
+range before use and report a failed check as FA_ERR_DEVICE_BOUNDS (the
+binding loads it when FA_GB300_LIBRARY names it; the tests use it to run the
+odd-shaped forward cases under those checks).
 """
 from __future__ import annotations
 
@@ -19,6 +26,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT, "libfa_gb300.so")
+DEBUG_LIB = os.path.join(OUT, "libfa_gb300_debug.so")
+DEBUG_SOURCES = ["fwd_tc.cu"]  # compiled a second time with -DFA_DEBUG
 SOURCES = ["fa_api.cu", "fwd_tc.cu", "fwd_f32.cu", "decode.cu", "combine.cu",
            "decode_noalloc.cu", "bwd_tc.cu", "rowstats.cu", "scan.cu",
            "decode_tc.cu"]
@@ -53,6 +62,7 @@ def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False) 
         os.path.join(ROOT, "include", "fa_gb300.h")]
     cc = nvcc()
     objs = []
+    debug_objs = []
     jobs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
@@ -61,6 +71,13 @@ def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False) 
         if force or _stale(o, [s, *headers]):
             extra = ["-Xptxas", "-v"] if ptxas_info else []
             jobs.append([cc, *_flags(extra), "-c", s, "-o", o])
+        if src in DEBUG_SOURCES:
+            od = os.path.join(OUT, src.replace(".cu", ".debug.o"))
+            debug_objs.append(od)
+            if force or _stale(od, [s, *headers]):
+                jobs.append([cc, *_flags(["-DFA_DEBUG"]), "-c", s, "-o", od])
+        else:
+            debug_objs.append(o)
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -73,13 +90,14 @@ def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False) 
                     sys.stderr.write(r.stdout + r.stderr)
                 if r.returncode != 0:
                     raise RuntimeError("nvcc failed: " + " ".join(cmd))
-    if force or jobs or _stale(LIB, objs):
-        cmd = [cc, *ARCH, "-shared", "-o", LIB + ".tmp", *objs]
-        r = subprocess.run(cmd, capture_output=True, text=True)
-        if r.returncode != 0:
-            sys.stderr.write(r.stdout + r.stderr)
-            raise RuntimeError("link failed")
-        os.replace(LIB + ".tmp", LIB)
+    for lib, lib_objs in ((LIB, objs), (DEBUG_LIB, debug_objs)):
+        if force or jobs or _stale(lib, lib_objs):
+            cmd = [cc, *ARCH, "-shared", "-o", lib + ".tmp", *lib_objs]
+            r = subprocess.run(cmd, capture_output=True, text=True)
+            if r.returncode != 0:
+                sys.stderr.write(r.stdout + r.stderr)
+                raise RuntimeError("link failed")
+            os.replace(lib + ".tmp", lib)
     return LIB
 
 

@@ -19,6 +19,22 @@ constexpr unsigned int kStatusBounds = 2u;
 // records kStatusTimeout, unwinds and returns instead of hanging the GPU.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
+// Range checks of the debug build (compiled with -DFA_DEBUG, in place of a
+// memory checker): a kernel passes a shared-memory, tensor-memory or output
+// index range through fa_dbg_ok before using it; a failed check records
+// kStatusBounds and the caller skips the access.  In the normal build the
+// check is the constant true and costs nothing.
+#ifdef FA_DEBUG
+constexpr bool kDebugChecks = true;
+__device__ __forceinline__ bool fa_dbg_ok(bool cond, unsigned int* status) {
+  if (!cond) atomicOr(status, kStatusBounds);
+  return cond;
+}
+#else
+constexpr bool kDebugChecks = false;
+__device__ __forceinline__ constexpr bool fa_dbg_ok(bool, unsigned int*) { return true; }
+#endif
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -255,6 +255,12 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const unsigned long long wlim = args.wait_limit_ns ? args.wait_limit_ns : kWaitLimitNs;
+  // Debug-build checks (fa_dbg_ok): a shared-memory range must lie in this
+  // CTA's dynamic shared memory above the aligned base.
+  const uint32_t smem_end = raw_addr + C::SMEM_BYTES;
+  auto smem_ok = [&](uint32_t addr, uint32_t bytes) -> bool {
+    return fa_dbg_ok(addr >= sbase && addr + bytes <= smem_end, args.status);
+  };
 
   // TMA box origin of a 128-row tile of item `it` starting at sequence
   // position `row0`, column half `c`.  Dense maps are (D, N, B*H); varlen
@@ -297,6 +303,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
     }
     const uint32_t fb = bar((is_v ? C::B_V_FULL : C::B_K_FULL) + st);
     const uint32_t dst = sbase + (is_v ? C::OFF_V : C::OFF_K) + st * C::TILE_BYTES;
+    if (!smem_ok(dst, C::TILE_BYTES) || !smem_ok(fb, 8)) return true;
     mbar_arrive_expect_tx(fb, C::TILE_BYTES);
 #pragma unroll
     for (int c = 0; c < C::HALVES; ++c) {
@@ -315,6 +322,8 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
       return false;
     q_issued = t + 1;
     const uint32_t fb = bar(C::B_Q_FULL + qb);
+    if (!smem_ok(sbase + C::OFF_Q + qb * C::TILE_BYTES, C::TILE_BYTES) || !smem_ok(fb, 8))
+      return true;
     mbar_arrive_expect_tx(fb, C::TILE_BYTES);
 #pragma unroll
     for (int c = 0; c < C::HALVES; ++c) {
@@ -370,6 +379,14 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  // Debug-build check: a tensor-memory range (lanes x columns starting at
+  // taddr = lane << 16 | column) must lie in this CTA's allocation.
+  auto tmem_ok = [&](uint32_t taddr, uint32_t lanes, uint32_t cols) -> bool {
+    const uint32_t col = taddr & 0xFFFFu, col0 = tmem & 0xFFFFu;
+    return fa_dbg_ok((taddr >> 16) + lanes <= 128u && col >= col0 &&
+                         col + cols <= col0 + C::TMEM_COLS,
+                     args.status);
+  };
 
   if (warp == 0) {
     // ======================= TMA producer =======================
@@ -430,8 +447,10 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
           tc_fence_after();
           const uint32_t k_s = sbase + C::OFF_K + (g % C::KS) * C::TILE_BYTES;
           const uint32_t s_t = tmem + C::TMEM_S + 128u * (g % C::NS);
+          const bool in_range = smem_ok(q_s, C::TILE_BYTES) && smem_ok(k_s, C::TILE_BYTES) &&
+                                tmem_ok(s_t, 128u, 128u);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
+          for (int kk = 0; kk < D / 16 && in_range; ++kk) {
             // 16-column slice kk of the head dimension: half kk/4, 32 bytes
             // per slice inside the 128-byte swizzled row.
             const uint32_t off = (kk >> 2) * C::HALF_BYTES + (kk & 3) * 32u;
@@ -469,8 +488,10 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
           const uint32_t v_s = sbase + C::OFF_V + sv * C::TILE_BYTES;
           // P_j lies over the second half of S_j's buffer
           const uint32_t p_t = tmem + C::TMEM_S + 128u * (g % C::NS) + 64u;
+          const bool in_range = smem_ok(v_s, C::TILE_BYTES) && tmem_ok(p_t, 128u, 64u) &&
+                                tmem_ok(tmem + C::TMEM_O, 128u, D);
 #pragma unroll
-          for (int kk = 0; kk < C::BN / 16; ++kk) {
+          for (int kk = 0; kk < C::BN / 16 && in_range; ++kk) {
             // B = V_j as an MN-major operand: N = D (64-column halves
             // HALF_BYTES apart), K = 16 keys starting at key 16*kk.  The
             // item's first product overwrites O (the previous item's
@@ -519,7 +540,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
         tc_fence_after();
 
         float t[128];
-        {
+        if (!kDebugChecks || __all_sync(0xffffffffu, tmem_ok(s_t, 32u, 128u))) {
           uint32_t raw[64];
           tmem_ld64(s_t, raw);
 #pragma unroll
@@ -527,6 +548,9 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
           tmem_ld64(s_t + 64, raw);
 #pragma unroll
           for (int i = 0; i < 64; ++i) t[64 + i] = __uint_as_float(raw[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 128; ++i) t[i] = 0.f;
         }
         const int kbase = (j0 + j) * C::BN;
         const bool win_edge = args.window > 0 && kbase < mb * C::BM + C::BM - args.window;
@@ -570,6 +594,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
         // buffer (its scores are in registers), from where P_j V_j reads it.
         const uint32_t p_t = s_t + 64u;
         const float2 cc = make_float2(c, c), nm = make_float2(-m_use, -m_use);
+        const bool p_ok = !kDebugChecks || __all_sync(0xffffffffu, tmem_ok(p_t, 32u, 64u));
         // Four packed sum chains keep the additions off each other's latency.
         float2 a[4];
 #pragma unroll
@@ -585,7 +610,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
             a[i & 3] = __fadd2_rn(a[i & 3], p);
             pk[i] = pack_bf16x2(p.x, p.y);
           }
-          tmem_st32(p_t + 32u * hh, pk);
+          if (p_ok) tmem_st32(p_t + 32u * hh, pk);
         }
         const float alpha = (m_new == m) ? 1.f : ex2_approx(m - m_use);
         const float2 aa = __fadd2_rn(__fadd2_rn(a[0], a[1]), __fadd2_rn(a[2], a[3]));
@@ -608,8 +633,9 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
           }
           tc_fence_after();
           const uint32_t o_t = tmem + lane_off + C::TMEM_O;
+          const bool o_ok = !kDebugChecks || __all_sync(0xffffffffu, tmem_ok(o_t, 32u, D));
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
+          for (int c0 = 0; c0 < D && o_ok; c0 += 32) {
             uint32_t ov[32];
             tmem_ld32(o_t + c0, ov);
 #pragma unroll
@@ -647,7 +673,15 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
       }
       const uint32_t o_t = tmem + lane_off + C::TMEM_O;
       const int wrow0 = mb * C::BM + quarter * 32;  // this warp's first row
-      if (D == 128 && args.o_tma && (varlen ? wrow0 + 32 <= L : wrow0 < L)) {
+      // Debug-build checks of the epilogue: O's TMEM range, the staging
+      // rows, and the output indices against the tensors' sizes.
+      const bool o_in = !kDebugChecks || __all_sync(0xffffffffu, tmem_ok(o_t, 32u, D));
+      const size_t rows_total = varlen ? static_cast<size_t>(args.total_tokens) * args.H
+                                       : static_cast<size_t>(BHt) * args.N;
+      const bool out_in = !store || fa_dbg_ok(orow < rows_total && lidx < rows_total, args.status);
+      if (!o_in) {
+        // (debug build only) nothing to read: skip the item's stores
+      } else if (D == 128 && args.o_tma && (varlen ? wrow0 + 32 <= L : wrow0 < L)) {
         // bf16 O through shared memory and one TMA store per 64-column half
         // and warp: the rows are staged in the item's Q buffer (no product
         // reads it any more) in the 128-byte-swizzled box layout, and the
@@ -661,6 +695,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
           uint32_t ov[64];
           tmem_ld64(o_t + c0, ov);
           uint8_t* row = qbuf + (c0 / 64) * C::HALF_BYTES + r * 128;
+          if (!smem_ok(sbase + static_cast<uint32_t>(row - smem), 128u)) continue;
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch) {
             uint4 u;
@@ -682,6 +717,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
           for (int cc = 0; cc < C::HALVES; ++cc) {
             const uint32_t src =
                 sbase + C::OFF_Q + qb * C::TILE_BYTES + cc * C::HALF_BYTES + quarter * 32 * 128;
+            if (!smem_ok(src, 32u * 128u)) continue;
             if (varlen)
               tma_store_3d(&tm_o, src, cc * 64, it.h, it.tok0 + wrow0);
             else
@@ -696,7 +732,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
         for (int c0 = 0; c0 < D; c0 += 64) {
           uint32_t ov[64];
           tmem_ld64(o_t + c0, ov);
-          if (store) {
+          if (store && out_in) {
             if (args.o_f32) {
               float4* dst =
                   reinterpret_cast<float4*>(static_cast<float*>(args.o) + orow * D + c0);
@@ -726,7 +762,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
           }
         }
       }
-      if (store) args.lse[lidx] = lse;
+      if (store && out_in) args.lse[lidx] = lse;
       // The item's Q buffer may take the Q tile of item ti + 2: its products
       // have finished (P_last V_last has) and the staged O has been read.
       tc_fence_before();
