@@ -8,6 +8,7 @@ status, so a range error anywhere in those launches fails this test.  (The
 memory checker of the CUDA toolkit is closed on this GPU pool; these checks
 stand in for it.)"""
 import os
+import re
 import subprocess
 import sys
 
@@ -32,6 +33,11 @@ def test_forward_cases_clean_under_debug_checks():
         from exact_io_aware_15_gb300 import build
         build.build()
     env = dict(os.environ, FA_GB300_LIBRARY=fa.DEBUG_LIB_PATH)
+    # the child's binding loads the debug library
+    which = subprocess.run([sys.executable, "-c",
+                            "import exact_io_aware_15_gb300 as fa; print(fa.LIB_PATH)"],
+                           cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert which.stdout.strip() == fa.DEBUG_LIB_PATH, which.stdout + which.stderr
     r = subprocess.run(
         [sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu",
          os.path.join(ROOT, "tests", "test_gpu_prefill.py"),
@@ -40,4 +46,5 @@ def test_forward_cases_clean_under_debug_checks():
          "-k", CASES],
         cwd=ROOT, env=env, capture_output=True, text=True, timeout=1200)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
-    assert " passed" in r.stdout
+    m = re.search(r"(\d+) passed", r.stdout)
+    assert m and int(m.group(1)) >= 30, r.stdout[-2000:]
