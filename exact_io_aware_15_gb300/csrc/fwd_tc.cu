@@ -88,7 +88,16 @@ constexpr float kRescaleLog2 = 32.f;
 // Sequences of at most this many 128-row query tiles run on persistent CTAs.
 constexpr int kPersistentMaxTiles = 32;
 
-template <int D>
+// Softmax warpgroups per CTA at D = 64 (at D = 128 tensor memory holds one O).
+constexpr int kSoftmaxGroups64 = 2;
+
+// NG softmax warpgroups per CTA.  With two (D = 64), group g folds the key
+// tiles j with j % 2 == g into its own state and O accumulator, and the
+// epilogue merges the two states (split-K inside the CTA, "Associativity is
+// All You Need"): each scheduler then runs two softmax warps on different
+// tiles.  Three S buffers and two O accumulators fit tensor memory only at
+// D = 64.
+template <int D, int NG = 1>
 struct TcCfg {
   static constexpr int BM = 128;
   static constexpr int BN = 128;
@@ -116,16 +125,27 @@ struct TcCfg {
   static constexpr int B_S_FULL = B_V_EMPTY + VS;
   static constexpr int B_P_FULL = B_S_FULL + NS;
   static constexpr int B_PV_DONE = B_P_FULL + NS;
-  static constexpr int B_DRAIN = B_PV_DONE + NS;  // one per issuing thread
+  // PV_GRP(g): a P V product of softmax group g has finished (one phase per
+  // product of that group; two groups only); XCH_FULL / XCH_DONE: the two
+  // groups' epilogue
+  // exchange (group 1's state is in shared memory and its O is final; group
+  // 0 has read group 1's O).
+  static constexpr int B_PV_GRP = B_PV_DONE + NS;
+  static constexpr int B_XCH_FULL = B_PV_GRP + NG;
+  static constexpr int B_XCH_DONE = B_XCH_FULL + 1;
+  static constexpr int B_DRAIN = B_XCH_DONE + 1;  // one per issuing thread
   static constexpr int NUM_BARS = B_DRAIN + 2;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+  static constexpr uint32_t OFF_XCH = (OFF_MISC + 16 + 15) & ~15u;  // [128 rows][4] floats
+  static constexpr uint32_t SMEM_BYTES = OFF_XCH + (NG > 1 ? 128 * 16 : 0) + 1024;  // + slack
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t TMEM_S = 0;    // buffer b at TMEM_S + 128 b
-  static constexpr uint32_t TMEM_O = 384;
-  static constexpr int THREADS = 224;
-  static constexpr int WARP_PV = 6;
-  static constexpr int SOFTMAX_THREADS = 128;
+  static constexpr uint32_t TMEM_O = 384;  // group g's O at TMEM_O + g D
+  static_assert(TMEM_O + NG * D <= TMEM_COLS, "S buffers and O accumulators exceed TMEM");
+  static constexpr int WARP_PV = NG == 1 ? 6 : 2;
+  static constexpr int WARP_SM0 = NG == 1 ? 2 : 3;  // first softmax warp
+  static constexpr int THREADS = 32 * (WARP_SM0 + 4 * NG + (NG == 1 ? 1 : 0));
+  static constexpr int SOFTMAX_THREADS = 128;  // one group
 };
 
 // max(a, b, c) in one instruction.
@@ -145,13 +165,13 @@ __device__ __forceinline__ void mbar_wait_unwind(uint32_t bar, uint32_t parity) 
   }
 }
 
-template <int D, bool PERSIST>
-__global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
+template <int D, bool PERSIST, int NG>
+__global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_o, const TcFwdArgs args) {
-  using C = TcCfg<D>;
+  using C = TcCfg<D, NG>;
   extern __shared__ uint8_t smem_raw[];
 
   const int nmb = args.num_mblocks;
@@ -363,6 +383,9 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
       mbar_init(bar(C::B_P_FULL + b), C::SOFTMAX_THREADS);
       mbar_init(bar(C::B_PV_DONE + b), 1);
     }
+    for (int gr = 0; gr < NG; ++gr) mbar_init(bar(C::B_PV_GRP + gr), 1);
+    mbar_init(bar(C::B_XCH_FULL), C::SOFTMAX_THREADS);
+    mbar_init(bar(C::B_XCH_DONE), C::SOFTMAX_THREADS);
     mbar_init(bar(C::B_DRAIN), 1);
     mbar_init(bar(C::B_DRAIN + 1), 1);
     *abort_flag = 0;
@@ -488,8 +511,12 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
           const uint32_t v_s = sbase + C::OFF_V + sv * C::TILE_BYTES;
           // P_j lies over the second half of S_j's buffer
           const uint32_t p_t = tmem + C::TMEM_S + 128u * (g % C::NS) + 64u;
+          // group j % NG's accumulator; its first product of the item
+          // overwrites it (the previous item's epilogue has read it).
+          const int grp = j % NG;
+          const uint32_t o_acc = tmem + C::TMEM_O + grp * D;
           const bool in_range = smem_ok(v_s, C::TILE_BYTES) && tmem_ok(p_t, 128u, 64u) &&
-                                tmem_ok(tmem + C::TMEM_O, 128u, D);
+                                tmem_ok(o_acc, 128u, D);
 #pragma unroll
           for (int kk = 0; kk < C::BN / 16 && in_range; ++kk) {
             // B = V_j as an MN-major operand: N = D (64-column halves
@@ -497,11 +524,11 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
             // item's first product overwrites O (the previous item's
             // epilogue has read it: its softmax warps wrote P_0 after).
             const uint64_t bdesc = sdesc_sw128(v_s + kk * 16u * 128u, C::HALF_BYTES, 1024u);
-            tc_mma_ts(tmem + C::TMEM_O, p_t + kk * 8u, bdesc, idesc_pv,
-                      (j > 0 || kk > 0) ? 1u : 0u);
+            tc_mma_ts(o_acc, p_t + kk * 8u, bdesc, idesc_pv, (j >= NG || kk > 0) ? 1u : 0u);
           }
           tc_commit(bar(C::B_V_EMPTY + sv));
           tc_commit(bar(C::B_PV_DONE + g % C::NS));
+          if constexpr (NG > 1) tc_commit(bar(C::B_PV_GRP + grp));
         }
         g0 += it.n_kv;
       } while (ok && next_item(k, it));
@@ -510,6 +537,10 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
     }
   } else {
     // ======================= softmax / epilogue =======================
+    // Group grp of NG folds the key tiles j with j % NG == grp; warp w reads
+    // TMEM lanes 32 (w % 4) ... + 31 (every group covers all 128 rows).
+    const int grp = (warp - C::WARP_SM0) >> 2;
+    int pvn = 0;  // P V products of this group so far (phases of PV_GRP(grp))
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -527,7 +558,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
       float dsum = 0.f;     // sum of the weights (for the log-sum-exp)
       float dnorm = 0.f;    // the same less the largest weights' rounding (divides O)
 
-      for (int j = 0; j < n_kv; ++j) {
+      for (int j = grp; j < n_kv; j += NG) {
         const int g = g0 + j;
         const int sb = g % C::NS;
         const uint32_t s_t = tmem + lane_off + C::TMEM_S + 128u * sb;
@@ -539,78 +570,155 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
         }
         tc_fence_after();
 
-        float t[128];
-        if (!kDebugChecks || __all_sync(0xffffffffu, tmem_ok(s_t, 32u, 128u))) {
-          uint32_t raw[64];
-          tmem_ld64(s_t, raw);
-#pragma unroll
-          for (int i = 0; i < 64; ++i) t[i] = __uint_as_float(raw[i]);
-          tmem_ld64(s_t + 64, raw);
-#pragma unroll
-          for (int i = 0; i < 64; ++i) t[64 + i] = __uint_as_float(raw[i]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 128; ++i) t[i] = 0.f;
-        }
         const int kbase = (j0 + j) * C::BN;
         const bool win_edge = args.window > 0 && kbase < mb * C::BM + C::BM - args.window;
         const bool masked = (args.causal && j0 + j == mb) || kbase + C::BN > L || win_edge;
-        if (masked) {
-          int lim = L - kbase;  // keys [lo, lim) of the tile are visible
-          if (args.causal) lim = min(lim, qpos - kbase + 1);
-          if (args.window > 0) {
-            const int lo = qpos - args.window + 1 - kbase;
-#pragma unroll
-            for (int i = 0; i < 128; ++i)
-              if (i >= lim || i < lo) t[i] = -INFINITY;
-          } else {
-            // Without a window the visible keys are a prefix: one compare.
-#pragma unroll
-            for (int i = 0; i < 128; ++i) t[i] = i < lim ? t[i] : -INFINITY;
-          }
-        }
-        if (zero_scale) {
-#pragma unroll
-          for (int i = 0; i < 128; ++i) t[i] = (t[i] == -INFINITY) ? -INFINITY : 0.f;
-        }
-        // Row max over 128 values in 16 independent chains of 3-input maxima.
-        float q[16];
-#pragma unroll
-        for (int kq = 0; kq < 16; ++kq) q[kq] = fmax3(t[8 * kq], t[8 * kq + 1], t[8 * kq + 2]);
-#pragma unroll
-        for (int kq = 0; kq < 16; ++kq) q[kq] = fmax3(q[kq], t[8 * kq + 3], t[8 * kq + 4]);
-#pragma unroll
-        for (int kq = 0; kq < 16; ++kq) q[kq] = fmax3(q[kq], t[8 * kq + 5], t[8 * kq + 6]);
-#pragma unroll
-        for (int kq = 0; kq < 16; ++kq) q[kq] = fmaxf(q[kq], t[8 * kq + 7]);
-        const float r0 = fmax3(q[0], q[1], q[2]), r1 = fmax3(q[3], q[4], q[5]);
-        const float r2 = fmax3(q[6], q[7], q[8]), r3 = fmax3(q[9], q[10], q[11]);
-        const float r4 = fmax3(q[12], q[13], q[14]);
-        const float tmax = fmaxf(fmax3(r0, r1, r2), fmax3(r3, r4, q[15]));
-        const float mx = tmax * c;
-        const float m_new = (mx > m + kRescaleLog2) ? mx : m;  // also moves off -inf
-        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        float tmax, m_new, m_use;
         // p = 2^(sigma - m_use), rounded to bf16 over the second half of S's
         // buffer (its scores are in registers), from where P_j V_j reads it.
         const uint32_t p_t = s_t + 64u;
-        const float2 cc = make_float2(c, c), nm = make_float2(-m_use, -m_use);
         const bool p_ok = !kDebugChecks || __all_sync(0xffffffffu, tmem_ok(p_t, 32u, 64u));
         // Four packed sum chains keep the additions off each other's latency.
         float2 a[4];
 #pragma unroll
         for (int kq = 0; kq < 4; ++kq) a[kq] = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float2 x =
-                __ffma2_rn(make_float2(t[64 * hh + 2 * i], t[64 * hh + 2 * i + 1]), cc, nm);
-            const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-            a[i & 3] = __fadd2_rn(a[i & 3], p);
-            pk[i] = pack_bf16x2(p.x, p.y);
+        if constexpr (NG == 1) {
+          float t[128];
+          if (!kDebugChecks || __all_sync(0xffffffffu, tmem_ok(s_t, 32u, 128u))) {
+            uint32_t raw[64];
+            tmem_ld64(s_t, raw);
+  #pragma unroll
+            for (int i = 0; i < 64; ++i) t[i] = __uint_as_float(raw[i]);
+            tmem_ld64(s_t + 64, raw);
+  #pragma unroll
+            for (int i = 0; i < 64; ++i) t[64 + i] = __uint_as_float(raw[i]);
+          } else {
+  #pragma unroll
+            for (int i = 0; i < 128; ++i) t[i] = 0.f;
           }
-          if (p_ok) tmem_st32(p_t + 32u * hh, pk);
+          if (masked) {
+            int lim = L - kbase;  // keys [lo, lim) of the tile are visible
+            if (args.causal) lim = min(lim, qpos - kbase + 1);
+            if (args.window > 0) {
+              const int lo = qpos - args.window + 1 - kbase;
+  #pragma unroll
+              for (int i = 0; i < 128; ++i)
+                if (i >= lim || i < lo) t[i] = -INFINITY;
+            } else {
+              // Without a window the visible keys are a prefix: one compare.
+  #pragma unroll
+              for (int i = 0; i < 128; ++i) t[i] = i < lim ? t[i] : -INFINITY;
+            }
+          }
+          if (zero_scale) {
+  #pragma unroll
+            for (int i = 0; i < 128; ++i) t[i] = (t[i] == -INFINITY) ? -INFINITY : 0.f;
+          }
+          // Row max over 128 values in 16 independent chains of 3-input maxima.
+          float q[16];
+  #pragma unroll
+          for (int kq = 0; kq < 16; ++kq) q[kq] = fmax3(t[8 * kq], t[8 * kq + 1], t[8 * kq + 2]);
+  #pragma unroll
+          for (int kq = 0; kq < 16; ++kq) q[kq] = fmax3(q[kq], t[8 * kq + 3], t[8 * kq + 4]);
+  #pragma unroll
+          for (int kq = 0; kq < 16; ++kq) q[kq] = fmax3(q[kq], t[8 * kq + 5], t[8 * kq + 6]);
+  #pragma unroll
+          for (int kq = 0; kq < 16; ++kq) q[kq] = fmaxf(q[kq], t[8 * kq + 7]);
+          const float r0 = fmax3(q[0], q[1], q[2]), r1 = fmax3(q[3], q[4], q[5]);
+          const float r2 = fmax3(q[6], q[7], q[8]), r3 = fmax3(q[9], q[10], q[11]);
+          const float r4 = fmax3(q[12], q[13], q[14]);
+          tmax = fmaxf(fmax3(r0, r1, r2), fmax3(r3, r4, q[15]));
+          const float mx = tmax * c;
+          m_new = (mx > m + kRescaleLog2) ? mx : m;  // also moves off -inf
+          m_use = (m_new == -INFINITY) ? 0.f : m_new;
+          const float2 cc = make_float2(c, c), nm = make_float2(-m_use, -m_use);
+  #pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t pk[32];
+  #pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float2 x =
+                  __ffma2_rn(make_float2(t[64 * hh + 2 * i], t[64 * hh + 2 * i + 1]), cc, nm);
+              const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+              a[i & 3] = __fadd2_rn(a[i & 3], p);
+              pk[i] = pack_bf16x2(p.x, p.y);
+            }
+            if (p_ok) tmem_st32(p_t + 32u * hh, pk);
+          }
+        } else {
+          // Two softmax groups share the registers of 352 threads, so the
+          // tile is taken in 64-key halves: both halves' maxima first, then
+          // the weights of keys 64..127 from registers (their P goes over S
+          // columns 96..127, whose scores are in registers), then keys 0..63
+          // reloaded from the first half of the buffer, which P never
+          // covers (their P over columns 64..95).
+          const bool s_in = !kDebugChecks || __all_sync(0xffffffffu, tmem_ok(s_t, 32u, 128u));
+          int lim = C::BN, lo = -1;  // the row's visible keys of the tile: [lo, lim)
+          if (masked) {
+            lim = L - kbase;
+            if (args.causal) lim = min(lim, qpos - kbase + 1);
+            if (args.window > 0) lo = qpos - args.window + 1 - kbase;
+          }
+          auto load_half = [&](int hh, float (&x)[64]) {
+            uint32_t raw[64];
+            if (s_in) {
+              tmem_ld64(s_t + 64u * hh, raw);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 64; ++i) raw[i] = 0u;
+            }
+#pragma unroll
+            for (int i = 0; i < 64; ++i) x[i] = __uint_as_float(raw[i]);
+            if (masked) {
+#pragma unroll
+              for (int i = 0; i < 64; ++i)
+                if (64 * hh + i >= lim || 64 * hh + i < lo) x[i] = -INFINITY;
+            }
+            if (zero_scale) {
+#pragma unroll
+              for (int i = 0; i < 64; ++i) x[i] = (x[i] == -INFINITY) ? -INFINITY : 0.f;
+            }
+          };
+          float th[64];
+          float q[16];
+          load_half(0, th);
+#pragma unroll
+          for (int kq = 0; kq < 8; ++kq) {
+            q[kq] = fmax3(th[8 * kq], th[8 * kq + 1], th[8 * kq + 2]);
+            q[kq] = fmax3(q[kq], th[8 * kq + 3], th[8 * kq + 4]);
+            q[kq] = fmax3(q[kq], th[8 * kq + 5], th[8 * kq + 6]);
+            q[kq] = fmaxf(q[kq], th[8 * kq + 7]);
+          }
+          load_half(1, th);  // keys 64..127, kept
+#pragma unroll
+          for (int kq = 0; kq < 8; ++kq) {
+            q[8 + kq] = fmax3(th[8 * kq], th[8 * kq + 1], th[8 * kq + 2]);
+            q[8 + kq] = fmax3(q[8 + kq], th[8 * kq + 3], th[8 * kq + 4]);
+            q[8 + kq] = fmax3(q[8 + kq], th[8 * kq + 5], th[8 * kq + 6]);
+            q[8 + kq] = fmaxf(q[8 + kq], th[8 * kq + 7]);
+          }
+          const float r0 = fmax3(q[0], q[1], q[2]), r1 = fmax3(q[3], q[4], q[5]);
+          const float r2 = fmax3(q[6], q[7], q[8]), r3 = fmax3(q[9], q[10], q[11]);
+          const float r4 = fmax3(q[12], q[13], q[14]);
+          tmax = fmaxf(fmax3(r0, r1, r2), fmax3(r3, r4, q[15]));
+          const float mx = tmax * c;
+          m_new = (mx > m + kRescaleLog2) ? mx : m;  // also moves off -inf
+          m_use = (m_new == -INFINITY) ? 0.f : m_new;
+          const float2 cc = make_float2(c, c), nm = make_float2(-m_use, -m_use);
+          auto exp_half = [&](const float (&x)[64], uint32_t dst) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float2 xv = __ffma2_rn(make_float2(x[2 * i], x[2 * i + 1]), cc, nm);
+              const float2 p = make_float2(ex2_approx(xv.x), ex2_approx(xv.y));
+              a[i & 3] = __fadd2_rn(a[i & 3], p);
+              pk[i] = pack_bf16x2(p.x, p.y);
+            }
+            if (p_ok) tmem_st32(dst, pk);
+          };
+          exp_half(th, p_t + 32u);
+          load_half(0, th);
+          exp_half(th, p_t);
         }
         const float alpha = (m_new == m) ? 1.f : ex2_approx(m - m_use);
         const float2 aa = __fadd2_rn(__fadd2_rn(a[0], a[1]), __fadd2_rn(a[2], a[3]));
@@ -622,17 +730,37 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
         dsum = dsum * alpha + (aa.x + aa.y);
         m = m_new;
 
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          // o <- alpha * o between P_{j-1} V_{j-1} and P_j V_j (rare: only
-          // when a row of this warp moved its reference maximum).
-          const bool w2 = mbar_wait(bar(C::B_PV_DONE + (g - 1) % C::NS), ((g - 1) / C::NS) & 1,
-                                    abort_flag, args.status, wlim);
-          if (__any_sync(0xffffffffu, !w2)) {
-            ok = false;
-            break;
+        if constexpr (NG > 1) {
+          // A group confirms its previous P V product at every tile, before
+          // it signals the next one: PV_GRP(grp) then never runs more than
+          // one phase ahead of the phase a wait names (a parity wait is only
+          // sound under that bound).
+          if (j >= NG) {
+            const bool w2 = mbar_wait(bar(C::B_PV_GRP + grp), (pvn - 1) & 1, abort_flag,
+                                      args.status, wlim);
+            if (__any_sync(0xffffffffu, !w2)) {
+              ok = false;
+              break;
+            }
+          }
+        }
+        if (j >= NG && __any_sync(0xffffffffu, alpha != 1.f)) {
+          // o <- alpha * o between the group's previous P V product and
+          // P_j V_j (rare: only when a row of this warp moved its reference
+          // maximum).  With one group that product's S buffer barrier is
+          // waited for (its next phase needs this warp's P, so it cannot
+          // run ahead of the wait); with two, the product was confirmed
+          // above.
+          if constexpr (NG == 1) {
+            const bool w2 = mbar_wait(bar(C::B_PV_DONE + (g - 1) % C::NS),
+                                      ((g - 1) / C::NS) & 1, abort_flag, args.status, wlim);
+            if (__any_sync(0xffffffffu, !w2)) {
+              ok = false;
+              break;
+            }
           }
           tc_fence_after();
-          const uint32_t o_t = tmem + lane_off + C::TMEM_O;
+          const uint32_t o_t = tmem + lane_off + C::TMEM_O + grp * D;
           const bool o_ok = !kDebugChecks || __all_sync(0xffffffffu, tmem_ok(o_t, 32u, D));
 #pragma unroll
           for (int c0 = 0; c0 < D && o_ok; c0 += 32) {
@@ -646,16 +774,28 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(C::B_P_FULL + sb));
+        ++pvn;
       }
       if (!ok) break;
 
       // ---- epilogue of the item ----
-      const int gl = g0 + n_kv - 1;
-      const bool w = mbar_wait(bar(C::B_PV_DONE + gl % C::NS), (gl / C::NS) & 1, abort_flag,
-                               args.status, wlim);
-      if (__any_sync(0xffffffffu, !w)) {
-        ok = false;
-        break;
+      // The group's last P V product of the item (none for a group beyond
+      // the item's tile count): with one group, through the S buffer
+      // barrier of the item's last step; with two, through the group's
+      // barrier (its earlier products were confirmed tile by tile).
+      if (n_kv > grp) {
+        bool w;
+        if constexpr (NG == 1) {
+          const int gl = g0 + n_kv - 1;
+          w = mbar_wait(bar(C::B_PV_DONE + gl % C::NS), (gl / C::NS) & 1, abort_flag,
+                        args.status, wlim);
+        } else {
+          w = mbar_wait(bar(C::B_PV_GRP + grp), (pvn - 1) & 1, abort_flag, args.status, wlim);
+        }
+        if (__any_sync(0xffffffffu, !w)) {
+          ok = false;
+          break;
+        }
       }
       tc_fence_after();
       const int qb = ti & 1;
@@ -670,6 +810,93 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
       } else {
         orow = static_cast<size_t>(it.bh) * args.N + qpos;
         lidx = orow;
+      }
+      if constexpr (NG == 2) {
+        // Two partial states per row: group 0 (here) and group 1, whose
+        // (m, dsum, dnorm) come through shared memory and whose O is read
+        // from its TMEM accumulator once final.  They merge by the rule of
+        // "The Merge, and the Twist": both sides rescaled to the larger
+        // reference.  Rows are stored one by one (D = 64).
+        float* xch = reinterpret_cast<float*>(smem + C::OFF_XCH);
+        if (grp == 1) {
+          xch[4 * r + 0] = m;
+          xch[4 * r + 1] = dsum;
+          xch[4 * r + 2] = dnorm;
+          tc_fence_before();
+          mbar_arrive(bar(C::B_XCH_FULL));
+          // Group 0 reads this group's O before its next item overwrites it.
+          const bool w3 = mbar_wait(bar(C::B_XCH_DONE), ti & 1, abort_flag, args.status, wlim);
+          if (__any_sync(0xffffffffu, !w3)) {
+            ok = false;
+            break;
+          }
+        } else {
+          const bool w3 = mbar_wait(bar(C::B_XCH_FULL), ti & 1, abort_flag, args.status, wlim);
+          if (__any_sync(0xffffffffu, !w3)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const bool has1 = n_kv > 1;  // group 1 folded a tile of this item
+          const float m1 = has1 ? xch[4 * r + 0] : -INFINITY;
+          const float ds1 = xch[4 * r + 1], dn1 = xch[4 * r + 2];
+          const uint32_t o_t0 = tmem + lane_off + C::TMEM_O;
+          const bool o_in = !kDebugChecks || __all_sync(0xffffffffu, tmem_ok(o_t0, 32u, 2u * D));
+          const float M = fmaxf(m, m1);
+          const float f0 = (m == -INFINITY) ? 0.f : ex2_approx(m - M);
+          const float f1 = (m1 == -INFINITY) ? 0.f : ex2_approx(m1 - M);
+          const float dn = dnorm * f0 + (has1 ? dn1 * f1 : 0.f);
+          const float ds = dsum * f0 + (has1 ? ds1 * f1 : 0.f);
+          const float inv = dn > 0.f ? 1.f / dn : 0.f;
+          const float lse2 = ds > 0.f ? (M + log2f(ds)) * 0.69314718055994530942f : -INFINITY;
+          const bool store2 = qpos < L;
+          const size_t rows_total = varlen ? static_cast<size_t>(args.total_tokens) * args.H
+                                           : static_cast<size_t>(BHt) * args.N;
+          const bool out_in =
+              !store2 || fa_dbg_ok(orow < rows_total && lidx < rows_total, args.status);
+          const float s0 = f0 * inv, s1 = f1 * inv;
+          // 32 columns of each accumulator at a time, merged and stored.
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o0[32], o1[32];
+            if (o_in) tmem_ld32(o_t0 + c0, o0);
+            if (o_in && has1) tmem_ld32(o_t0 + D + c0, o1);
+            if (store2 && out_in && o_in) {
+              float ov[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                ov[i] = __uint_as_float(o0[i]) * s0 + (has1 ? __uint_as_float(o1[i]) * s1 : 0.f);
+              if (args.o_f32) {
+                float4* dst =
+                    reinterpret_cast<float4*>(static_cast<float*>(args.o) + orow * D + c0);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                  dst[i] = make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
+              } else {
+                uint4* dst =
+                    reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.o) + orow * D + c0);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  uint4 u;
+                  u.x = pack_bf16x2(ov[8 * i + 0], ov[8 * i + 1]);
+                  u.y = pack_bf16x2(ov[8 * i + 2], ov[8 * i + 3]);
+                  u.z = pack_bf16x2(ov[8 * i + 4], ov[8 * i + 5]);
+                  u.w = pack_bf16x2(ov[8 * i + 6], ov[8 * i + 7]);
+                  dst[i] = u;
+                }
+              }
+            }
+          }
+          // Group 1's accumulator has been read: its next item may overwrite it.
+          tc_fence_before();
+          mbar_arrive(bar(C::B_XCH_DONE));
+          if (store2 && out_in) args.lse[lidx] = lse2;
+          tc_fence_before();
+          mbar_arrive(bar(C::B_Q_EMPTY + qb));
+        }
+        g0 += n_kv;
+        ++ti;
+        continue;
       }
       const uint32_t o_t = tmem + lane_off + C::TMEM_O;
       const int wrow0 = mb * C::BM + quarter * 32;  // this warp's first row
@@ -783,21 +1010,21 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
   }
 }
 
-template <int D>
+template <int D, int NG>
 static cudaError_t launch_tc_impl(const TcMaps& maps, const TcFwdArgs& a, int grid_x,
                                   cudaStream_t stream) {
-  using C = TcCfg<D>;
+  using C = TcCfg<D, NG>;
   // The shared-memory opt-in is a per-device attribute of each function.
   static std::atomic<bool> attr_set[64];  // per device: attributes already set
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D, false>,
+    e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D, false, NG>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::SMEM_BYTES));
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D, true>,
+    e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D, true, NG>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::SMEM_BYTES));
     if (e != cudaSuccess) return e;
@@ -822,18 +1049,19 @@ static cudaError_t launch_tc_impl(const TcMaps& maps, const TcFwdArgs& a, int gr
                         ? 1
                         : 0;
   if (args.persistent)
-    fa_fwd_tc_kernel<D, true><<<dim3(static_cast<unsigned>(nsm)), C::THREADS, C::SMEM_BYTES,
-                                stream>>>(maps.q, maps.k, maps.v, maps.o, args);
+    fa_fwd_tc_kernel<D, true, NG><<<dim3(static_cast<unsigned>(nsm)), C::THREADS, C::SMEM_BYTES,
+                                    stream>>>(maps.q, maps.k, maps.v, maps.o, args);
   else
-    fa_fwd_tc_kernel<D, false><<<dim3(static_cast<unsigned>(args.num_items)), C::THREADS,
-                                 C::SMEM_BYTES, stream>>>(maps.q, maps.k, maps.v, maps.o, args);
+    fa_fwd_tc_kernel<D, false, NG><<<dim3(static_cast<unsigned>(args.num_items)), C::THREADS,
+                                     C::SMEM_BYTES, stream>>>(maps.q, maps.k, maps.v, maps.o,
+                                                              args);
   return cudaGetLastError();
 }
 
 cudaError_t launch_fwd_tc(const TcMaps& maps, const TcFwdArgs& a, int D, int grid_x,
                           cudaStream_t stream) {
-  if (D == 128) return launch_tc_impl<128>(maps, a, grid_x, stream);
-  return launch_tc_impl<64>(maps, a, grid_x, stream);
+  if (D == 128) return launch_tc_impl<128, 1>(maps, a, grid_x, stream);
+  return launch_tc_impl<64, kSoftmaxGroups64>(maps, a, grid_x, stream);
 }
 
 }  // namespace fa

@@ -102,6 +102,23 @@ def test_config2_full(fa):
     check_lse(np64(lse), L)
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_persistent_equals_one_item(fa, D):
+    """B=4 H=16 N=2048 causal (1024 query tiles, more than the SMs) runs on
+    persistent CTAs; each head alone (16 tiles) runs one tile per CTA.  The
+    per-tile arithmetic is the same, so the outputs agree bit for bit."""
+    case = inp.dense(4, 16, 2048, D, seed=60 + D, causal=True)
+    q, k, v = _dense_gpu(case)
+    o, lse = fa.fa_fwd(q, k, v, case.scale, True)
+    for b in range(4):
+        for h in range(16):
+            sl = lambda t: t[b:b + 1, h:h + 1].contiguous()
+            o1, l1 = fa.fa_fwd(sl(q), sl(k), sl(v), case.scale, True)
+            assert torch.equal(o1[0, 0], o[b, h]), (b, h)
+            assert torch.equal(l1[0, 0], lse[b, h]), (b, h)
+    assert fa.fa_check_device_status() == fa.FA_OK
+
+
 @pytest.mark.parametrize("c", [-90.0, 50.0, 90.0, 200.0])
 def test_offset_invariance(fa, c):
     """Append a coordinate so every score of a row moves by c (q' = [q, c/scale],
