@@ -301,9 +301,7 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
   // KV step of the CTA go to ring stages g % KS and g % VS, the Q tile of the
   // t-th item to buffer t % 2.
   int k_issued = 0, v_issued = 0, q_issued = 0;
-  bool k_skipped[C::KS];  // the stage's last request was left out (fault injection)
-#pragma unroll
-  for (int s = 0; s < C::KS; ++s) k_skipped[s] = false;
+  uint32_t k_skipped = 0;  // bit s: stage s's last request was left out (fault injection)
   // The tile of KV step j of item `it` (global step g) into its ring, once
   // the product that read the stage's previous tile has finished.
   auto load_kv = [&](bool is_v, const Item& it, int j, int g) -> bool {
@@ -318,8 +316,11 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
       k_issued = g + 1;
       // Fault injection (tests of the timeout path only): this key tile is
       // never requested, so its full barrier never completes.
-      k_skipped[st] = j == args.skip_k_tile;
-      if (k_skipped[st]) return true;
+      if (j == args.skip_k_tile) {
+        k_skipped |= 1u << st;
+        return true;
+      }
+      k_skipped &= ~(1u << st);
     }
     const uint32_t fb = bar((is_v ? C::B_V_FULL : C::B_K_FULL) + st);
     const uint32_t dst = sbase + (is_v ? C::OFF_V : C::OFF_K) + st * C::TILE_BYTES;
@@ -437,7 +438,7 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
         for (int i = max(0, q_issued - 2); i < q_issued; ++i)
           mbar_wait_unwind(bar(C::B_Q_FULL + (i & 1)), (i >> 1) & 1);
         for (int g = max(0, k_issued - C::KS); g < k_issued; ++g)
-          if (!k_skipped[g % C::KS])  // never requested: nothing in flight
+          if (!((k_skipped >> (g % C::KS)) & 1u))  // never requested: nothing in flight
             mbar_wait_unwind(bar(C::B_K_FULL + g % C::KS), (g / C::KS) & 1);
         for (int g = max(0, v_issued - C::VS); g < v_issued; ++g)
           mbar_wait_unwind(bar(C::B_V_FULL + g % C::VS), (g / C::VS) & 1);
