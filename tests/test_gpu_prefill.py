@@ -227,6 +227,25 @@ def test_long_sequence_sampled(fa, N, D, causal, qk_std):
 
 # --- varlen -------------------------------------------------------------------------
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_two_group_odd_tile_counts(fa, causal):
+    """D = 64 splits a query tile's key tiles between two softmax groups
+    (even and odd tiles) and merges their states: sequences of 1, 2, 3 and
+    5 key tiles (group 1 with no tile, one, or fewer than group 0), ragged
+    tails, keys that grow along the sequence so that the reference maximum
+    moves inside each group."""
+    for N in (100, 200, 300, 600):
+        case = inp.dense(1, 3, N, 64, seed=70 + N, causal=causal, qk_std=3.0)
+        ramp = (1.0 + 3.0 * torch.arange(N, dtype=torch.float32) / N).view(1, 1, -1, 1)
+        k = (case.k.float() * ramp).to(torch.bfloat16)
+        o, lse = fa.fa_fwd_ex(case.q.cuda(), k.cuda(), case.v.cuda(), case.scale, causal,
+                              o_dtype=torch.float32)
+        O, L = ora.attention_ref(case.q, k, case.v, case.scale, causal)
+        check_o_f32(np64(o), O, f"two groups N={N} causal={causal}")
+        check_lse(np64(lse), L)
+    assert fa.fa_check_device_status() == fa.FA_OK
+
+
 @pytest.mark.parametrize("D", [64, 128])
 def test_varlen_small(fa, D):
     lens = [1, 127, 128, 129, 0, 300, 5, 257]

@@ -52,6 +52,27 @@ def test_window_long_sampled(fa):
     check_lse(np64(lse.index_select(2, ri)), L)
 
 
+@pytest.mark.parametrize("D,w", [(128, 300), (64, 300), (64, 129)])
+def test_window_persistent(fa, D, w):
+    """B=2 H=40 N=1300 (880 query tiles, more than the SMs) runs on persistent
+    CTAs: window edges inside items, items whose key range starts past the
+    first tile.  Two heads against the oracle, every head against the same
+    head launched alone (one tile per CTA) bit for bit."""
+    case = inp.dense(2, 40, 1300, D, seed=w + 3 * D, causal=True, qk_std=2.0)
+    q, k, v = case.q.cuda(), case.k.cuda(), case.v.cuda()
+    o, lse = fa.fa_fwd_window(q, k, v, w, case.scale)
+    O, L = ora.attention_ref(case.q[:, :1], case.k[:, :1], case.v[:, :1], case.scale, True,
+                             window=w)
+    check_o_bf16(np64(o[:, :1]), O, f"window {w} D={D}")
+    check_lse(np64(lse[:, :1]), L)
+    for b in range(2):
+        for h in range(0, 40, 7):
+            sl = lambda t: t[b:b + 1, h:h + 1].contiguous()
+            o1, l1 = fa.fa_fwd_window(sl(q), sl(k), sl(v), w, case.scale)
+            assert torch.equal(o1[0, 0], o[b, h]) and torch.equal(l1[0, 0], lse[b, h]), (b, h)
+    assert fa.fa_check_device_status() == fa.FA_OK
+
+
 def test_window_invalid(fa):
     q = torch.zeros(1, 1, 16, 64, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(fa.FAError) as e:
