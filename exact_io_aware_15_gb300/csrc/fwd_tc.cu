@@ -142,6 +142,7 @@ struct TcCfg {
   static constexpr uint32_t TMEM_S = 0;    // buffer b at TMEM_S + 128 b
   static constexpr uint32_t TMEM_O = 384;  // group g's O at TMEM_O + g D
   static_assert(TMEM_O + NG * D <= TMEM_COLS, "S buffers and O accumulators exceed TMEM");
+  static_assert(SMEM_BYTES <= 227u * 1024u, "shared memory per CTA exceeded");
   static constexpr int WARP_PV = NG == 1 ? 6 : 2;
   static constexpr int WARP_SM0 = NG == 1 ? 2 : 3;  // first softmax warp
   static constexpr int THREADS = 32 * (WARP_SM0 + 4 * NG + (NG == 1 ? 1 : 0));
