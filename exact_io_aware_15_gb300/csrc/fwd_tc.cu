@@ -199,23 +199,28 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
   // the bounds check (reported once, by thread 0), gets n_kv = 0 and is
   // skipped by every role.
   auto item_at = [&](int k, Item& it) -> bool {
+    // (32-bit unsigned divisions: num_items fits in an int, and the 64-bit
+    // ones cost several hundred cycles at every item change)
     int mb, bh;
     if constexpr (PERSIST) {
-      const int P = static_cast<int>(gridDim.x);
-      const int c = static_cast<int>(blockIdx.x);
-      const long long idx = static_cast<long long>(k) * P + ((k & 1) ? P - 1 - c : c);
-      if (idx >= args.num_items) return false;
-      mb = nmb - 1 - static_cast<int>(idx / BHt);
-      bh = static_cast<int>(idx % BHt);
+      const unsigned P = gridDim.x;
+      const unsigned c = blockIdx.x;
+      if (static_cast<long long>(k) * P >= args.num_items) return false;
+      const unsigned idx = static_cast<unsigned>(k) * P + ((k & 1) ? P - 1u - c : c);
+      if (idx >= static_cast<unsigned>(args.num_items)) return false;
+      const unsigned hq = idx / static_cast<unsigned>(BHt);
+      mb = nmb - 1 - static_cast<int>(hq);
+      bh = static_cast<int>(idx - hq * static_cast<unsigned>(BHt));
     } else {
       if (k > 0) return false;
-      const long long lin = blockIdx.x;
-      const long long per_group = 4LL * nmb;
-      const int g = static_cast<int>(lin / per_group);
-      const int gsize = min(4, BHt - g * 4);
-      const int rr = static_cast<int>(lin - g * per_group);
-      mb = nmb - 1 - rr / gsize;
-      bh = g * 4 + rr % gsize;
+      const unsigned lin = blockIdx.x;
+      const unsigned per_group = 4u * static_cast<unsigned>(nmb);
+      const unsigned g = lin / per_group;
+      const unsigned gsize = static_cast<unsigned>(min(4, BHt - static_cast<int>(g) * 4));
+      const unsigned rr = lin - g * per_group;
+      const unsigned q = rr / gsize;
+      mb = nmb - 1 - static_cast<int>(q);
+      bh = static_cast<int>(g * 4u + (rr - q * gsize));
     }
     it.mb = mb;
     it.bh = bh;
@@ -553,6 +558,17 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
     bool ok = true;
     int g0 = 0, ti = 0, k = first_k;
     Item it = first;
+    // Persistent CTAs: the Q buffer holding an item's O for TMA stores whose
+    // read of it has not been waited for yet (-1: none).  Lane 0 of the warp
+    // issued the stores; the buffer is released (Q_EMPTY) after the wait.
+    int q_release = -1;
+    auto release_q = [&]() {
+      if (lane == 0) tma_store_wait_read();
+      __syncwarp();
+      tc_fence_before();
+      mbar_arrive(bar(C::B_Q_EMPTY + q_release));
+      q_release = -1;
+    };
     do {
       const int mb = it.mb, L = it.L, j0 = it.j0, n_kv = it.n_kv;
       const int qpos = mb * C::BM + r;
@@ -777,10 +793,29 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
         tc_fence_before();
         mbar_arrive(bar(C::B_P_FULL + sb));
         ++pvn;
+        if constexpr (PERSIST && NG == 1) {
+          // the previous item's staged O: its TMA stores have read it by now
+          if (q_release >= 0) release_q();
+        }
       }
       if (!ok) break;
 
       // ---- epilogue of the item ----
+      // (the row's scalars first: they need only the state, and overlap the
+      // wait for the last product)
+      const int qb = ti & 1;
+      const float inv = dnorm > 0.f ? 1.f / dnorm : 0.f;
+      const float lse = dsum > 0.f ? (m + log2f(dsum)) * 0.69314718055994530942f : -INFINITY;
+      const bool store = qpos < L;
+      size_t orow, lidx;
+      if (varlen) {
+        const size_t tk = static_cast<size_t>(it.tok0) + qpos;
+        orow = tk * args.H + it.h;
+        lidx = static_cast<size_t>(it.h) * args.total_tokens + tk;
+      } else {
+        orow = static_cast<size_t>(it.bh) * args.N + qpos;
+        lidx = orow;
+      }
       // The group's last P V product of the item (none for a group beyond
       // the item's tile count): with one group, through the S buffer
       // barrier of the item's last step; with two, through the group's
@@ -800,19 +835,6 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
         }
       }
       tc_fence_after();
-      const int qb = ti & 1;
-      const float inv = dnorm > 0.f ? 1.f / dnorm : 0.f;
-      const float lse = dsum > 0.f ? (m + log2f(dsum)) * 0.69314718055994530942f : -INFINITY;
-      const bool store = qpos < L;
-      size_t orow, lidx;
-      if (varlen) {
-        const size_t tk = static_cast<size_t>(it.tok0) + qpos;
-        orow = tk * args.H + it.h;
-        lidx = static_cast<size_t>(it.h) * args.total_tokens + tk;
-      } else {
-        orow = static_cast<size_t>(it.bh) * args.N + qpos;
-        lidx = orow;
-      }
       if constexpr (NG == 2) {
         // Two partial states per row: group 0 (here) and group 1, whose
         // (m, dsum, dnorm) come through shared memory and whose O is read
@@ -919,23 +941,20 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
         // warp with rows past its end stores row by row below.)  At D = 64 a
         // row is 128 bytes and the row-by-row stores are faster.
         uint8_t* qbuf = smem + C::OFF_Q + qb * C::TILE_BYTES;
+        uint32_t ov[128];  // the row's 128 columns in one TMEM load and wait
+        tmem_ld128(o_t, ov);
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 64) {
-          uint32_t ov[64];
-          tmem_ld64(o_t + c0, ov);
+        for (int c0 = 0; c0 < 128; c0 += 64) {
           uint8_t* row = qbuf + (c0 / 64) * C::HALF_BYTES + r * 128;
           if (!smem_ok(sbase + static_cast<uint32_t>(row - smem), 128u)) continue;
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch) {
+            const uint32_t* v8 = ov + c0 + 8 * ch;
             uint4 u;
-            u.x = pack_bf16x2(__uint_as_float(ov[8 * ch + 0]) * inv,
-                              __uint_as_float(ov[8 * ch + 1]) * inv);
-            u.y = pack_bf16x2(__uint_as_float(ov[8 * ch + 2]) * inv,
-                              __uint_as_float(ov[8 * ch + 3]) * inv);
-            u.z = pack_bf16x2(__uint_as_float(ov[8 * ch + 4]) * inv,
-                              __uint_as_float(ov[8 * ch + 5]) * inv);
-            u.w = pack_bf16x2(__uint_as_float(ov[8 * ch + 6]) * inv,
-                              __uint_as_float(ov[8 * ch + 7]) * inv);
+            u.x = pack_bf16x2(__uint_as_float(v8[0]) * inv, __uint_as_float(v8[1]) * inv);
+            u.y = pack_bf16x2(__uint_as_float(v8[2]) * inv, __uint_as_float(v8[3]) * inv);
+            u.z = pack_bf16x2(__uint_as_float(v8[4]) * inv, __uint_as_float(v8[5]) * inv);
+            u.w = pack_bf16x2(__uint_as_float(v8[6]) * inv, __uint_as_float(v8[7]) * inv);
             *reinterpret_cast<uint4*>(row + ((ch ^ (r & 7)) << 4)) = u;
           }
         }
@@ -952,9 +971,14 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
             else
               tma_store_3d(&tm_o, src, cc * 64, wrow0, it.bh);
           }
-          tma_store_commit_and_wait_read();
+          tma_store_commit();
+          // One item per CTA: the staging buffer must be read before the CTA
+          // exits.  Persistent: the wait and the buffer's release follow the
+          // next item's first tile (the stores read it meanwhile).
+          if constexpr (!PERSIST) tma_store_wait_read();
         }
         __syncwarp();
+        if constexpr (PERSIST) q_release = qb;
       } else {
         // 64 columns per TMEM load (one wait each), then the stores.
 #pragma unroll
@@ -993,12 +1017,21 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
       }
       if (store && out_in) args.lse[lidx] = lse;
       // The item's Q buffer may take the Q tile of item ti + 2: its products
-      // have finished (P_last V_last has) and the staged O has been read.
-      tc_fence_before();
-      mbar_arrive(bar(C::B_Q_EMPTY + qb));
+      // have finished (P_last V_last has) and the staged O has been read
+      // (or, for deferred TMA stores, will have been once q_release runs).
+      if (q_release != qb) {
+        tc_fence_before();
+        mbar_arrive(bar(C::B_Q_EMPTY + qb));
+      }
       g0 += n_kv;
       ++ti;
     } while (ok && next_item(k, it));
+    // Outstanding stores read shared memory until this wait; the CTA may not
+    // exit before.
+    if (q_release >= 0) {
+      if (lane == 0) tma_store_wait_read();
+      __syncwarp();
+    }
     tc_fence_before();
   }
 
