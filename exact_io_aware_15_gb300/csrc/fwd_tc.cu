@@ -134,7 +134,11 @@ struct TcCfg {
   static constexpr int B_XCH_FULL = B_PV_GRP + NG;
   static constexpr int B_XCH_DONE = B_XCH_FULL + 1;
   static constexpr int B_DRAIN = B_XCH_DONE + 1;  // one per issuing thread
-  static constexpr int NUM_BARS = B_DRAIN + 2;
+  // PH_FULL(b) (two groups, one item per CTA): P's second half (keys
+  // 64..127) is in S buffer b, so P_j V_j may start on those keys while the
+  // first half is computed.
+  static constexpr int B_PH_FULL = B_DRAIN + 2;
+  static constexpr int NUM_BARS = B_PH_FULL + NS;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr uint32_t OFF_XCH = (OFF_MISC + 16 + 15) & ~15u;  // [128 rows][4] floats
   static constexpr uint32_t SMEM_BYTES = OFF_XCH + (NG > 1 ? 128 * 16 : 0) + 1024;  // + slack
@@ -174,6 +178,10 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
                      const __grid_constant__ CUtensorMap tm_o, const TcFwdArgs args) {
   using C = TcCfg<D, NG>;
   extern __shared__ uint8_t smem_raw[];
+  // Two groups, one item per CTA: P V products start on P's second half
+  // (PH_FULL).  (The persistent instantiation keeps one signal per P: the
+  // early rescale's registers cost it more than the split gains.)
+  constexpr bool kHalfP = NG > 1 && !PERSIST;
 
   const int nmb = args.num_mblocks;
   const int BHt = args.num_items / nmb;  // (sequence, head) pairs
@@ -395,6 +403,7 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
     mbar_init(bar(C::B_XCH_DONE), C::SOFTMAX_THREADS);
     mbar_init(bar(C::B_DRAIN), 1);
     mbar_init(bar(C::B_DRAIN + 1), 1);
+    for (int b = 0; b < C::NS; ++b) mbar_init(bar(C::B_PH_FULL + b), C::SOFTMAX_THREADS);
     *abort_flag = 0;
     fence_mbar_init();
     // The first item's copies need no free stage: start them before the
@@ -508,8 +517,9 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
         for (int j = 0; j < it.n_kv; ++j) {
           const int g = g0 + j;
           const int sv = g % C::VS;
-          if (!mbar_wait(bar(C::B_P_FULL + g % C::NS), (g / C::NS) & 1, abort_flag, args.status,
-                         wlim) ||
+          // (split P: the products on P's second half wait only for it)
+          if (!mbar_wait(bar((kHalfP ? C::B_PH_FULL : C::B_P_FULL) + g % C::NS), (g / C::NS) & 1,
+                         abort_flag, args.status, wlim) ||
               !mbar_wait(bar(C::B_V_FULL + sv), (g / C::VS) & 1, abort_flag, args.status, wlim)) {
             ok = false;
             break;
@@ -524,14 +534,35 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
           const uint32_t o_acc = tmem + C::TMEM_O + grp * D;
           const bool in_range = smem_ok(v_s, C::TILE_BYTES) && tmem_ok(p_t, 128u, 64u) &&
                                 tmem_ok(o_acc, 128u, D);
+          // B = V_j as an MN-major operand: N = D (64-column halves
+          // HALF_BYTES apart), K = 16 keys starting at key 16*kk.  The
+          // item's first product overwrites O (the previous item's epilogue
+          // has read it: its softmax warps wrote P_0 after).  With two
+          // groups keys 64..127 go first, then 0..63 (with P split, once the
+          // whole of P is in; both instantiations then add in one order).
+          auto pv_steps = [&](int k0, int k1, bool first) {
 #pragma unroll
-          for (int kk = 0; kk < C::BN / 16 && in_range; ++kk) {
-            // B = V_j as an MN-major operand: N = D (64-column halves
-            // HALF_BYTES apart), K = 16 keys starting at key 16*kk.  The
-            // item's first product overwrites O (the previous item's
-            // epilogue has read it: its softmax warps wrote P_0 after).
-            const uint64_t bdesc = sdesc_sw128(v_s + kk * 16u * 128u, C::HALF_BYTES, 1024u);
-            tc_mma_ts(o_acc, p_t + kk * 8u, bdesc, idesc_pv, (j >= NG || kk > 0) ? 1u : 0u);
+            for (int kk = k0; kk < k1; ++kk) {
+              if (!in_range) break;
+              const uint64_t bdesc = sdesc_sw128(v_s + kk * 16u * 128u, C::HALF_BYTES, 1024u);
+              tc_mma_ts(o_acc, p_t + kk * 8u, bdesc, idesc_pv,
+                        (j >= NG || !first || kk > k0) ? 1u : 0u);
+            }
+          };
+          if constexpr (NG == 1) {
+            pv_steps(0, C::BN / 16, true);
+          } else if constexpr (!kHalfP) {
+            pv_steps(C::BN / 32, C::BN / 16, true);
+            pv_steps(0, C::BN / 32, false);
+          } else {
+            pv_steps(C::BN / 32, C::BN / 16, true);
+            if (!mbar_wait(bar(C::B_P_FULL + g % C::NS), (g / C::NS) & 1, abort_flag, args.status,
+                           wlim)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            pv_steps(0, C::BN / 32, false);
           }
           tc_commit(bar(C::B_V_EMPTY + sv));
           tc_commit(bar(C::B_PV_DONE + g % C::NS));
@@ -723,6 +754,32 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
           m_new = (mx > m + kRescaleLog2) ? mx : m;  // also moves off -inf
           m_use = (m_new == -INFINITY) ? 0.f : m_new;
           const float2 cc = make_float2(c, c), nm = make_float2(-m_use, -m_use);
+          // With P split, the group's previous P V product is confirmed here
+          // (see below) and O is rescaled now, before P_j V_j can start on
+          // P's second half.
+          if (kHalfP && j >= NG) {
+            const bool w2 = mbar_wait(bar(C::B_PV_GRP + grp), (pvn - 1) & 1, abort_flag,
+                                      args.status, wlim);
+            if (__any_sync(0xffffffffu, !w2)) {
+              ok = false;
+              break;
+            }
+            const float alpha_g = (m_new == m) ? 1.f : ex2_approx(m - m_use);
+            if (__any_sync(0xffffffffu, alpha_g != 1.f)) {
+              tc_fence_after();
+              const uint32_t o_t = tmem + lane_off + C::TMEM_O + grp * D;
+              const bool o_ok = !kDebugChecks || __all_sync(0xffffffffu, tmem_ok(o_t, 32u, D));
+#pragma unroll
+              for (int c0 = 0; c0 < D && o_ok; c0 += 32) {
+                uint32_t ov[32];
+                tmem_ld32(o_t + c0, ov);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha_g);
+                tmem_st32(o_t + c0, ov);
+              }
+            }
+          }
           auto exp_half = [&](const float (&x)[64], uint32_t dst) {
             uint32_t pk[32];
 #pragma unroll
@@ -735,6 +792,11 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
             if (p_ok) tmem_st32(dst, pk);
           };
           exp_half(th, p_t + 32u);
+          if constexpr (kHalfP) {
+            tmem_st_wait();  // (also the rescaled O)
+            tc_fence_before();
+            mbar_arrive(bar(C::B_PH_FULL + sb));
+          }
           load_half(0, th);
           exp_half(th, p_t);
         }
@@ -748,7 +810,7 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
         dsum = dsum * alpha + (aa.x + aa.y);
         m = m_new;
 
-        if constexpr (NG > 1) {
+        if constexpr (NG > 1 && !kHalfP) {
           // A group confirms its previous P V product at every tile, before
           // it signals the next one: PV_GRP(grp) then never runs more than
           // one phase ahead of the phase a wait names (a parity wait is only
@@ -762,13 +824,13 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
             }
           }
         }
-        if (j >= NG && __any_sync(0xffffffffu, alpha != 1.f)) {
+        if (!kHalfP && j >= NG && __any_sync(0xffffffffu, alpha != 1.f)) {
           // o <- alpha * o between the group's previous P V product and
           // P_j V_j (rare: only when a row of this warp moved its reference
-          // maximum).  With one group that product's S buffer barrier is
-          // waited for (its next phase needs this warp's P, so it cannot
-          // run ahead of the wait); with two, the product was confirmed
-          // above.
+          // maximum; with P split this happened before the exponentials).
+          // With one group that product's S buffer barrier is waited for
+          // (its next phase needs this warp's P, so it cannot run ahead of
+          // the wait); with two, the product was confirmed above.
           if constexpr (NG == 1) {
             const bool w2 = mbar_wait(bar(C::B_PV_DONE + (g - 1) % C::NS),
                                       ((g - 1) / C::NS) & 1, abort_flag, args.status, wlim);
