@@ -664,35 +664,63 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
             for (int i = 0; i < 128; ++i) t[i] = (t[i] == -INFINITY) ? -INFINITY : 0.f;
           }
           // Row max over 128 values in 16 independent chains of 3-input maxima.
-          float q[16];
+          auto tile_max = [&]() -> float {
+            float q[16];
   #pragma unroll
-          for (int kq = 0; kq < 16; ++kq) q[kq] = fmax3(t[8 * kq], t[8 * kq + 1], t[8 * kq + 2]);
+            for (int kq = 0; kq < 16; ++kq) q[kq] = fmax3(t[8 * kq], t[8 * kq + 1], t[8 * kq + 2]);
   #pragma unroll
-          for (int kq = 0; kq < 16; ++kq) q[kq] = fmax3(q[kq], t[8 * kq + 3], t[8 * kq + 4]);
+            for (int kq = 0; kq < 16; ++kq) q[kq] = fmax3(q[kq], t[8 * kq + 3], t[8 * kq + 4]);
   #pragma unroll
-          for (int kq = 0; kq < 16; ++kq) q[kq] = fmax3(q[kq], t[8 * kq + 5], t[8 * kq + 6]);
+            for (int kq = 0; kq < 16; ++kq) q[kq] = fmax3(q[kq], t[8 * kq + 5], t[8 * kq + 6]);
   #pragma unroll
-          for (int kq = 0; kq < 16; ++kq) q[kq] = fmaxf(q[kq], t[8 * kq + 7]);
-          const float r0 = fmax3(q[0], q[1], q[2]), r1 = fmax3(q[3], q[4], q[5]);
-          const float r2 = fmax3(q[6], q[7], q[8]), r3 = fmax3(q[9], q[10], q[11]);
-          const float r4 = fmax3(q[12], q[13], q[14]);
-          tmax = fmaxf(fmax3(r0, r1, r2), fmax3(r3, r4, q[15]));
-          const float mx = tmax * c;
-          m_new = (mx > m + kRescaleLog2) ? mx : m;  // also moves off -inf
-          m_use = (m_new == -INFINITY) ? 0.f : m_new;
-          const float2 cc = make_float2(c, c), nm = make_float2(-m_use, -m_use);
+            for (int kq = 0; kq < 16; ++kq) q[kq] = fmaxf(q[kq], t[8 * kq + 7]);
+            const float r0 = fmax3(q[0], q[1], q[2]), r1 = fmax3(q[3], q[4], q[5]);
+            const float r2 = fmax3(q[6], q[7], q[8]), r3 = fmax3(q[9], q[10], q[11]);
+            const float r4 = fmax3(q[12], q[13], q[14]);
+            return fmaxf(fmax3(r0, r1, r2), fmax3(r3, r4, q[15]));
+          };
+          // p = 2^(sigma - mu) for the tile, summed into a[] and stored as P.
+          auto tile_exp = [&](float mu) {
+            const float2 cc = make_float2(c, c), nm = make_float2(-mu, -mu);
   #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            uint32_t pk[32];
+            for (int hh = 0; hh < 2; ++hh) {
+              uint32_t pk[32];
   #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float2 x =
-                  __ffma2_rn(make_float2(t[64 * hh + 2 * i], t[64 * hh + 2 * i + 1]), cc, nm);
-              const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-              a[i & 3] = __fadd2_rn(a[i & 3], p);
-              pk[i] = pack_bf16x2(p.x, p.y);
+              for (int i = 0; i < 32; ++i) {
+                const float2 x =
+                    __ffma2_rn(make_float2(t[64 * hh + 2 * i], t[64 * hh + 2 * i + 1]), cc, nm);
+                const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                a[i & 3] = __fadd2_rn(a[i & 3], p);
+                pk[i] = pack_bf16x2(p.x, p.y);
+              }
+              if (p_ok) tmem_st32(p_t + 32u * hh, pk);
             }
-            if (p_ok) tmem_st32(p_t + 32u * hh, pk);
+          };
+          // Once every row of the warp has a reference, the reference moves
+          // only when the tile's maximum exceeds it by kRescaleLog2: the
+          // weights are computed against the current reference while the
+          // maximum is reduced, and recomputed in the rare tile where a row
+          // moves (all lanes store P, so the warp redoes it together).  (One
+          // item per CTA only: in the persistent instantiation the second
+          // copy of the exponential loop costs more registers than it gains.)
+          if (!PERSIST && __all_sync(0xffffffffu, m != -INFINITY)) {
+            m_use = m;
+            tile_exp(m_use);
+            tmax = tile_max();
+            const float mx = tmax * c;
+            m_new = (mx > m + kRescaleLog2) ? mx : m;
+            if (__any_sync(0xffffffffu, m_new != m)) {
+              m_use = m_new;
+  #pragma unroll
+              for (int kq = 0; kq < 4; ++kq) a[kq] = make_float2(0.f, 0.f);
+              tile_exp(m_use);
+            }
+          } else {
+            tmax = tile_max();
+            const float mx = tmax * c;
+            m_new = (mx > m + kRescaleLog2) ? mx : m;  // also moves off -inf
+            m_use = (m_new == -INFINITY) ? 0.f : m_new;
+            tile_exp(m_use);
           }
         } else {
           // Two softmax groups share the registers of 352 threads, so the
