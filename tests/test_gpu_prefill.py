@@ -102,13 +102,19 @@ def test_config2_full(fa):
     check_lse(np64(lse), L)
 
 
-@pytest.mark.parametrize("D", [64, 128])
-def test_persistent_equals_one_item(fa, D):
+@pytest.mark.parametrize("D,ramp", [(64, False), (128, False), (64, True), (128, True)])
+def test_persistent_equals_one_item(fa, D, ramp):
     """B=4 H=16 N=2048 causal (1024 query tiles, more than the SMs) runs on
     persistent CTAs; each head alone (16 tiles) runs one tile per CTA.  The
-    per-tile arithmetic is the same, so the outputs agree bit for bit."""
-    case = inp.dense(4, 16, 2048, D, seed=60 + D, causal=True)
+    per-tile arithmetic is the same, so the outputs agree bit for bit.  With
+    keys that grow along the sequence (ramp) rows move their reference on
+    many tiles, where the one-item kernel redoes the weights it computed
+    against the old reference."""
+    case = inp.dense(4, 16, 2048, D, seed=60 + D, causal=True, qk_std=3.0 if ramp else 1.0)
     q, k, v = _dense_gpu(case)
+    if ramp:
+        r = (1.0 + 4.0 * torch.arange(2048, dtype=torch.float32, device="cuda") / 2048)
+        k = (k.float() * r.view(1, 1, -1, 1)).to(torch.bfloat16)
     o, lse = fa.fa_fwd(q, k, v, case.scale, True)
     for b in range(4):
         for h in range(16):
