@@ -170,7 +170,9 @@ __device__ __forceinline__ void mbar_wait_unwind(uint32_t bar, uint32_t parity) 
   }
 }
 
-template <int D, bool PERSIST, int NG>
+// SPEC (one group, one item per CTA, no window): weights computed against
+// the current reference while the tile maximum is reduced (see below).
+template <int D, bool PERSIST, int NG, bool SPEC>
 __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
@@ -701,9 +703,10 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
           // weights are computed against the current reference while the
           // maximum is reduced, and recomputed in the rare tile where a row
           // moves (all lanes store P, so the warp redoes it together).  (One
-          // item per CTA only: in the persistent instantiation the second
-          // copy of the exponential loop costs more registers than it gains.)
-          if (!PERSIST && __all_sync(0xffffffffu, m != -INFINITY)) {
+          // item per CTA without a window only: in the persistent and the
+          // window instantiations the second copy of the exponential loop
+          // costs more registers and code than it gains.)
+          if (SPEC && __all_sync(0xffffffffu, m != -INFINITY)) {
             m_use = m;
             tile_exp(m_use);
             tmax = tile_max();
@@ -1145,14 +1148,20 @@ static cudaError_t launch_tc_impl(const TcMaps& maps, const TcFwdArgs& a, int gr
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D, false, NG>,
+    e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D, false, NG, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::SMEM_BYTES));
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D, true, NG>,
+    e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D, true, NG, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::SMEM_BYTES));
     if (e != cudaSuccess) return e;
+    if constexpr (NG == 1) {
+      e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D, false, NG, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(C::SMEM_BYTES));
+      if (e != cudaSuccess) return e;
+    }
     if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_release);
   }
   static std::atomic<int> sm_count[64];  // per device: multiprocessors (0 = not read yet)
@@ -1173,13 +1182,17 @@ static cudaError_t launch_tc_impl(const TcMaps& maps, const TcFwdArgs& a, int gr
                      args.num_items > nsm)
                         ? 1
                         : 0;
+  const dim3 one_item(static_cast<unsigned>(args.num_items));
   if (args.persistent)
-    fa_fwd_tc_kernel<D, true, NG><<<dim3(static_cast<unsigned>(nsm)), C::THREADS, C::SMEM_BYTES,
-                                    stream>>>(maps.q, maps.k, maps.v, maps.o, args);
+    fa_fwd_tc_kernel<D, true, NG, false><<<dim3(static_cast<unsigned>(nsm)), C::THREADS,
+                                           C::SMEM_BYTES, stream>>>(maps.q, maps.k, maps.v,
+                                                                    maps.o, args);
+  else if (NG == 1 && args.window == 0)
+    fa_fwd_tc_kernel<D, false, NG, NG == 1><<<one_item, C::THREADS, C::SMEM_BYTES, stream>>>(
+        maps.q, maps.k, maps.v, maps.o, args);
   else
-    fa_fwd_tc_kernel<D, false, NG><<<dim3(static_cast<unsigned>(args.num_items)), C::THREADS,
-                                     C::SMEM_BYTES, stream>>>(maps.q, maps.k, maps.v, maps.o,
-                                                              args);
+    fa_fwd_tc_kernel<D, false, NG, false><<<one_item, C::THREADS, C::SMEM_BYTES, stream>>>(
+        maps.q, maps.k, maps.v, maps.o, args);
   return cudaGetLastError();
 }
 
