@@ -1043,11 +1043,17 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch) {
             const uint32_t* v8 = ov + c0 + 8 * ch;
+            const float2 ii = make_float2(inv, inv);
+            auto scaled = [&](int e) {  // (packed multiply, the same rounding per element)
+              const float2 pr = __fmul2_rn(
+                  make_float2(__uint_as_float(v8[e]), __uint_as_float(v8[e + 1])), ii);
+              return pack_bf16x2(pr.x, pr.y);
+            };
             uint4 u;
-            u.x = pack_bf16x2(__uint_as_float(v8[0]) * inv, __uint_as_float(v8[1]) * inv);
-            u.y = pack_bf16x2(__uint_as_float(v8[2]) * inv, __uint_as_float(v8[3]) * inv);
-            u.z = pack_bf16x2(__uint_as_float(v8[4]) * inv, __uint_as_float(v8[5]) * inv);
-            u.w = pack_bf16x2(__uint_as_float(v8[6]) * inv, __uint_as_float(v8[7]) * inv);
+            u.x = scaled(0);
+            u.y = scaled(2);
+            u.z = scaled(4);
+            u.w = scaled(6);
             *reinterpret_cast<uint4*>(row + ((ch ^ (r & 7)) << 4)) = u;
           }
         }
