@@ -85,8 +85,11 @@ namespace fa {
 // more than this (base-2 units).
 constexpr float kRescaleLog2 = 32.f;
 
-// Sequences of at most this many 128-row query tiles run on persistent CTAs.
-constexpr int kPersistentMaxTiles = 32;
+// Sequences of at most this many 128-row query tiles run on persistent CTAs
+// (measured crossovers: at D = 128 the one-item kernel, which computes weights
+// before the maximum, wins from 32 tiles on; at D = 64, where its groups
+// start P V on half of P, from 16 tiles on).
+constexpr int persistent_max_tiles(int D) { return D == 128 ? 28 : 8; }
 
 // Softmax warpgroups per CTA at D = 64 (at D = 128 tensor memory holds one O).
 constexpr int kSoftmaxGroups64 = 2;
@@ -1184,7 +1187,7 @@ static cudaError_t launch_tc_impl(const TcMaps& maps, const TcFwdArgs& a, int gr
   // work; one CTA per item otherwise (the hardware scheduler balances the
   // long causal ranges, the head-grouped order keeps K/V in L2, and most
   // items of a packed batch are empty, which a one-item CTA skips at once).
-  args.persistent = (a.cu_seqlens == nullptr && a.num_mblocks <= kPersistentMaxTiles &&
+  args.persistent = (a.cu_seqlens == nullptr && a.num_mblocks <= persistent_max_tiles(D) &&
                      args.num_items > nsm)
                         ? 1
                         : 0;
