@@ -1,7 +1,9 @@
 // Exact attention forward on the sm_103a tensor cores (bf16 in, fp32 state).
 //
-// One CTA owns one 128-row query tile of one (sequence, head) and folds the
-// key/value tiles of that sequence into the per-row state (m, d, o) of
+// A work item is one 128-row query tile of one (sequence, head); a CTA takes
+// one item (or, on persistent CTAs for short dense sequences, a sequence of
+// them) and folds the key/value tiles of that sequence into the per-row
+// state (m, d, o) of
 // "Learning FlashAttention the Hard Way - Part 1", sections "The State" and
 // "The Merge, and the Twist", in the base-2 coordinates of "Alternative Twist:
 // Base 2" (sigma = s * scale * log2 e, every exponential an ex2).  Each KV tile
@@ -29,7 +31,8 @@
 // from the tile's largest weight (that weight is recomputed exactly as the
 // tile loop computes it); the log-sum-exp uses d itself.
 //
-// Roles (224 threads):
+// Roles at D = 128 (224 threads; at D = 64 two softmax groups of four warps
+// split the key tiles between them, see TcCfg and the softmax section):
 //   warp 0      TMA producer: Q once, then K and V tiles into two rings of
 //               stages, in the order the MMA issuers consume them
 //               (K_0 .. K_{KS-1}, then V_j, K_{j+KS} for each j).
@@ -52,9 +55,11 @@
 //               kRescaleLog2, computes p = 2^(s c - m) with one packed fused
 //               multiply-add per pair of columns, rounds P to bf16 over the
 //               second half of the tile's S buffer (those scores are in
-//               registers by then), sums p with packed adds (four chains),
-//               and, on the
-//               rare tiles where a row of the warp moved its reference,
+//               registers by then), sums p with packed adds (four chains).
+//               (Dense one-item launches without a window compute the
+//               weights against the current reference while the maximum is
+//               reduced, and redo them in the rare tile where a row moves.)
+//               On the rare tiles where a row of the warp moved its reference,
 //               waits for P_{j-1} V_{j-1} and rescales its O row in TMEM by
 //               alpha_j = 2^(m_old - m_new) (the rescale half of the merge);
 //               then it signals P_j.
@@ -63,8 +68,8 @@
 //               D = 128: staged in Q's buffer, one TMA store per warp and
 //               64-column half).
 //
-// Shared memory (1024-byte aligned): Q tile, KS K tiles, VS V tiles, the
-// mbarriers.  A 128 x D bf16 tile is stored as D/64 column halves of
+// Shared memory (1024-byte aligned): two Q tiles (consecutive items), KS K
+// tiles, VS V tiles, the mbarriers.  A 128 x D bf16 tile is stored as D/64 column halves of
 // 128 rows x 128 bytes, 128-byte swizzled (the TMA box layout and the
 // canonical K-major / MN-major tcgen05 operand layouts).
 // Tensor memory (512 columns): S buffers at [128 b, 128 b + 128) for b < 3
