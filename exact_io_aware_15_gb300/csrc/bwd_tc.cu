@@ -139,14 +139,17 @@ __device__ __forceinline__ void store_row(uint32_t tmem_row, void* dst, size_t r
 // masking) first: the tensors the tiles stream (Q and dO, or K and V: 4
 // heads x 8 MB at N = 16384, D = 128) stay in L2 while the group runs.
 // Returns the head and the tile's rank by weight (0 = heaviest).
+// (32-bit unsigned divisions: the grid has fewer than 2^31 CTAs, and a 64-bit
+// division costs several hundred cycles.)
 __device__ __forceinline__ void tile_of(int nt, int BH, int& bh, int& rank) {
-  const long long lin = blockIdx.x;
-  const long long per_group = 4LL * nt;
-  const int g = static_cast<int>(lin / per_group);
-  const int gsize = min(4, BH - g * 4);
-  const int rr = static_cast<int>(lin - g * per_group);
-  rank = rr / gsize;
-  bh = g * 4 + rr % gsize;
+  const unsigned lin = blockIdx.x;
+  const unsigned per_group = 4u * static_cast<unsigned>(nt);
+  const unsigned g = lin / per_group;
+  const unsigned gsize = static_cast<unsigned>(min(4, BH - static_cast<int>(g) * 4));
+  const unsigned rr = lin - g * per_group;
+  const unsigned q = rr / gsize;
+  rank = static_cast<int>(q);
+  bh = static_cast<int>(g * 4u + (rr - q * gsize));
 }
 
 // Where one (sequence, head) of the problem lives.  Dense: [B, H, N, D]
