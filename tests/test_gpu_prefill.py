@@ -148,9 +148,10 @@ def test_offset_invariance(fa, c):
     check_lse(np64(lse) - shift, L, tol=2e-3)
 
 
-def test_scale_zero_prefix_means(fa):
+@pytest.mark.parametrize("D", [64, 128])
+def test_scale_zero_prefix_means(fa, D):
     """Identical scores: causal rows are prefix means of V, LSE = ln(i+1)."""
-    case = inp.dense(1, 2, 260, 64, seed=5, causal=True)
+    case = inp.dense(1, 2, 260, D, seed=5, causal=True)
     o, lse = fa.fa_fwd_ex(*_dense_gpu(case), 0.0, True, o_dtype=torch.float32)
     v = np64(case.v)
     ref = np.cumsum(v, axis=2) / np.arange(1, 261)[None, None, :, None]
@@ -273,6 +274,37 @@ def test_varlen_small(fa, D):
             od, ld = fa.fa_fwd(qs, ks, vs, case.scale, True)
             assert torch.equal(od[0].permute(1, 0, 2), o[a:b])
             assert torch.equal(ld[0], lse[:, a:b])
+    assert fa.fa_check_device_status() == fa.FA_OK
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_varlen_moving_reference(fa, D):
+    """Packed sequences whose keys grow along each sequence (scores with a
+    spread of many units), so rows move their reference on many tiles: the
+    one-item kernel redoes the weights of those tiles.  Every row against
+    the oracle, and each sequence alone through the dense entry point bit
+    for bit."""
+    lens = [300, 700, 129, 1000, 1]
+    case = inp.varlen(lens, H=2, D=D, seed=70 + D, causal=True)
+    cuh = case.cu_seqlens.tolist()
+    ramp = torch.ones(case.k.shape[0])
+    for s_ in range(len(lens)):
+        a, b = cuh[s_], cuh[s_ + 1]
+        ramp[a:b] = 1.0 + 4.0 * torch.arange(b - a, dtype=torch.float32) / max(1, b - a)
+    qh = (case.q.float() * 3.0).to(torch.bfloat16)
+    kh = (case.k.float() * 3.0 * ramp.view(-1, 1, 1)).to(torch.bfloat16)
+    q, k, v = qh.cuda(), kh.cuda(), case.v.cuda()
+    cu = case.cu_seqlens.cuda()
+    o, lse = fa.fa_fwd_varlen(q, k, v, cu, case.max_seqlen, case.scale, True)
+    ref = ora.varlen_ref(qh, kh, case.v, case.cu_seqlens, case.scale, True)
+    for s_, (O, L) in ref.items():
+        a, b = cuh[s_], cuh[s_ + 1]
+        check_o_bf16(np64(o[a:b]), O, f"seq {s_}")
+        check_lse(np64(lse[:, a:b]), L)
+        qs, ks, vs = (t[a:b].permute(1, 0, 2).unsqueeze(0).contiguous() for t in (q, k, v))
+        od, ld = fa.fa_fwd(qs, ks, vs, case.scale, True)
+        assert torch.equal(od[0].permute(1, 0, 2), o[a:b])
+        assert torch.equal(ld[0], lse[:, a:b])
     assert fa.fa_check_device_status() == fa.FA_OK
 
 
