@@ -379,7 +379,10 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
     return FA_ERR_INVALID_ARG;
   const long long SH = static_cast<long long>(num_seqs) * H;
   const long long mblocks = (static_cast<long long>(max_seqlen) + 127) / 128;
-  if (SH > 0x7fffffffLL || SH * mblocks > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  // (the launch's grid: H x (total_tokens / 128 + num_seqs) query-tile slots)
+  const long long slots = static_cast<long long>(total_tokens) / 128 + num_seqs;
+  if (SH > 0x7fffffffLL || SH * mblocks > 0x7fffffffLL || slots * H > 0x7fffffffLL)
+    return FA_ERR_INVALID_ARG;
   unsigned int* status = nullptr;
   int rc = current_device(&status);
   if (rc != FA_OK) return rc;
@@ -403,6 +406,7 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
   a.window = 0;
   a.scale_log2 = scale_log2(scale);
   a.cu_seqlens = cu_seqlens;
+  a.num_seqs = num_seqs;
   a.total_tokens = total_tokens;
   a.max_seqlen = max_seqlen;
   a.o = o;

@@ -16,6 +16,7 @@ struct TcFwdArgs {
   int window;        // > 0: causal sliding window, query i sees keys i-window+1 .. i
   float scale_log2;  // softmax scale * log2(e)
   const int* cu_seqlens;  // varlen token offsets [num_seqs + 1]; NULL when dense
+  int num_seqs;           // varlen: sequences
   int total_tokens;       // varlen: T
   int max_seqlen;         // varlen: bound checked against every length
   void* o;

@@ -161,6 +161,60 @@ struct TcCfg {
   static constexpr int SOFTMAX_THREADS = 128;  // one group
 };
 
+// The item of CTA `lin` of a packed-sequence launch (one item per CTA).
+// Sequence s owns the query-tile slots [st(s), st(s+1)) with st(s) =
+// cu[s] / 128 + s, at least its number of query tiles, so the grid (H CTAs
+// per slot) holds every tile of every sequence and one or two empty slots
+// per sequence.  Inside a sequence the order is the dense one: groups of four
+// heads, heaviest tile first.  n_kv = 0 marks an empty slot or offsets that
+// fail the bounds check (reported once, by thread 0).
+struct VarlenItem {
+  int mb, bh, h, L, tok0, n_kv;
+};
+__device__ __forceinline__ VarlenItem varlen_item(const TcFwdArgs& args, unsigned lin) {
+  constexpr int BM = 128;
+  VarlenItem it{0, 0, 0, 0, 0, 0};
+  const unsigned Hu = static_cast<unsigned>(args.H);
+  int lo = 0, hi = args.num_seqs;  // the last sequence with st(s) * H <= lin
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    const long long st = __ldg(args.cu_seqlens + mid) / BM + mid;
+    if (st * static_cast<long long>(Hu) <= static_cast<long long>(lin))
+      lo = mid;
+    else
+      hi = mid;
+  }
+  const int seq = lo;
+  const int a = __ldg(args.cu_seqlens + seq);
+  const int e = __ldg(args.cu_seqlens + seq + 1);
+  it.bh = seq * args.H;
+  if (a < 0 || e < a || e > args.total_tokens || e - a > args.max_seqlen) {
+    if (threadIdx.x == 0) atomicOr(args.status, kStatusBounds);
+    return it;
+  }
+  const unsigned st0 = static_cast<unsigned>(a / BM + seq);
+  const unsigned slots = static_cast<unsigned>(e / BM + seq + 1) - st0;
+  if (lin < st0 * Hu || lin - st0 * Hu >= slots * Hu) return it;  // (inconsistent offsets)
+  const unsigned local = lin - st0 * Hu;
+  const unsigned g = local / (4u * slots);
+  const unsigned gsize = static_cast<unsigned>(min(4, args.H - static_cast<int>(g) * 4));
+  const unsigned rr = local - g * 4u * slots;
+  const unsigned i = rr / gsize;  // rank by weight, 0 = heaviest
+  const int h = static_cast<int>(g * 4u + (rr - i * gsize));
+  const int L = e - a;
+  const int tiles = (L + BM - 1) / BM;
+  it.h = h;
+  it.bh = seq * args.H + h;
+  it.L = L;
+  it.tok0 = a;
+  if (static_cast<int>(i) >= tiles) return it;  // an empty slot
+  it.mb = tiles - 1 - static_cast<int>(i);
+  int n_kv = tiles;  // 128-key tiles (BN = BM)
+  if (args.causal) n_kv = min(n_kv, it.mb + 1);
+  it.n_kv = n_kv;
+  return it;
+}
+
 // max(a, b, c) in one instruction.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
@@ -180,7 +234,8 @@ __device__ __forceinline__ void mbar_wait_unwind(uint32_t bar, uint32_t parity) 
 
 // SPEC (one group, one item per CTA, no window): weights computed against
 // the current reference while the tile maximum is reduced (see below).
-template <int D, bool PERSIST, int NG, bool SPEC>
+// VL: packed sequences (cu_seqlens), one item per CTA.
+template <int D, bool PERSIST, int NG, bool SPEC, bool VL>
 __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
@@ -195,7 +250,7 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
 
   const int nmb = args.num_mblocks;
   const int BHt = args.num_items / nmb;  // (sequence, head) pairs
-  const bool varlen = args.cu_seqlens != nullptr;
+  constexpr bool varlen = VL;
 
   // ---- work items ----
   // An item is one 128-row query tile of one (sequence, head).  With one CTA
@@ -229,6 +284,17 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
       const unsigned hq = idx / static_cast<unsigned>(BHt);
       mb = nmb - 1 - static_cast<int>(hq);
       bh = static_cast<int>(idx - hq * static_cast<unsigned>(BHt));
+    } else if constexpr (VL) {
+      if (k > 0) return false;
+      const VarlenItem v = varlen_item(args, blockIdx.x);
+      it.mb = v.mb;
+      it.bh = v.bh;
+      it.h = v.h;
+      it.L = v.L;
+      it.tok0 = v.tok0;
+      it.n_kv = v.n_kv;
+      it.j0 = 0;
+      return true;
     } else {
       if (k > 0) return false;
       const unsigned lin = blockIdx.x;
@@ -1162,16 +1228,20 @@ static cudaError_t launch_tc_impl(const TcMaps& maps, const TcFwdArgs& a, int gr
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D, false, NG, false>,
+    e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D, false, NG, false, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::SMEM_BYTES));
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D, true, NG, false>,
+    e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D, true, NG, false, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(C::SMEM_BYTES));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D, false, NG, NG == 1, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::SMEM_BYTES));
     if (e != cudaSuccess) return e;
     if constexpr (NG == 1) {
-      e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D, false, NG, true>,
+      e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D, false, NG, true, false>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(C::SMEM_BYTES));
       if (e != cudaSuccess) return e;
@@ -1186,7 +1256,10 @@ static cudaError_t launch_tc_impl(const TcMaps& maps, const TcFwdArgs& a, int gr
     if (dev >= 0 && dev < 64) sm_count[dev].store(nsm, std::memory_order_release);
   }
   TcFwdArgs args = a;
-  args.num_items = grid_x * a.num_mblocks;
+  // Packed sequences: H slots per query-tile slot (see the kernel's item
+  // mapping); dense: every (sequence, head) pair's query tiles.
+  args.num_items = a.cu_seqlens != nullptr ? a.H * (a.total_tokens / 128 + a.num_seqs)
+                                           : grid_x * a.num_mblocks;
   // Persistent CTAs (one per SM) for short dense sequences, where the fixed
   // cost of a CTA (setup, first product, epilogue) is a large share of its
   // work; one CTA per item otherwise (the hardware scheduler balances the
@@ -1198,15 +1271,21 @@ static cudaError_t launch_tc_impl(const TcMaps& maps, const TcFwdArgs& a, int gr
                         : 0;
   const dim3 one_item(static_cast<unsigned>(args.num_items));
   if (args.persistent)
-    fa_fwd_tc_kernel<D, true, NG, false><<<dim3(static_cast<unsigned>(nsm)), C::THREADS,
-                                           C::SMEM_BYTES, stream>>>(maps.q, maps.k, maps.v,
-                                                                    maps.o, args);
+    fa_fwd_tc_kernel<D, true, NG, false, false><<<dim3(static_cast<unsigned>(nsm)), C::THREADS,
+                                                  C::SMEM_BYTES, stream>>>(maps.q, maps.k,
+                                                                           maps.v, maps.o, args);
+  else if (a.cu_seqlens != nullptr)
+    fa_fwd_tc_kernel<D, false, NG, NG == 1, true><<<one_item, C::THREADS, C::SMEM_BYTES,
+                                                    stream>>>(maps.q, maps.k, maps.v, maps.o,
+                                                              args);
   else if (NG == 1 && args.window == 0)
-    fa_fwd_tc_kernel<D, false, NG, NG == 1><<<one_item, C::THREADS, C::SMEM_BYTES, stream>>>(
-        maps.q, maps.k, maps.v, maps.o, args);
+    fa_fwd_tc_kernel<D, false, NG, NG == 1, false><<<one_item, C::THREADS, C::SMEM_BYTES,
+                                                     stream>>>(maps.q, maps.k, maps.v, maps.o,
+                                                               args);
   else
-    fa_fwd_tc_kernel<D, false, NG, false><<<one_item, C::THREADS, C::SMEM_BYTES, stream>>>(
-        maps.q, maps.k, maps.v, maps.o, args);
+    fa_fwd_tc_kernel<D, false, NG, false, false><<<one_item, C::THREADS, C::SMEM_BYTES,
+                                                   stream>>>(maps.q, maps.k, maps.v, maps.o,
+                                                             args);
   return cudaGetLastError();
 }
 
