@@ -152,6 +152,43 @@ __device__ __forceinline__ void tile_of(int nt, int BH, int& bh, int& rank) {
   bh = static_cast<int>(g * 4u + (rr - q * gsize));
 }
 
+// Packed sequences: sequence s owns the tile slots [st(s), st(s+1)) with
+// st(s) = cu[s] / 128 + s, at least its number of 128-row tiles, so the grid
+// (H CTAs per slot) holds every tile of every sequence and one or two empty
+// slots per sequence; inside a sequence the order is tile_of's.  Returns
+// the (sequence, head) pair and the tile's rank by weight; a rank past the
+// sequence's tiles marks an empty slot.  Offsets that fail the bounds check
+// leave the CTA to seq_of's check.
+__device__ __forceinline__ void slot_of(const BwdArgs& a, int& bh, int& rank) {
+  constexpr int BM = 128;
+  const unsigned Hu = static_cast<unsigned>(a.H);
+  const unsigned lin = blockIdx.x;
+  int lo = 0, hi = a.BH / a.H;  // the last sequence with st(s) * H <= lin
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    const long long st = __ldg(a.cu_seqlens + mid) / BM + mid;
+    if (st * static_cast<long long>(Hu) <= static_cast<long long>(lin))
+      lo = mid;
+    else
+      hi = mid;
+  }
+  const int seq = lo;
+  const int b0 = __ldg(a.cu_seqlens + seq), b1 = __ldg(a.cu_seqlens + seq + 1);
+  bh = seq * a.H;
+  rank = 0x7fffffff;
+  if (b0 < 0 || b1 < b0) return;  // seq_of reports it
+  const unsigned st0 = static_cast<unsigned>(b0 / BM + seq);
+  const unsigned slots = static_cast<unsigned>(b1 / BM + seq + 1) - st0;
+  if (lin < st0 * Hu || lin - st0 * Hu >= slots * Hu) return;
+  const unsigned local = lin - st0 * Hu;
+  const unsigned g = local / (4u * slots);
+  const unsigned gsize = static_cast<unsigned>(min(4, a.H - static_cast<int>(g) * 4));
+  const unsigned rr = local - g * 4u * slots;
+  const unsigned q = rr / gsize;
+  rank = static_cast<int>(q);
+  bh = seq * a.H + static_cast<int>(g * 4u + (rr - q * gsize));
+}
+
 // Where one (sequence, head) of the problem lives.  Dense: [B, H, N, D]
 // tensors, LSE / Delta [B, H, N].  Varlen: packed [T, H, D] tensors,
 // LSE / Delta [H, T], sequence s owning tokens [cu[s], cu[s+1]).
@@ -253,9 +290,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int nt = args.num_tiles;
-  int bh, n;  // key tile n sees query tiles n..ntl-1 under causal masking
-  tile_of(nt, args.BH, bh, n);
   constexpr bool VAR = MODE == kVarlen, WIN = MODE == kWindow;
+  int bh, n;  // key tile n sees query tiles n..ntl-1 under causal masking
+  if constexpr (VAR)
+    slot_of(args, bh, n);
+  else
+    tile_of(nt, args.BH, bh, n);
   const SeqView sv = seq_of<VAR>(args, bh);
   if (!sv.ok) {
     if (threadIdx.x == 0) atomicOr(args.status, kStatusBounds);
@@ -533,16 +573,22 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int nt = args.num_tiles;
-  int bh, rank;  // query tile m sees key tiles 0..m under causal masking
-  tile_of(nt, args.BH, bh, rank);
-  const int m = nt - 1 - rank;
   constexpr bool VAR = MODE == kVarlen, WIN = MODE == kWindow;
+  int bh, rank;  // query tile m sees key tiles 0..m under causal masking
+  if constexpr (VAR)
+    slot_of(args, bh, rank);
+  else
+    tile_of(nt, args.BH, bh, rank);
   const SeqView sv = seq_of<VAR>(args, bh);
   if (!sv.ok) {
     if (threadIdx.x == 0) atomicOr(args.status, kStatusBounds);
     return;
   }
   const int ntl = (sv.L + kBM - 1) / kBM;  // tiles of this sequence
+  // heaviest first: the last query tile of the sequence (of the longest one
+  // for dense tensors, where every sequence has nt tiles)
+  if (rank >= (VAR ? ntl : nt)) return;
+  const int m = (VAR ? ntl : nt) - 1 - rank;
   if (m >= ntl) return;
   // key tiles j0 .. j0 + count - 1: under the window, query rows
   // m*128 .. m*128+127 see no key below m*128 - window + 1
@@ -819,7 +865,10 @@ cudaError_t launch_impl(const BwdMaps& m, const BwdArgs& a, cudaStream_t stream)
   fa_bwd_delta_kernel<D><<<static_cast<unsigned>((a.rows + 7) / 8), 256, 0, stream>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const unsigned blocks = static_cast<unsigned>(static_cast<long long>(a.BH) * a.num_tiles);
+  const unsigned blocks =
+      MODE == kVarlen
+          ? static_cast<unsigned>(a.H * (a.total_tokens / 128 + a.BH / a.H))
+          : static_cast<unsigned>(static_cast<long long>(a.BH) * a.num_tiles);
   fa_bwd_dkdv_kernel<D, MODE>
       <<<blocks, kThreads, DkdvCfg<D>::SMEM_BYTES, stream>>>(m.q, m.k, m.v, m.dout, a);
   e = cudaGetLastError();

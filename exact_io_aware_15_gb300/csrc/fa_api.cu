@@ -284,7 +284,10 @@ int bwd_varlen(const void* q, const void* k, const void* v, const void* o, const
     return FA_ERR_INVALID_ARG;
   const long long BH = static_cast<long long>(num_seqs) * H;
   const long long tiles = (static_cast<long long>(max_seqlen) + 127) / 128;
-  if (max_seqlen < 1 || BH * tiles > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  // (the tile kernels' grid: H x (total_tokens / 128 + num_seqs) tile slots)
+  const long long slots = static_cast<long long>(total_tokens) / 128 + num_seqs;
+  if (max_seqlen < 1 || BH * tiles > 0x7fffffffLL || slots * H > 0x7fffffffLL)
+    return FA_ERR_INVALID_ARG;
   unsigned int* status = nullptr;
   int rc = current_device(&status);
   if (rc != FA_OK) return rc;
