@@ -251,6 +251,9 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
   const int nmb = args.num_mblocks;
   const int BHt = args.num_items / nmb;  // (sequence, head) pairs
   constexpr bool varlen = VL;
+  // The sliding window: none in the weights-before-maximum and the packed
+  // instantiations (their launches have no window), so its code folds away.
+  const int window = (SPEC || VL) ? 0 : args.window;
 
   // ---- work items ----
   // An item is one 128-row query tile of one (sequence, head).  With one CTA
@@ -331,8 +334,8 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
     // With a sliding window the tile's rows see no key below
     // mb*BM - window + 1, so the KV tiles start at j0 (all later tile indices
     // j run from 0 and stand for KV tile j0 + j).
-    if (args.window > 0) {
-      const int lo = mb * C::BM - args.window + 1;
+    if (window > 0) {
+      const int lo = mb * C::BM - window + 1;
       it.j0 = lo > 0 ? lo / C::BN : 0;
     }
     it.n_kv = n_kv - it.j0;
@@ -696,7 +699,7 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
         tc_fence_after();
 
         const int kbase = (j0 + j) * C::BN;
-        const bool win_edge = args.window > 0 && kbase < mb * C::BM + C::BM - args.window;
+        const bool win_edge = window > 0 && kbase < mb * C::BM + C::BM - window;
         const bool masked = (args.causal && j0 + j == mb) || kbase + C::BN > L || win_edge;
         float tmax, m_new, m_use;
         // p = 2^(sigma - m_use), rounded to bf16 over the second half of S's
@@ -724,8 +727,8 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
           if (masked) {
             int lim = L - kbase;  // keys [lo, lim) of the tile are visible
             if (args.causal) lim = min(lim, qpos - kbase + 1);
-            if (args.window > 0) {
-              const int lo = qpos - args.window + 1 - kbase;
+            if (window > 0) {
+              const int lo = qpos - window + 1 - kbase;
   #pragma unroll
               for (int i = 0; i < 128; ++i)
                 if (i >= lim || i < lo) t[i] = -INFINITY;
@@ -811,7 +814,7 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
           if (masked) {
             lim = L - kbase;
             if (args.causal) lim = min(lim, qpos - kbase + 1);
-            if (args.window > 0) lo = qpos - args.window + 1 - kbase;
+            if (window > 0) lo = qpos - window + 1 - kbase;
           }
           auto load_half = [&](int hh, float (&x)[64]) {
             uint32_t raw[64];
