@@ -121,15 +121,19 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
  *                [cu_seqlens[s], cu_seqlens[s+1])
  *   cu_seqlens : int32 [num_seqs + 1] DEVICE array, cu_seqlens[0] = 0,
  *                non-decreasing, cu_seqlens[num_seqs] = total_tokens
- *   max_seqlen : >= every sequence length (sizes the launch grid)
+ *   max_seqlen : >= every sequence length (checked against each length)
  *   o          : bf16 [total_tokens, H, D]  (written)
  *   lse        : f32  [H, total_tokens]     (written)
  * Positions restart at 0 in every sequence (causal = keys j <= i of the same
  * sequence).  Tiles never mix sequences: rows beyond a sequence's end are
- * masked with the identity and not stored.  The device checks the
- * cu_seqlens it reads against total_tokens and max_seqlen and reports
+ * masked with the identity and not stored.  The launch grid is
+ * H * (total_tokens / 128 + num_seqs) CTAs (sequence s owns the 128-row tile
+ * slots from cu_seqlens[s] / 128 + s on); FA_ERR_INVALID_ARG if that count or
+ * num_seqs * H * ceil(max_seqlen / 128) exceeds 2^31 - 1.  The device checks
+ * the cu_seqlens it reads against total_tokens and max_seqlen and reports
  * FA_ERR_DEVICE_BOUNDS (through fa_check_device_status) instead of reading
- * out of range.
+ * out of range; offsets that are in range but inconsistent with
+ * total_tokens (cu_seqlens[num_seqs] != total_tokens) leave rows unwritten.
  */
 int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
                   const int* cu_seqlens, int num_seqs, int total_tokens,
@@ -182,9 +186,11 @@ int fa_bwd_window(const void* q, const void* k, const void* v, const void* o,
  *   dq, dk, dv       : bf16 [total_tokens, H, D] (written)
  *   workspace        : f32, fa_bwd_workspace_bytes(1, H, total_tokens) bytes
  *   cu_seqlens       : int32 [num_seqs + 1] DEVICE array; max_seqlen >= every
- *                      length (sizes the grid).  Offsets that fail the device's
- *                      bounds check are reported as FA_ERR_DEVICE_BOUNDS.
- * Positions restart at 0 in every sequence; tiles never mix sequences.
+ *                      length.  Offsets that fail the device's bounds check
+ *                      are reported as FA_ERR_DEVICE_BOUNDS.
+ * Positions restart at 0 in every sequence; tiles never mix sequences.  The
+ * tile kernels' grids are H * (total_tokens / 128 + num_seqs) CTAs, as in
+ * fa_fwd_varlen (FA_ERR_INVALID_ARG past 2^31 - 1).
  */
 int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
                   const void* dout, const float* lse, void* dq, void* dk, void* dv,
