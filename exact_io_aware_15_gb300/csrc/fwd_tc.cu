@@ -234,8 +234,9 @@ __device__ __forceinline__ void mbar_wait_unwind(uint32_t bar, uint32_t parity) 
 
 // SPEC (one group, one item per CTA, no window): weights computed against
 // the current reference while the tile maximum is reduced (see below).
-// VL: packed sequences (cu_seqlens), one item per CTA.
-template <int D, bool PERSIST, int NG, bool SPEC, bool VL>
+// VL: packed sequences (cu_seqlens), one item per CTA.  WIN: the launch may
+// have a sliding window (without it the window code folds away).
+template <int D, bool PERSIST, int NG, bool SPEC, bool VL, bool WIN>
 __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
@@ -251,9 +252,7 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
   const int nmb = args.num_mblocks;
   const int BHt = args.num_items / nmb;  // (sequence, head) pairs
   constexpr bool varlen = VL;
-  // The sliding window: none in the weights-before-maximum and the packed
-  // instantiations (their launches have no window), so its code folds away.
-  const int window = (SPEC || VL) ? 0 : args.window;
+  const int window = WIN ? args.window : 0;
 
   // ---- work items ----
   // An item is one 128-row query tile of one (sequence, head).  With one CTA
@@ -1231,21 +1230,13 @@ static cudaError_t launch_tc_impl(const TcMaps& maps, const TcFwdArgs& a, int gr
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D, false, NG, false, false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(C::SMEM_BYTES));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D, true, NG, false, false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(C::SMEM_BYTES));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D, false, NG, NG == 1, true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(C::SMEM_BYTES));
-    if (e != cudaSuccess) return e;
-    if constexpr (NG == 1) {
-      e = cudaFuncSetAttribute(fa_fwd_tc_kernel<D, false, NG, true, false>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+    // every instantiation launch_tc_impl may launch (see the choice below)
+    for (const void* f : {reinterpret_cast<const void*>(fa_fwd_tc_kernel<D, true, NG, false, false, true>),
+                          reinterpret_cast<const void*>(fa_fwd_tc_kernel<D, true, NG, false, false, false>),
+                          reinterpret_cast<const void*>(fa_fwd_tc_kernel<D, false, NG, NG == 1, true, false>),
+                          reinterpret_cast<const void*>(fa_fwd_tc_kernel<D, false, NG, NG == 1, false, false>),
+                          reinterpret_cast<const void*>(fa_fwd_tc_kernel<D, false, NG, false, false, true>)}) {
+      e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(C::SMEM_BYTES));
       if (e != cudaSuccess) return e;
     }
@@ -1273,22 +1264,23 @@ static cudaError_t launch_tc_impl(const TcMaps& maps, const TcFwdArgs& a, int gr
                         ? 1
                         : 0;
   const dim3 one_item(static_cast<unsigned>(args.num_items));
-  if (args.persistent)
-    fa_fwd_tc_kernel<D, true, NG, false, false><<<dim3(static_cast<unsigned>(nsm)), C::THREADS,
-                                                  C::SMEM_BYTES, stream>>>(maps.q, maps.k,
-                                                                           maps.v, maps.o, args);
-  else if (a.cu_seqlens != nullptr)
-    fa_fwd_tc_kernel<D, false, NG, NG == 1, true><<<one_item, C::THREADS, C::SMEM_BYTES,
-                                                    stream>>>(maps.q, maps.k, maps.v, maps.o,
-                                                              args);
-  else if (NG == 1 && args.window == 0)
-    fa_fwd_tc_kernel<D, false, NG, NG == 1, false><<<one_item, C::THREADS, C::SMEM_BYTES,
-                                                     stream>>>(maps.q, maps.k, maps.v, maps.o,
-                                                               args);
+  const dim3 per_sm(static_cast<unsigned>(nsm));
+  const unsigned T = C::THREADS, SM = C::SMEM_BYTES;
+  if (args.persistent && args.window > 0)
+    fa_fwd_tc_kernel<D, true, NG, false, false, true><<<per_sm, T, SM, stream>>>(
+        maps.q, maps.k, maps.v, maps.o, args);
+  else if (args.persistent)
+    fa_fwd_tc_kernel<D, true, NG, false, false, false><<<per_sm, T, SM, stream>>>(
+        maps.q, maps.k, maps.v, maps.o, args);
+  else if (a.cu_seqlens != nullptr)  // (packed launches have no window)
+    fa_fwd_tc_kernel<D, false, NG, NG == 1, true, false><<<one_item, T, SM, stream>>>(
+        maps.q, maps.k, maps.v, maps.o, args);
+  else if (args.window == 0)
+    fa_fwd_tc_kernel<D, false, NG, NG == 1, false, false><<<one_item, T, SM, stream>>>(
+        maps.q, maps.k, maps.v, maps.o, args);
   else
-    fa_fwd_tc_kernel<D, false, NG, false, false><<<one_item, C::THREADS, C::SMEM_BYTES,
-                                                   stream>>>(maps.q, maps.k, maps.v, maps.o,
-                                                             args);
+    fa_fwd_tc_kernel<D, false, NG, false, false, true><<<one_item, T, SM, stream>>>(
+        maps.q, maps.k, maps.v, maps.o, args);
   return cudaGetLastError();
 }
 
