@@ -31,8 +31,9 @@
 // from the tile's largest weight (that weight is recomputed exactly as the
 // tile loop computes it); the log-sum-exp uses d itself.
 //
-// Roles at D = 128 (224 threads; at D = 64 two softmax groups of four warps
-// split the key tiles between them, see TcCfg and the softmax section):
+// Roles at D = 128 (224 threads; at D = 64, 384 threads: two softmax groups
+// of four warps split the key tiles between them, and each group has its own
+// P V issuing thread, see TcCfg and the softmax section):
 //   warp 0      TMA producer: Q once, then K and V tiles into two rings of
 //               stages, in the order the MMA issuers consume them
 //               (K_0 .. K_{KS-1}, then V_j, K_{j+KS} for each j).
@@ -74,7 +75,8 @@
 // canonical K-major / MN-major tcgen05 operand layouts).
 // Tensor memory (512 columns): S buffers at [128 b, 128 b + 128) for b < 3
 // (P_j, bf16 pairs, over columns [64, 128) of its buffer) and O at
-// [384, 384 + D).
+// [384, 384 + D); at D = 64 two S buffers at [0, 256), two P buffers at
+// [256, 384) and the two groups' O at [384, 512).
 
 #include <cuda.h>
 #include <atomic>
@@ -103,8 +105,10 @@ constexpr int kSoftmaxGroups64 = 2;
 // tiles j with j % 2 == g into its own state and O accumulator, and the
 // epilogue merges the two states (split-K inside the CTA, "Associativity is
 // All You Need"): each scheduler then runs two softmax warps on different
-// tiles.  Three S buffers and two O accumulators fit tensor memory only at
-// D = 64.
+// tiles.  At D = 64 tensor memory then holds two S buffers, two separate P
+// buffers and the two O accumulators: a group frees its S buffer for the
+// product Q K_{j+2}^T as soon as it has read the scores, instead of when
+// P_j V_j has finished.
 template <int D, int NG = 1>
 struct TcCfg {
   static constexpr int BM = 128;
@@ -113,8 +117,12 @@ struct TcCfg {
   static constexpr uint32_t HALF_BYTES = 128u * 128u;
   static constexpr uint32_t TILE_BYTES = HALVES * HALF_BYTES;
   static constexpr int KS = 2;  // K ring stages
-  static constexpr int VS = 3;  // V ring stages
-  static constexpr int NS = 3;  // S buffers in TMEM (P_j is written over S_j)
+  // V ring stages; with two groups, tile j takes stage j % 4, so each stage
+  // serves one group (and its P V issuer) alone.
+  static constexpr int VS = NG == 1 ? 3 : 4;
+  // S buffers in TMEM: with one group P_j is written over S_j; with two, S
+  // buffer b and P buffer b (tiles j with j % 2 == b) are separate.
+  static constexpr int NS = NG == 1 ? 3 : 2;
   static constexpr uint32_t OFF_Q = 0;  // two Q buffers (consecutive items)
   static constexpr uint32_t OFF_K = OFF_Q + 2 * TILE_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + KS * TILE_BYTES;
@@ -122,8 +130,9 @@ struct TcCfg {
   // barrier indices, one per stage or buffer.  V_EMPTY(s) completes when the
   // P V product that read V stage s has finished; S_FULL(b) when Q K_j^T is
   // in S buffer b = j % NS, P_FULL(b) when the softmax warps have written
-  // P_j over it, PV_DONE(b) when P_j V_j has finished (O holds it and S
-  // buffer b is free for Q K_{j+NS}^T).
+  // P_j (over it, or into P buffer b), PV_DONE(b) when P_j V_j has finished
+  // (O holds it; with one group S buffer b is then free for Q K_{j+NS}^T,
+  // with two P buffer b is free for P_{j+2}).
   static constexpr int B_Q_FULL = 0;   // two: one per Q buffer
   static constexpr int B_Q_EMPTY = 2;  // two: the item's epilogue is done with it
   static constexpr int B_K_FULL = 4;
@@ -141,23 +150,31 @@ struct TcCfg {
   static constexpr int B_PV_GRP = B_PV_DONE + NS;
   static constexpr int B_XCH_FULL = B_PV_GRP + NG;
   static constexpr int B_XCH_DONE = B_XCH_FULL + 1;
-  static constexpr int B_DRAIN = B_XCH_DONE + 1;  // one per issuing thread
+  static constexpr int B_DRAIN = B_XCH_DONE + 1;  // one per issuing thread (three)
   // PH_FULL(b) (two groups, one item per CTA): P's second half (keys
   // 64..127) is in S buffer b, so P_j V_j may start on those keys while the
   // first half is computed.
-  static constexpr int B_PH_FULL = B_DRAIN + 2;
-  static constexpr int NUM_BARS = B_PH_FULL + NS;
+  static constexpr int B_PH_FULL = B_DRAIN + 3;
+  // S_FREE(b) (two groups): the softmax warps have read S_j out of S buffer
+  // b, so Q K_{j+2}^T may overwrite it.
+  static constexpr int B_S_FREE = B_PH_FULL + NS;
+  static constexpr int NUM_BARS = B_S_FREE + NS;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr uint32_t OFF_XCH = (OFF_MISC + 16 + 15) & ~15u;  // [128 rows][4] floats
   static constexpr uint32_t SMEM_BYTES = OFF_XCH + (NG > 1 ? 128 * 16 : 0) + 1024;  // + slack
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t TMEM_S = 0;    // buffer b at TMEM_S + 128 b
+  static constexpr uint32_t TMEM_P = 256;  // two groups: P buffer b at TMEM_P + 64 b
   static constexpr uint32_t TMEM_O = 384;  // group g's O at TMEM_O + g D
   static_assert(TMEM_O + NG * D <= TMEM_COLS, "S buffers and O accumulators exceed TMEM");
+  static_assert(NG == 1 || (TMEM_S + 128 * NS <= TMEM_P && TMEM_P + 64 * NS <= TMEM_O),
+                "S and P buffers overlap");
   static_assert(SMEM_BYTES <= 227u * 1024u, "shared memory per CTA exceeded");
   static constexpr int WARP_PV = NG == 1 ? 6 : 2;
   static constexpr int WARP_SM0 = NG == 1 ? 2 : 3;  // first softmax warp
-  static constexpr int THREADS = 32 * (WARP_SM0 + 4 * NG + (NG == 1 ? 1 : 0));
+  // two groups: the P V issuer of group 1 (one item per CTA; idle otherwise)
+  static constexpr int WARP_PV1 = NG == 1 ? -1 : WARP_SM0 + 4 * NG;
+  static constexpr int THREADS = 32 * (WARP_SM0 + 4 * NG + 1);
   static constexpr int SOFTMAX_THREADS = 128;  // one group
 };
 
@@ -479,9 +496,11 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
     for (int gr = 0; gr < NG; ++gr) mbar_init(bar(C::B_PV_GRP + gr), 1);
     mbar_init(bar(C::B_XCH_FULL), C::SOFTMAX_THREADS);
     mbar_init(bar(C::B_XCH_DONE), C::SOFTMAX_THREADS);
-    mbar_init(bar(C::B_DRAIN), 1);
-    mbar_init(bar(C::B_DRAIN + 1), 1);
-    for (int b = 0; b < C::NS; ++b) mbar_init(bar(C::B_PH_FULL + b), C::SOFTMAX_THREADS);
+    for (int i = 0; i < 3; ++i) mbar_init(bar(C::B_DRAIN + i), 1);
+    for (int b = 0; b < C::NS; ++b) {
+      mbar_init(bar(C::B_PH_FULL + b), C::SOFTMAX_THREADS);
+      mbar_init(bar(C::B_S_FREE + b), C::SOFTMAX_THREADS);
+    }
     *abort_flag = 0;
     fence_mbar_init();
     // The first item's copies need no free stage: start them before the
@@ -552,12 +571,13 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
           const int g = g0 + j;
           // S buffer g % NS is free once P_{g-NS} V_{g-NS}, which read the P
           // written over it, has finished (the softmax warps loaded S_{g-NS}
-          // before writing that P).
+          // before writing that P); with two groups, once the softmax warps
+          // have read S_{g-NS}.
           if (!mbar_wait(bar(C::B_K_FULL + g % C::KS), (g / C::KS) & 1, abort_flag,
                          args.status, wlim) ||
-              (g >= C::NS && !mbar_wait(bar(C::B_PV_DONE + g % C::NS),
-                                        ((g - C::NS) / C::NS) & 1, abort_flag, args.status,
-                                        wlim))) {
+              (g >= C::NS &&
+               !mbar_wait(bar((NG == 1 ? C::B_PV_DONE : C::B_S_FREE) + g % C::NS),
+                          ((g - C::NS) / C::NS) & 1, abort_flag, args.status, wlim))) {
             ok = false;
             break;
           }
@@ -584,15 +604,20 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
       tc_commit(bar(C::B_DRAIN));
       mbar_wait_unwind(bar(C::B_DRAIN), 0);
     }
-  } else if (warp == C::WARP_PV) {
-    // ======================= PV issuer =======================
-    if (lane == 0) {
+  } else if (warp == C::WARP_PV || warp == C::WARP_PV1) {
+    // ======================= PV issuer(s) =======================
+    // Two groups, one item per CTA: one issuing thread per group, each for
+    // the tiles j % 2 == pv of its group (its own P, V stages and
+    // accumulator).  Otherwise warp WARP_PV issues every product.
+    constexpr int NPV = kHalfP ? 2 : 1;
+    const int pv = warp == C::WARP_PV ? 0 : 1;
+    if (lane == 0 && pv < NPV) {
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
       int g0 = 0, k = first_k;
       bool ok = true;
       Item it = first;
       do {
-        for (int j = 0; j < it.n_kv; ++j) {
+        for (int j = pv; j < it.n_kv; j += NPV) {
           const int g = g0 + j;
           const int sv = g % C::VS;
           // (split P: the products on P's second half wait only for it)
@@ -604,8 +629,10 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
           }
           tc_fence_after();
           const uint32_t v_s = sbase + C::OFF_V + sv * C::TILE_BYTES;
-          // P_j lies over the second half of S_j's buffer
-          const uint32_t p_t = tmem + C::TMEM_S + 128u * (g % C::NS) + 64u;
+          // P_j lies over the second half of S_j's buffer (one group) or in P
+          // buffer g % NS (two)
+          const uint32_t p_t = NG == 1 ? tmem + C::TMEM_S + 128u * (g % C::NS) + 64u
+                                       : tmem + C::TMEM_P + 64u * (g % C::NS);
           // group j % NG's accumulator; its first product of the item
           // overwrites it (the previous item's epilogue has read it).
           const int grp = j % NG;
@@ -643,13 +670,14 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
             pv_steps(0, C::BN / 32, false);
           }
           tc_commit(bar(C::B_V_EMPTY + sv));
-          tc_commit(bar(C::B_PV_DONE + g % C::NS));
+          // (two issuers: nothing waits for PV_DONE; PV_GRP tells each group)
+          if constexpr (!kHalfP) tc_commit(bar(C::B_PV_DONE + g % C::NS));
           if constexpr (NG > 1) tc_commit(bar(C::B_PV_GRP + grp));
         }
         g0 += it.n_kv;
       } while (ok && next_item(k, it));
-      tc_commit(bar(C::B_DRAIN + 1));
-      mbar_wait_unwind(bar(C::B_DRAIN + 1), 0);
+      tc_commit(bar(C::B_DRAIN + 1 + pv));
+      mbar_wait_unwind(bar(C::B_DRAIN + 1 + pv), 0);
     }
   } else {
     // ======================= softmax / epilogue =======================
@@ -702,8 +730,10 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
         const bool masked = (args.causal && j0 + j == mb) || kbase + C::BN > L || win_edge;
         float tmax, m_new, m_use;
         // p = 2^(sigma - m_use), rounded to bf16 over the second half of S's
-        // buffer (its scores are in registers), from where P_j V_j reads it.
-        const uint32_t p_t = s_t + 64u;
+        // buffer (its scores are in registers) or, with two groups, into P
+        // buffer sb, from where P_j V_j reads it.
+        const uint32_t p_t =
+            NG == 1 ? s_t + 64u : tmem + lane_off + C::TMEM_P + 64u * static_cast<uint32_t>(sb);
         const bool p_ok = !kDebugChecks || __all_sync(0xffffffffu, tmem_ok(p_t, 32u, 64u));
         // Four packed sum chains keep the additions off each other's latency.
         float2 a[4];
@@ -804,10 +834,9 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
         } else {
           // Two softmax groups share the registers of 352 threads, so the
           // tile is taken in 64-key halves: both halves' maxima first, then
-          // the weights of keys 64..127 from registers (their P goes over S
-          // columns 96..127, whose scores are in registers), then keys 0..63
-          // reloaded from the first half of the buffer, which P never
-          // covers (their P over columns 64..95).
+          // the weights of keys 64..127 from registers, then keys 0..63
+          // reloaded from S, after which S buffer sb is released.  P goes to
+          // P buffer sb (keys 64..127 in its columns 32..63).
           const bool s_in = !kDebugChecks || __all_sync(0xffffffffu, tmem_ok(s_t, 32u, 128u));
           int lim = C::BN, lo = -1;  // the row's visible keys of the tile: [lo, lim)
           if (masked) {
@@ -861,9 +890,22 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
           m_new = (mx > m + kRescaleLog2) ? mx : m;  // also moves off -inf
           m_use = (m_new == -INFINITY) ? 0.f : m_new;
           const float2 cc = make_float2(c, c), nm = make_float2(-m_use, -m_use);
-          // With P split, the group's previous P V product is confirmed here
-          // (see below) and O is rescaled now, before P_j V_j can start on
-          // P's second half.
+          auto exp_half = [&](const float (&x)[64], uint32_t (&pk)[32]) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float2 xv = __ffma2_rn(make_float2(x[2 * i], x[2 * i + 1]), cc, nm);
+              const float2 p = make_float2(ex2_approx(xv.x), ex2_approx(xv.y));
+              a[i & 3] = __fadd2_rn(a[i & 3], p);
+              pk[i] = pack_bf16x2(p.x, p.y);
+            }
+          };
+          uint32_t pk[32];
+          exp_half(th, pk);
+          // P buffer sb last held P_{g-2}, whose product must have read it.
+          // One item per CTA: that is the group's previous product, confirmed
+          // here (see below), and O is rescaled now, before P_j V_j can start
+          // on P's second half.  Persistent CTAs: the tile two steps back may
+          // be the other group's, so the buffer's own barrier.
           if (kHalfP && j >= NG) {
             const bool w2 = mbar_wait(bar(C::B_PV_GRP + grp), (pvn - 1) & 1, abort_flag,
                                       args.status, wlim);
@@ -886,26 +928,28 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
                 tmem_st32(o_t + c0, ov);
               }
             }
-          }
-          auto exp_half = [&](const float (&x)[64], uint32_t dst) {
-            uint32_t pk[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float2 xv = __ffma2_rn(make_float2(x[2 * i], x[2 * i + 1]), cc, nm);
-              const float2 p = make_float2(ex2_approx(xv.x), ex2_approx(xv.y));
-              a[i & 3] = __fadd2_rn(a[i & 3], p);
-              pk[i] = pack_bf16x2(p.x, p.y);
+          } else if (!kHalfP && g >= C::NS) {
+            const bool w2 = mbar_wait(bar(C::B_PV_DONE + sb), ((g - C::NS) / C::NS) & 1,
+                                      abort_flag, args.status, wlim);
+            if (__any_sync(0xffffffffu, !w2)) {
+              ok = false;
+              break;
             }
-            if (p_ok) tmem_st32(dst, pk);
-          };
-          exp_half(th, p_t + 32u);
+          }
+          tc_fence_after();
+          if (p_ok) tmem_st32(p_t + 32u, pk);
           if constexpr (kHalfP) {
             tmem_st_wait();  // (also the rescaled O)
             tc_fence_before();
             mbar_arrive(bar(C::B_PH_FULL + sb));
           }
           load_half(0, th);
-          exp_half(th, p_t);
+          // S_j has been read (the load waited for its data): the buffer is
+          // free for Q K_{j+2}^T.
+          tc_fence_before();
+          mbar_arrive(bar(C::B_S_FREE + sb));
+          exp_half(th, pk);
+          if (p_ok) tmem_st32(p_t, pk);
         }
         const float alpha = (m_new == m) ? 1.f : ex2_approx(m - m_use);
         const float2 aa = __fadd2_rn(__fadd2_rn(a[0], a[1]), __fadd2_rn(a[2], a[3]));
