@@ -117,11 +117,12 @@ struct TcCfg {
   static constexpr uint32_t HALF_BYTES = 128u * 128u;
   static constexpr uint32_t TILE_BYTES = HALVES * HALF_BYTES;
   static constexpr int KS = 2;  // K ring stages
-  // V ring stages; with two groups, tile j takes stage j % 4, so each stage
-  // serves one group (and its P V issuer) alone.
+  // V ring stages; with two groups, each group has two of them (its c-th
+  // tile takes stage 2 g + c % 2), so a stage serves one group (and its P V
+  // issuer) alone.
   static constexpr int VS = NG == 1 ? 3 : 4;
-  // S buffers in TMEM: with one group P_j is written over S_j; with two, S
-  // buffer b and P buffer b (tiles j with j % 2 == b) are separate.
+  // S buffers in TMEM: with one group P_j is written over S_j; with two,
+  // group g has S buffer g and P buffer g (separate) for its tiles.
   static constexpr int NS = NG == 1 ? 3 : 2;
   static constexpr uint32_t OFF_Q = 0;  // two Q buffers (consecutive items)
   static constexpr uint32_t OFF_K = OFF_Q + 2 * TILE_BYTES;
@@ -129,10 +130,10 @@ struct TcCfg {
   static constexpr uint32_t OFF_BAR = OFF_V + VS * TILE_BYTES;
   // barrier indices, one per stage or buffer.  V_EMPTY(s) completes when the
   // P V product that read V stage s has finished; S_FULL(b) when Q K_j^T is
-  // in S buffer b = j % NS, P_FULL(b) when the softmax warps have written
-  // P_j (over it, or into P buffer b), PV_DONE(b) when P_j V_j has finished
-  // (O holds it; with one group S buffer b is then free for Q K_{j+NS}^T,
-  // with two P buffer b is free for P_{j+2}).
+  // in S buffer b (j % NS; with two groups the tile's group), P_FULL(b) when
+  // the softmax warps have written P_j (over it, or into P buffer b),
+  // PV_DONE(b) (one group) when P_j V_j has finished: O holds it and S
+  // buffer b is free for Q K_{j+NS}^T.
   static constexpr int B_Q_FULL = 0;   // two: one per Q buffer
   static constexpr int B_Q_EMPTY = 2;  // two: the item's epilogue is done with it
   static constexpr int B_K_FULL = 4;
@@ -172,7 +173,7 @@ struct TcCfg {
   static_assert(SMEM_BYTES <= 227u * 1024u, "shared memory per CTA exceeded");
   static constexpr int WARP_PV = NG == 1 ? 6 : 2;
   static constexpr int WARP_SM0 = NG == 1 ? 2 : 3;  // first softmax warp
-  // two groups: the P V issuer of group 1 (one item per CTA; idle otherwise)
+  // two groups: the P V issuer of group 1 (WARP_PV issues group 0's)
   static constexpr int WARP_PV1 = NG == 1 ? -1 : WARP_SM0 + 4 * NG;
   static constexpr int THREADS = 32 * (WARP_SM0 + 4 * NG + 1);
   static constexpr int SOFTMAX_THREADS = 128;  // one group
@@ -293,7 +294,7 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
   auto item_at = [&](int k, Item& it) -> bool {
     // (32-bit unsigned divisions: num_items fits in an int, and the 64-bit
     // ones cost several hundred cycles at every item change)
-    int mb, bh;
+    int mb = 0, bh = 0;
     if constexpr (PERSIST) {
       const unsigned P = gridDim.x;
       const unsigned c = blockIdx.x;
@@ -407,20 +408,30 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
 
   // ---- producer state (thread 0) ----
   // Loads are numbered per CTA across items: the K and V tiles of the g-th
-  // KV step of the CTA go to ring stages g % KS and g % VS, the Q tile of the
+  // KV step of the CTA go to ring stages g % KS and g % VS (with two groups
+  // the c-th V tile of group gr to stage 2 gr + c % 2), the Q tile of the
   // t-th item to buffer t % 2.
-  int k_issued = 0, v_issued = 0, q_issued = 0;
+  int k_issued = 0, q_issued = 0;
+  int v_cnt0 = 0, v_cnt1 = 0;  // V tiles loaded for group 0 / 1 (two groups)
+  uint32_t v_used = 0, v_par = 0;  // bit s: V stage s loaded; the parity of its last load
   uint32_t k_skipped = 0;  // bit s: stage s's last request was left out (fault injection)
   // The tile of KV step j of item `it` (global step g) into its ring, once
   // the product that read the stage's previous tile has finished.
   auto load_kv = [&](bool is_v, const Item& it, int j, int g) -> bool {
     const int S = is_v ? C::VS : C::KS;
-    const int st = g % S;
-    if (g >= S && !mbar_wait(bar((is_v ? C::B_V_EMPTY : C::B_K_EMPTY) + st), ((g / S) - 1) & 1,
+    int st = g % S, n = g / S;  // stage, and this load's index among the stage's loads
+    if (NG == 2 && is_v) {
+      const int gr = j & 1;
+      const int c = gr ? v_cnt1++ : v_cnt0++;
+      st = 2 * gr + (c & 1);
+      n = c >> 1;
+    }
+    if (n >= 1 && !mbar_wait(bar((is_v ? C::B_V_EMPTY : C::B_K_EMPTY) + st), (n - 1) & 1,
                              abort_flag, args.status, wlim))
       return false;
     if (is_v) {
-      v_issued = g + 1;
+      v_used |= 1u << st;
+      v_par = (v_par & ~(1u << st)) | (static_cast<uint32_t>(n & 1) << st);
     } else {
       k_issued = g + 1;
       // Fault injection (tests of the timeout path only): this key tile is
@@ -544,16 +555,16 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
       } while (ok && next_item(k, it));
       if (*abort_flag) {
         // Let every copy this thread started land before the CTA exits.
-        // Copies before the last two Q tiles and the last KS (VS) K (V)
-        // tiles were waited for by the products that freed their buffers
-        // for the later ones.
+        // Copies before the last two Q tiles, the last KS K tiles and the
+        // last V tile of each stage were waited for by the products that
+        // freed their buffers for the later ones.
         for (int i = max(0, q_issued - 2); i < q_issued; ++i)
           mbar_wait_unwind(bar(C::B_Q_FULL + (i & 1)), (i >> 1) & 1);
         for (int g = max(0, k_issued - C::KS); g < k_issued; ++g)
           if (!((k_skipped >> (g % C::KS)) & 1u))  // never requested: nothing in flight
             mbar_wait_unwind(bar(C::B_K_FULL + g % C::KS), (g / C::KS) & 1);
-        for (int g = max(0, v_issued - C::VS); g < v_issued; ++g)
-          mbar_wait_unwind(bar(C::B_V_FULL + g % C::VS), (g / C::VS) & 1);
+        for (int st = 0; st < C::VS; ++st)
+          if ((v_used >> st) & 1u) mbar_wait_unwind(bar(C::B_V_FULL + st), (v_par >> st) & 1u);
       }
     }
   } else if (warp == 1) {
@@ -561,6 +572,7 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
       int g0 = 0, ti = 0, k = first_k;
+      int qc0 = 0, qc1 = 0;  // S products issued for group 0 / 1 (two groups)
       bool ok = true;
       Item it = first;
       do {
@@ -571,19 +583,23 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
           const int g = g0 + j;
           // S buffer g % NS is free once P_{g-NS} V_{g-NS}, which read the P
           // written over it, has finished (the softmax warps loaded S_{g-NS}
-          // before writing that P); with two groups, once the softmax warps
-          // have read S_{g-NS}.
+          // before writing that P).  Two groups: the tile's group's buffer,
+          // once that group has read its previous S.
+          int sb = g % C::NS, sn = g / C::NS;  // buffer; this product's index among its products
+          if constexpr (NG == 2) {
+            sb = j & 1;
+            sn = sb ? qc1++ : qc0++;
+          }
           if (!mbar_wait(bar(C::B_K_FULL + g % C::KS), (g / C::KS) & 1, abort_flag,
                          args.status, wlim) ||
-              (g >= C::NS &&
-               !mbar_wait(bar((NG == 1 ? C::B_PV_DONE : C::B_S_FREE) + g % C::NS),
-                          ((g - C::NS) / C::NS) & 1, abort_flag, args.status, wlim))) {
+              (sn >= 1 && !mbar_wait(bar((NG == 1 ? C::B_PV_DONE : C::B_S_FREE) + sb),
+                                     (sn - 1) & 1, abort_flag, args.status, wlim))) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t k_s = sbase + C::OFF_K + (g % C::KS) * C::TILE_BYTES;
-          const uint32_t s_t = tmem + C::TMEM_S + 128u * (g % C::NS);
+          const uint32_t s_t = tmem + C::TMEM_S + 128u * sb;
           const bool in_range = smem_ok(q_s, C::TILE_BYTES) && smem_ok(k_s, C::TILE_BYTES) &&
                                 tmem_ok(s_t, 128u, 128u);
 #pragma unroll
@@ -594,7 +610,7 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
             tc_mma_ss(s_t, sdesc_sw128(q_s + off, 16u, 1024u),
                       sdesc_sw128(k_s + off, 16u, 1024u), idesc_qk, kk > 0 ? 1u : 0u);
           }
-          tc_commit(bar(C::B_S_FULL + g % C::NS));
+          tc_commit(bar(C::B_S_FULL + sb));
           tc_commit(bar(C::B_K_EMPTY + g % C::KS));
         }
         g0 += it.n_kv;
@@ -606,33 +622,42 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
     }
   } else if (warp == C::WARP_PV || warp == C::WARP_PV1) {
     // ======================= PV issuer(s) =======================
-    // Two groups, one item per CTA: one issuing thread per group, each for
-    // the tiles j % 2 == pv of its group (its own P, V stages and
-    // accumulator).  Otherwise warp WARP_PV issues every product.
-    constexpr int NPV = kHalfP ? 2 : 1;
+    // Two groups: one issuing thread per group, each for the tiles j % 2 ==
+    // pv of its group (its own P buffer, V stages and accumulator).  One
+    // group: warp WARP_PV issues every product.
+    constexpr int NPV = NG;
     const int pv = warp == C::WARP_PV ? 0 : 1;
     if (lane == 0 && pv < NPV) {
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
       int g0 = 0, k = first_k;
+      int pc = 0;  // products of this issuer so far (two groups)
       bool ok = true;
       Item it = first;
       do {
         for (int j = pv; j < it.n_kv; j += NPV) {
           const int g = g0 + j;
-          const int sv = g % C::VS;
+          // P buffer and V stage, and this tile's index among their tiles
+          int pb = g % C::NS, pn = g / C::NS, sv = g % C::VS, vn = g / C::VS;
+          if constexpr (NG == 2) {
+            pb = pv;
+            pn = pc;
+            sv = 2 * pv + (pc & 1);
+            vn = pc >> 1;
+            ++pc;
+          }
           // (split P: the products on P's second half wait only for it)
-          if (!mbar_wait(bar((kHalfP ? C::B_PH_FULL : C::B_P_FULL) + g % C::NS), (g / C::NS) & 1,
-                         abort_flag, args.status, wlim) ||
-              !mbar_wait(bar(C::B_V_FULL + sv), (g / C::VS) & 1, abort_flag, args.status, wlim)) {
+          if (!mbar_wait(bar((kHalfP ? C::B_PH_FULL : C::B_P_FULL) + pb), pn & 1, abort_flag,
+                         args.status, wlim) ||
+              !mbar_wait(bar(C::B_V_FULL + sv), vn & 1, abort_flag, args.status, wlim)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t v_s = sbase + C::OFF_V + sv * C::TILE_BYTES;
-          // P_j lies over the second half of S_j's buffer (one group) or in P
-          // buffer g % NS (two)
-          const uint32_t p_t = NG == 1 ? tmem + C::TMEM_S + 128u * (g % C::NS) + 64u
-                                       : tmem + C::TMEM_P + 64u * (g % C::NS);
+          // P_j lies over the second half of S_j's buffer (one group) or in the
+          // group's P buffer (two)
+          const uint32_t p_t = NG == 1 ? tmem + C::TMEM_S + 128u * pb + 64u
+                                       : tmem + C::TMEM_P + 64u * pb;
           // group j % NG's accumulator; its first product of the item
           // overwrites it (the previous item's epilogue has read it).
           const int grp = j % NG;
@@ -661,8 +686,7 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
             pv_steps(0, C::BN / 32, false);
           } else {
             pv_steps(C::BN / 32, C::BN / 16, true);
-            if (!mbar_wait(bar(C::B_P_FULL + g % C::NS), (g / C::NS) & 1, abort_flag, args.status,
-                           wlim)) {
+            if (!mbar_wait(bar(C::B_P_FULL + pb), pn & 1, abort_flag, args.status, wlim)) {
               ok = false;
               break;
             }
@@ -670,8 +694,8 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
             pv_steps(0, C::BN / 32, false);
           }
           tc_commit(bar(C::B_V_EMPTY + sv));
-          // (two issuers: nothing waits for PV_DONE; PV_GRP tells each group)
-          if constexpr (!kHalfP) tc_commit(bar(C::B_PV_DONE + g % C::NS));
+          // (two groups: nothing waits for PV_DONE; PV_GRP tells each group)
+          if constexpr (NG == 1) tc_commit(bar(C::B_PV_DONE + pb));
           if constexpr (NG > 1) tc_commit(bar(C::B_PV_GRP + grp));
         }
         g0 += it.n_kv;
@@ -715,10 +739,11 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
 
       for (int j = grp; j < n_kv; j += NG) {
         const int g = g0 + j;
-        const int sb = g % C::NS;
+        // S buffer (two groups: the group's own, its pvn-th S)
+        const int sb = NG == 1 ? g % C::NS : grp;
         const uint32_t s_t = tmem + lane_off + C::TMEM_S + 128u * sb;
-        const bool w = mbar_wait(bar(C::B_S_FULL + sb), (g / C::NS) & 1, abort_flag,
-                                 args.status, wlim);
+        const bool w = mbar_wait(bar(C::B_S_FULL + sb), (NG == 1 ? g / C::NS : pvn) & 1,
+                                 abort_flag, args.status, wlim);
         if (__any_sync(0xffffffffu, !w)) {
           ok = false;
           break;
@@ -901,11 +926,11 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
           };
           uint32_t pk[32];
           exp_half(th, pk);
-          // P buffer sb last held P_{g-2}, whose product must have read it.
-          // One item per CTA: that is the group's previous product, confirmed
-          // here (see below), and O is rescaled now, before P_j V_j can start
-          // on P's second half.  Persistent CTAs: the tile two steps back may
-          // be the other group's, so the buffer's own barrier.
+          // The group's P buffer holds its previous P, whose product must
+          // have read it: that product is confirmed here (within the item;
+          // the item's epilogue confirmed the last one of the previous item),
+          // and with P split O is rescaled now, before P_j V_j can start on
+          // P's second half.
           if (kHalfP && j >= NG) {
             const bool w2 = mbar_wait(bar(C::B_PV_GRP + grp), (pvn - 1) & 1, abort_flag,
                                       args.status, wlim);
@@ -928,9 +953,9 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
                 tmem_st32(o_t + c0, ov);
               }
             }
-          } else if (!kHalfP && g >= C::NS) {
-            const bool w2 = mbar_wait(bar(C::B_PV_DONE + sb), ((g - C::NS) / C::NS) & 1,
-                                      abort_flag, args.status, wlim);
+          } else if (!kHalfP && j >= NG) {
+            const bool w2 = mbar_wait(bar(C::B_PV_GRP + grp), (pvn - 1) & 1, abort_flag,
+                                      args.status, wlim);
             if (__any_sync(0xffffffffu, !w2)) {
               ok = false;
               break;
@@ -961,20 +986,6 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
         dsum = dsum * alpha + (aa.x + aa.y);
         m = m_new;
 
-        if constexpr (NG > 1 && !kHalfP) {
-          // A group confirms its previous P V product at every tile, before
-          // it signals the next one: PV_GRP(grp) then never runs more than
-          // one phase ahead of the phase a wait names (a parity wait is only
-          // sound under that bound).
-          if (j >= NG) {
-            const bool w2 = mbar_wait(bar(C::B_PV_GRP + grp), (pvn - 1) & 1, abort_flag,
-                                      args.status, wlim);
-            if (__any_sync(0xffffffffu, !w2)) {
-              ok = false;
-              break;
-            }
-          }
-        }
         if (!kHalfP && j >= NG && __any_sync(0xffffffffu, alpha != 1.f)) {
           // o <- alpha * o between the group's previous P V product and
           // P_j V_j (rare: only when a row of this warp moved its reference
