@@ -715,7 +715,8 @@ def run_profile_case(args):
     (B=64, H=32 over H_kv=8, pages of 64, 4.7 GB of KV); scan = prefix
     attention over the decode workload's caches; scan_small = the same on
     its first 8 sequences with every row cut into 4 chunks (about 2.2 GB of
-    caches and 1.1 GB of output, 1024 CTAs); decode = split-KV decode on the
+    caches and 1.1 GB of output, 1024 CTAs); varlen64 = the packed causal
+    prefill of 65536 tokens, H=16, D=64 (201 MB of inputs); decode = split-KV decode on the
     first 8 sequences of the decode workload (about 2.2 GB of KV cache, larger than L2, small enough for a
     multi-pass capture)."""
     import exact_io_aware_15_gb300 as fa
@@ -727,6 +728,10 @@ def run_profile_case(args):
         o = torch.empty_like(c.q)
         lse = torch.empty((P["B"], P["H"], P["N"]), dtype=torch.float32, device="cuda")
         run = lambda: fa.fa_fwd(c.q, c.k, c.v, c.scale, True, o=o, lse=lse)
+    elif args.profile_case == "varlen64":
+        c5 = inp.config5(64, device="cuda")
+        cu = c5.cu_seqlens.cuda()
+        run = lambda: fa.fa_fwd_varlen(c5.q, c5.k, c5.v, cu, c5.max_seqlen, c5.scale, True)
     elif args.profile_case == "bwd":
         P = PREFILL
         c = inp.dense(P["B"], P["H"], P["N"], P["D"], seed=5, causal=True, device="cuda")
@@ -797,7 +802,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-other-configs", action="store_true")
     ap.add_argument("--profile-case", choices=["prefill", "decode", "bwd", "rowstats", "paged",
-                                                "scan", "scan_small", "combine"],
+                                                "scan", "scan_small", "combine", "varlen64"],
                     default=None)
     args = ap.parse_args(argv)
     if args.profile_case:
