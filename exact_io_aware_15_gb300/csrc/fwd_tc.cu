@@ -172,10 +172,20 @@ struct TcCfg {
                 "S and P buffers overlap");
   static_assert(SMEM_BYTES <= 227u * 1024u, "shared memory per CTA exceeded");
   static constexpr int WARP_PV = NG == 1 ? 6 : 2;
-  static constexpr int WARP_SM0 = NG == 1 ? 2 : 3;  // first softmax warp
+  static constexpr int WARP_SM0 = NG == 1 ? 2 : 4;  // first softmax warp
   // two groups: the P V issuer of group 1 (WARP_PV issues group 0's)
-  static constexpr int WARP_PV1 = NG == 1 ? -1 : WARP_SM0 + 4 * NG;
-  static constexpr int THREADS = 32 * (WARP_SM0 + 4 * NG + 1);
+  static constexpr int WARP_PV1 = NG == 1 ? -1 : 3;
+  static constexpr int THREADS = 32 * (NG == 1 ? 7 : 12);
+  // Two groups: the issuing warps 0..3 form one warpgroup, the softmax groups
+  // the other two.  A thread starts with REGS_LAUNCH registers (the most 384
+  // threads can have); the issuing warpgroup then gives registers to the
+  // softmax warpgroups, which hold a tile's 128 scores at once.  The split
+  // may not exceed the CTA's pool, or the raise would wait forever; the
+  // launcher checks that the compiled kernel starts with REGS_LAUNCH.
+  static constexpr int REGS_LAUNCH = 168, REGS_ISSUE = 88, REGS_SOFTMAX = 200;
+  static_assert(NG == 1 || (65536 / THREADS) / 8 * 8 == REGS_LAUNCH, "registers at launch");
+  static_assert(NG == 1 || 128 * REGS_ISSUE + 256 * REGS_SOFTMAX <= THREADS * REGS_LAUNCH,
+                "register split exceeds the CTA's pool");
   static constexpr int SOFTMAX_THREADS = 128;  // one group
 };
 
@@ -535,6 +545,12 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
                      args.status);
   };
 
+  // The issuing warps (producer, QK issuer, P V issuers) and the softmax
+  // warps; with two groups the former are one warpgroup, which gives
+  // registers to the latter.
+  const bool issuing = NG == 1 ? (warp < C::WARP_SM0 || warp == C::WARP_PV) : warp < 4;
+  if (issuing) {
+  if constexpr (NG == 2) regs_release<C::REGS_ISSUE>();
   if (warp == 0) {
     // ======================= TMA producer =======================
     if (lane == 0) {
@@ -703,7 +719,9 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
       tc_commit(bar(C::B_DRAIN + 1 + pv));
       mbar_wait_unwind(bar(C::B_DRAIN + 1 + pv), 0);
     }
+  }
   } else {
+    if constexpr (NG == 2) regs_acquire<C::REGS_SOFTMAX>();
     // ======================= softmax / epilogue =======================
     // Group grp of NG folds the key tiles j with j % NG == grp; warp w reads
     // TMEM lanes 32 (w % 4) ... + 31 (every group covers all 128 rows).
@@ -857,55 +875,47 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
             tile_exp(m_use);
           }
         } else {
-          // Two softmax groups share the registers of 352 threads, so the
-          // tile is taken in 64-key halves: both halves' maxima first, then
-          // the weights of keys 64..127 from registers, then keys 0..63
-          // reloaded from S, after which S buffer sb is released.  P goes to
-          // P buffer sb (keys 64..127 in its columns 32..63).
+          // The issuing warpgroup gave the softmax warps the registers to
+          // hold a tile's 128 scores: one read of S, after which S buffer sb
+          // is released for Q K_{j+2}^T, then the row maximum, then the
+          // weights of keys 64..127 (into columns 32..63 of P buffer sb) and
+          // of keys 0..63.
           const bool s_in = !kDebugChecks || __all_sync(0xffffffffu, tmem_ok(s_t, 32u, 128u));
-          int lim = C::BN, lo = -1;  // the row's visible keys of the tile: [lo, lim)
-          if (masked) {
-            lim = L - kbase;
-            if (args.causal) lim = min(lim, qpos - kbase + 1);
-            if (window > 0) lo = qpos - window + 1 - kbase;
-          }
-          auto load_half = [&](int hh, float (&x)[64]) {
+          float t[128];
+          if (s_in) {
             uint32_t raw[64];
-            if (s_in) {
-              tmem_ld64(s_t + 64u * hh, raw);
-            } else {
+            tmem_ld64(s_t, raw);
 #pragma unroll
-              for (int i = 0; i < 64; ++i) raw[i] = 0u;
-            }
+            for (int i = 0; i < 64; ++i) t[i] = __uint_as_float(raw[i]);
+            tmem_ld64(s_t + 64u, raw);
 #pragma unroll
-            for (int i = 0; i < 64; ++i) x[i] = __uint_as_float(raw[i]);
-            if (masked) {
+            for (int i = 0; i < 64; ++i) t[64 + i] = __uint_as_float(raw[i]);
+          } else {
 #pragma unroll
-              for (int i = 0; i < 64; ++i)
-                if (64 * hh + i >= lim || 64 * hh + i < lo) x[i] = -INFINITY;
-            }
-            if (zero_scale) {
-#pragma unroll
-              for (int i = 0; i < 64; ++i) x[i] = (x[i] == -INFINITY) ? -INFINITY : 0.f;
-            }
-          };
-          float th[64];
-          float q[16];
-          load_half(0, th);
-#pragma unroll
-          for (int kq = 0; kq < 8; ++kq) {
-            q[kq] = fmax3(th[8 * kq], th[8 * kq + 1], th[8 * kq + 2]);
-            q[kq] = fmax3(q[kq], th[8 * kq + 3], th[8 * kq + 4]);
-            q[kq] = fmax3(q[kq], th[8 * kq + 5], th[8 * kq + 6]);
-            q[kq] = fmaxf(q[kq], th[8 * kq + 7]);
+            for (int i = 0; i < 128; ++i) t[i] = 0.f;
           }
-          load_half(1, th);  // keys 64..127, kept
+          // S_j has been read (the loads waited for their data).
+          tc_fence_before();
+          mbar_arrive(bar(C::B_S_FREE + sb));
+          if (masked) {
+            int lim = L - kbase;  // the row's visible keys of the tile: [lo, lim)
+            if (args.causal) lim = min(lim, qpos - kbase + 1);
+            const int lo = window > 0 ? qpos - window + 1 - kbase : -1;
 #pragma unroll
-          for (int kq = 0; kq < 8; ++kq) {
-            q[8 + kq] = fmax3(th[8 * kq], th[8 * kq + 1], th[8 * kq + 2]);
-            q[8 + kq] = fmax3(q[8 + kq], th[8 * kq + 3], th[8 * kq + 4]);
-            q[8 + kq] = fmax3(q[8 + kq], th[8 * kq + 5], th[8 * kq + 6]);
-            q[8 + kq] = fmaxf(q[8 + kq], th[8 * kq + 7]);
+            for (int i = 0; i < 128; ++i)
+              if (i >= lim || i < lo) t[i] = -INFINITY;
+          }
+          if (zero_scale) {
+#pragma unroll
+            for (int i = 0; i < 128; ++i) t[i] = (t[i] == -INFINITY) ? -INFINITY : 0.f;
+          }
+          float q[16];
+#pragma unroll
+          for (int kq = 0; kq < 16; ++kq) {
+            q[kq] = fmax3(t[8 * kq], t[8 * kq + 1], t[8 * kq + 2]);
+            q[kq] = fmax3(q[kq], t[8 * kq + 3], t[8 * kq + 4]);
+            q[kq] = fmax3(q[kq], t[8 * kq + 5], t[8 * kq + 6]);
+            q[kq] = fmaxf(q[kq], t[8 * kq + 7]);
           }
           const float r0 = fmax3(q[0], q[1], q[2]), r1 = fmax3(q[3], q[4], q[5]);
           const float r2 = fmax3(q[6], q[7], q[8]), r3 = fmax3(q[9], q[10], q[11]);
@@ -915,17 +925,19 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
           m_new = (mx > m + kRescaleLog2) ? mx : m;  // also moves off -inf
           m_use = (m_new == -INFINITY) ? 0.f : m_new;
           const float2 cc = make_float2(c, c), nm = make_float2(-m_use, -m_use);
-          auto exp_half = [&](const float (&x)[64], uint32_t (&pk)[32]) {
+          // keys base .. base + 63 (pair i into a[i % 4])
+          auto exp_half = [&](int base, uint32_t (&pk)[32]) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              const float2 xv = __ffma2_rn(make_float2(x[2 * i], x[2 * i + 1]), cc, nm);
+              const float2 xv =
+                  __ffma2_rn(make_float2(t[base + 2 * i], t[base + 2 * i + 1]), cc, nm);
               const float2 p = make_float2(ex2_approx(xv.x), ex2_approx(xv.y));
               a[i & 3] = __fadd2_rn(a[i & 3], p);
               pk[i] = pack_bf16x2(p.x, p.y);
             }
           };
           uint32_t pk[32];
-          exp_half(th, pk);
+          exp_half(64, pk);
           // The group's P buffer holds its previous P, whose product must
           // have read it: that product is confirmed here (within the item;
           // the item's epilogue confirmed the last one of the previous item),
@@ -968,12 +980,7 @@ __global__ void __launch_bounds__(TcCfg<D, NG>::THREADS, 1)
             tc_fence_before();
             mbar_arrive(bar(C::B_PH_FULL + sb));
           }
-          load_half(0, th);
-          // S_j has been read (the load waited for its data): the buffer is
-          // free for Q K_{j+2}^T.
-          tc_fence_before();
-          mbar_arrive(bar(C::B_S_FREE + sb));
-          exp_half(th, pk);
+          exp_half(0, pk);
           if (p_ok) tmem_st32(p_t, pk);
         }
         const float alpha = (m_new == m) ? 1.f : ex2_approx(m - m_use);
@@ -1294,6 +1301,14 @@ static cudaError_t launch_tc_impl(const TcMaps& maps, const TcFwdArgs& a, int gr
       e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(C::SMEM_BYTES));
       if (e != cudaSuccess) return e;
+      if constexpr (NG == 2) {
+        // The warpgroups' register split adds up only if a thread starts
+        // with REGS_LAUNCH registers: refuse any other build of the kernel.
+        cudaFuncAttributes fattr{};
+        e = cudaFuncGetAttributes(&fattr, f);
+        if (e != cudaSuccess) return e;
+        if (fattr.numRegs != C::REGS_LAUNCH) return cudaErrorInvalidKernelImage;
+      }
     }
     if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_release);
   }
