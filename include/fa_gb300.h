@@ -57,7 +57,10 @@ extern "C" {
 #define FA_OK                    0
 #define FA_ERR_INVALID_ARG      -1  /* NULL / misaligned pointer, bad size, bad dtype */
 #define FA_ERR_UNSUPPORTED_ARCH -2  /* current device is not sm_103 */
-#define FA_ERR_LAUNCH           -3  /* the CUDA launch itself failed */
+#define FA_ERR_LAUNCH           -3  /* the CUDA launch itself failed; also a D = 64 forward whose
+                                       kernel image does not start with the 168 registers per
+                                       thread its warpgroup register split assumes
+                                       (cudaErrorInvalidKernelImage in fa_last_cuda_error) */
 #define FA_ERR_DEVICE_TIMEOUT   -4  /* a device-side pipeline wait ran past its limit */
 #define FA_ERR_DEVICE_BOUNDS    -5  /* a device-side index check failed */
 #define FA_ERR_DRIVER           -6  /* CUDA driver entry point or tensor-map encoding failed */
