@@ -94,9 +94,9 @@ constexpr float kRescaleLog2 = 32.f;
 
 // Sequences of at most this many 128-row query tiles run on persistent CTAs
 // (measured crossovers: at D = 128 the one-item kernel, which computes weights
-// before the maximum, wins from 32 tiles on; at D = 64, where its groups
-// start P V on half of P and have one issuing thread each, from 24 tiles on).
-constexpr int persistent_max_tiles(int D) { return D == 128 ? 28 : 16; }
+// before the maximum, wins from 24 tiles on; at D = 64, where its groups
+// start P V on half of P and have one issuing thread each, from 20 tiles on).
+constexpr int persistent_max_tiles(int D) { return D == 128 ? 20 : 16; }
 
 // Softmax warpgroups per CTA at D = 64 (at D = 128 tensor memory holds one O).
 constexpr int kSoftmaxGroups64 = 2;
